@@ -1,0 +1,419 @@
+"""Benchmark: exact attention forward + backward on one GB300 (or N replicas).
+
+One step = one forward and one backward over one batch of the workload
+(inputs resident in HBM), through the library's C ABI. Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl fa|reference] [--no-cpu-baseline]
+
+Default workload: the GPT-2-small-shaped causal attention (B=8 H=12 N=1024
+d=64, bf16). Metric: TFLOP/s with FLOPs = 4*B*H*N^2*d for the forward and
+2.5x that for the backward, halved for causal and scaled by the block
+density for block-sparse masks (the literal formula; key padding counts the
+dense N^2). For N > 1 GPUs (torchrun), every rank runs the same workload on
+its own GPU with no collective on the data path (independent heads/batches:
+weak scaling); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd / fwd+bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# FLOP and byte models
+# ---------------------------------------------------------------------------
+
+def density_of(inp, w):
+    if inp.get("block_mask") is None:
+        return 1.0
+    return float(inp["block_mask"].double().mean())
+
+
+def flops(w, density=1.0):
+    f = 4.0 * w.B * w.H * w.N * w.N * w.d
+    if w.causal:
+        f *= 0.5
+    f *= density
+    return f, 2.5 * f
+
+
+def algorithmic_bytes(w):
+    """Forward: read Q, K, V, write O (elements) + write LSE (fp32).
+    Backward: read Q, K, V, O, dO, LSE; write dQ, dK, dV."""
+    e = 2 if w.dtype == "bf16" else 4
+    bhnd = w.B * w.H * w.N * w.d
+    bhn = w.B * w.H * w.N
+    return 4 * bhnd * e + 4 * bhn, 8 * bhnd * e + 8 * bhn
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return dict(bf16=float(pk["bf16_tflops"]), bf16_sustained=float(pk.get("bf16_tflops_sustained", 0) or 0),
+                    hbm=float(pk["hbm_gbs"]), source="measured")
+    except Exception:
+        return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# Distributed helpers (torchrun); N == 1 runs without a process group.
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value, device=None):
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample of heads
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, inp, budget_s=12.0, backward=True):
+    """Times the fp64 oracle on whole heads of the workload (fwd+bwd)."""
+    import oracle
+    total_heads = w.B * w.H
+    fwd_f, bwd_f = flops(w, density_of(inp, w))
+    per_head = (fwd_f + (bwd_f if backward else 0.0)) / total_heads
+    kw = dict(causal=w.causal, block_mask=inp["block_mask"], block=128, kv_len=inp["kv_len"],
+              dropout_p=w.dropout_p, seed=inp["seed"])
+    q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
+
+    def run(heads):
+        t0 = time.perf_counter()
+        oracle.attention_fwd(q, k, v, w.softmax_scale, heads=heads, **kw)
+        if backward:
+            oracle.attention_bwd(q, k, v, do, w.softmax_scale, heads=heads, **kw)
+        return time.perf_counter() - t0
+
+    t1 = run([0])
+    n = max(1, min(total_heads, int(budget_s / max(t1, 1e-6))))
+    heads = list(range(n))
+    t = run(heads) if n > 1 else t1
+    value = per_head * n / t / 1e12
+    return {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n} of {total_heads} heads, fp64 {'fwd+bwd' if backward else 'fwd'}, {t:.2f} s"}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_fa(args, w, ws, rank, device):
+    import torch
+    import io_aware_exact_08_gb300 as fa
+    from workloads import make_inputs
+
+    inp = make_inputs(w)
+    dens = density_of(inp, w)
+    fwd_f, bwd_f = flops(w, dens)
+    fwd_b, bwd_b = algorithmic_bytes(w)
+    dev = lambda t: None if t is None else t.to(device).contiguous()
+    q, k, v, do = (dev(inp[n]) for n in ("q", "k", "v", "do"))
+    bm, kl = dev(inp["block_mask"]), dev(inp["kv_len"])
+    B, H, N, d = w.B, w.H, w.N, w.d
+    dtype = fa.FA_BF16 if w.dtype == "bf16" else fa.FA_FP32
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    wsb = fa.fa_bwd_workspace_size(B, H, N, d)
+    work = torch.empty(wsb, dtype=torch.uint8, device=device)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    ptr = lambda t: None if t is None else t.data_ptr()
+    scale, causal, p, seed = w.softmax_scale, int(w.causal), float(w.dropout_p), int(inp["seed"])
+
+    def fwd():
+        rc = fa.fa_fwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, N, d, scale, causal, ptr(bm), p, seed,
+                       dtype, ptr(kl), sh)
+        assert rc == 0, fa.fa_status_string(rc)
+
+    def bwd():
+        rc = fa.fa_bwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), ptr(do), ptr(dq), ptr(dk), ptr(dv), B, H, N, d,
+                       scale, causal, ptr(bm), p, seed, dtype, ptr(kl), ptr(work), wsb, sh)
+        assert rc == 0, fa.fa_status_string(rc)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(device)
+    st, site = fa.fa_check_device_status(sh)
+    assert st == 0, f"device status {st} at site {site}"
+
+    # timed region: K steps; L2 flushed before each step, outside the events
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    launches0 = fa.fa_launch_count()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(device)
+    launches = fa.fa_launch_count() - launches0
+    barrier(device)
+    clk = clocks.stop()
+    st, site = fa.fa_check_device_status(sh)
+    assert st == 0, f"device status {st} at site {site}"
+    fwd_ms = [a.elapsed_time(b) for a, b, c in ev]
+    bwd_ms = [b.elapsed_time(c) for a, b, c in ev]
+    step_ms = sum(f + g for f, g in zip(fwd_ms, bwd_ms)) / args.steps
+    step_ms_max = max_over_ranks(step_ms, device)
+    fwd_avg = max_over_ranks(sum(fwd_ms) / args.steps, device)
+    bwd_avg = max_over_ranks(sum(bwd_ms) / args.steps, device)
+
+    # end to end through the public API with host buffers (pinned), every step
+    # copies Q, K, V, dO in and O, dQ, dK, dV out
+    host_in = [inp[n].pin_memory() for n in ("q", "k", "v", "do")]
+    host_out = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    barrier(device)
+    torch.cuda.synchronize(device)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        for dst, src in zip((q, k, v, do), host_in):
+            dst.copy_(src, non_blocking=True)
+        fwd()
+        bwd()
+        for dst, src in zip(host_out, (o, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / e2e_steps, device)
+
+    total_f = (fwd_f + bwd_f) * ws
+    value = total_f / (step_ms_max * 1e-3) / 1e12
+    e2e_value = total_f / (e2e_ms * 1e-3) / 1e12
+    fwd_tflops = fwd_f * ws / (fwd_avg * 1e-3) / 1e12
+    bwd_tflops = bwd_f * ws / (bwd_avg * 1e-3) / 1e12
+    peaks = load_peaks()
+    # dominant call of the step; the forward is one kernel launch, the
+    # backward call is three (preprocess, main, dq convert)
+    dominant = "fa_bwd" if bwd_avg >= fwd_avg else "fa_fwd"
+    dom_ms = bwd_avg if dominant == "fa_bwd" else fwd_avg
+    dom_f = bwd_f if dominant == "fa_bwd" else fwd_f
+    dom_b = bwd_b if dominant == "fa_bwd" else fwd_b
+    tensor_ach = dom_f / (dom_ms * 1e-3) / 1e12
+    hbm_ach = dom_b / (dom_ms * 1e-3) / 1e9
+    tensor_frac = tensor_ach / peaks["bf16"]
+    hbm_frac = hbm_ach / peaks["hbm"]
+    if w.dtype == "bf16" and tensor_frac >= hbm_frac:
+        roof = {"bound": "tensor", "achieved": round(tensor_ach, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": round(tensor_frac, 4)}
+    elif w.dtype == "bf16":
+        roof = {"bound": "hbm", "achieved": round(hbm_ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(hbm_frac, 4)}
+    else:
+        roof = {"bound": "alu", "achieved": round(tensor_ach, 3), "peak": None, "unit": "TFLOP/s", "frac": None}
+    roof.update({"kernel": dominant, "traffic": None, "peak_source": peaks["source"] + " (burst)",
+                 "tensor_frac": round(tensor_frac, 4), "hbm_frac": round(hbm_frac, 4),
+                 "algorithmic_flops": dom_f, "algorithmic_bytes": dom_b, "avg_ms": round(dom_ms, 4)})
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+                   "dropout_p": w.dropout_p, "kv_len_range": w.kv_len_range, "block_density": round(dens, 5),
+                   "scale": scale, "step": "fa_fwd + fa_bwd", "l2": "flushed before every timed step",
+                   "parallelism": f"replicas x{ws}"},
+        "fwd_tflops": round(fwd_tflops, 3), "bwd_tflops": round(bwd_tflops, 3),
+        "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
+        "frac_of_bf16_peak": round(value / ws / peaks["bf16"], 4) if w.dtype == "bf16" else None,
+        "fwd_frac_of_bf16_peak": round(fwd_tflops / ws / peaks["bf16"], 4) if w.dtype == "bf16" else None,
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = oracle_sample(w, inp, budget_s=args.cpu_budget)
+    return line
+
+
+def run_reference(args, w, ws, rank):
+    """The oracle (fp64, host cores) timed on a bounded sample of the workload."""
+    from workloads import make_inputs
+    if rank != 0:
+        return None
+    inp = make_inputs(w)
+    vals = []
+    samples = []
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, budget_s=1.0)
+    for _ in range(args.steps):
+        r = oracle_sample(w, inp, budget_s=args.cpu_budget / max(1, args.steps))
+        vals.append(r["value"])
+        samples.append(r["sample"])
+    value = statistics.mean(vals)
+    import oracle
+    dens = density_of(inp, w)
+    fwd_f, bwd_f = flops(w, dens)
+    ms = (fwd_f + bwd_f) / (value * 1e12) * 1e3
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": "; ".join(samples[:3])},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gpt2_causal")
+    ap.add_argument("--impl", default="fa", choices=["fa", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from workloads import WORKLOADS, sweep_workloads
+    table = dict(WORKLOADS)
+    table.update({w.name: w for w in sweep_workloads()})
+    w = table[args.workload]
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        line = run_reference(args, w, ws, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    import io_aware_exact_08_gb300 as fa
+    fa.load_library()
+    line = run_fa(args, w, ws, rank, device)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

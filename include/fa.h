@@ -1,0 +1,130 @@
+/*
+ * fa.h - C ABI of the exact IO-aware attention library (GB300, sm_103a).
+ *
+ * The library computes exact attention O = softmax(scale * Q K^T + mask) V
+ * block by block with the running row-max / row-sum rescaling, so the N x N
+ * score matrix never reaches HBM ("FlashAttention: Fast and Memory-Efficient
+ * Exact Attention with IO-Awareness", sections "Ide Utama" and "Metode",
+ * steps 1-4), and the backward pass that keeps only O and the per-row
+ * log-sum-exp and recomputes S and P tile by tile (same page, "Ide Utama",
+ * third point; "FlashAttention" blog post, section "Recomputation").
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are contiguous [B, H, N, d] row-major (d fastest), in device
+ *    memory, 16-byte aligned. q, k, v, o, dO, dq, dk, dv all have that shape
+ *    and the element type `dtype`. lse is fp32 [B, H, N] in natural log:
+ *    lse = m + ln(l), which carries the same information as the pair (l, m)
+ *    the pages keep for the backward pass.
+ *  - d must be 64 or 128. B, H >= 1, N >= 0 (N == 0 is a no-op).
+ *  - Masks combine by AND: causal (key j > query i is masked, top-left
+ *    aligned), key padding (j >= kv_len[b] masked; kv_len is int32[B] in
+ *    device memory, or NULL), block mask (block_mask[(i/128)*nb + j/128] == 0
+ *    masks the block; nb = ceil(N/128); uint8 in device memory, or NULL).
+ *    The block-sparse form follows "FlashAttention: Fast and Memory-Efficient
+ *    Exact Attention with IO-Awareness", section "Ekstensi: Block-Sparse
+ *    FlashAttention"; the block edge is fixed at 128 for queries and keys.
+ *  - A query row with every key masked gives O = 0, lse = -inf and no
+ *    gradient.
+ *  - Dropout (0 <= dropout_p < 1) is applied to the normalised P for the
+ *    P V product only (inverted: kept entries scaled by 1/(1-p)); lse does
+ *    not include it. The keep bit of (b, h, i, j) is word (j mod 4) of
+ *    Philox4x32-10 (Salmon et al., SC'11) with key (lo32(seed), hi32(seed))
+ *    and counter (j/4, i, h, b), kept iff that word >= floor(p * 2^32)
+ *    (clamped to 2^32 - 1). It is independent of tiling, so the forward,
+ *    the backward and fa_dropout_mask agree bit for bit.
+ *  - stream is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *    asynchronous on it; the library allocates no device memory and
+ *    synchronises nothing except fa_check_device_status.
+ *  - Every call returns FA_OK (0) or a negative fa_status. Argument errors
+ *    are detected on the host before any launch; nothing is thrown across
+ *    the ABI. Device-side bounded waits that run out set a status word that
+ *    fa_check_device_status reports.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = -1,   /* null pointer, negative size, p outside [0,1), misalignment */
+    FA_ERR_UNSUPPORTED = -2,   /* d not in {64,128}, unknown dtype */
+    FA_ERR_CUDA = -3,          /* a CUDA runtime call failed (launch, attribute, symbol) */
+    FA_ERR_WORKSPACE = -4,     /* workspace missing or smaller than fa_bwd_workspace_size */
+    FA_ERR_DEVICE_TIMEOUT = -5 /* a device-side bounded wait ran out (see fa_check_device_status) */
+} fa_status;
+
+/*
+ * Forward: o = softmax(scale * q k^T + mask) v with optional dropout, and
+ * lse[b,h,i] = log-sum-exp of row i's (masked, scaled) scores.
+ * Inputs q, k, v; outputs o (dtype) and lse (fp32). All device pointers,
+ * owned by the caller. bf16 runs on the tcgen05 tensor-core kernel; fp32 on
+ * an fp32 CUDA-core kernel.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, float scale, int causal,
+           const uint8_t* block_mask, float dropout_p, uint64_t seed,
+           fa_dtype dtype, const int32_t* kv_len, void* stream);
+
+/*
+ * Backward: given the forward's inputs, its outputs o and lse, and the
+ * output gradient dO, writes dq, dk, dv (dtype, [B,H,N,d]). S and P are
+ * recomputed tile by tile from lse; the same masks, scale and dropout
+ * (seed, p) as the forward must be passed. workspace is caller-owned device
+ * memory of at least fa_bwd_workspace_size(B,H,N,d) bytes, 256-byte aligned;
+ * its contents on entry do not matter and on exit are unspecified.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dO, void* dq, void* dk, void* dv,
+           int B, int H, int N, int d, float scale, int causal,
+           const uint8_t* block_mask, float dropout_p, uint64_t seed,
+           fa_dtype dtype, const int32_t* kv_len,
+           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of backward workspace: rowsum(dO o O) (fp32 [B,H,N]) plus the fp32
+ * dQ accumulator ([B,H,N,d]), each rounded up to 256 bytes. O(B*H*N*d): the
+ * backward keeps no N x N state. Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Test hook: writes the dropout keep mask Z (uint8 0/1, [B,H,N,N], device
+ * memory owned by the caller) that fa_fwd/fa_bwd apply for (p, seed).
+ */
+int fa_dropout_mask(uint8_t* keep, int B, int H, int N, float p, uint64_t seed, void* stream);
+
+/*
+ * Synchronises `stream`, returns the device status word (FA_OK, or
+ * FA_ERR_DEVICE_TIMEOUT when a kernel's bounded wait ran out), then clears
+ * it. *site (optional) receives the id of the wait that gave up.
+ */
+int fa_check_device_status(void* stream, int* site);
+
+/* Human-readable name of a status code (static string). */
+const char* fa_status_string(int status);
+
+/*
+ * Diagnostic: 0 = default kernels (tcgen05 for bf16), 1 = force the
+ * CUDA-core kernels for every dtype. Process-wide; returns the old value.
+ */
+int fa_set_kernel_path(int path);
+
+/*
+ * Diagnostic: number of CUDA kernels this library has launched in the
+ * calling process (all devices, all entry points).
+ */
+uint64_t fa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

@@ -1,0 +1,252 @@
+"""Exact IO-aware attention for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over the C ABI in ``include/fa.h`` (``libfa_gb300.so``,
+built in-tree by ``build.py``). The functions ``fa_fwd``, ``fa_bwd``,
+``fa_bwd_workspace_size``, ``fa_dropout_mask``, ``fa_check_device_status``,
+``fa_status_string`` and ``fa_set_kernel_path`` take the same arguments as
+their C counterparts (device pointers as integers, sizes, a stream handle)
+and only marshal them. ``attention_fwd`` / ``attention_bwd`` and
+``FlashAttention`` add the tensor plumbing: PyTorch allocates the outputs
+and the workspace and supplies the current stream; every step of the
+computation runs in the library's CUDA kernels.
+
+There is no CPU fallback: if the library cannot be loaded, importing the
+binding's functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "FA_BF16", "FA_FP32", "FaError", "load_library", "library_path",
+    "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
+    "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
+    "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
+]
+
+FA_BF16 = 0
+FA_FP32 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "lib", "libfa_gb300.so")
+_lib = None
+_lock = threading.Lock()
+
+EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
+            "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count")
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(build_if_missing: bool = True):
+    """Loads libfa_gb300.so (building it with nvcc if it is absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            if not build_if_missing:
+                raise RuntimeError(f"attention library not built: {_LIB_PATH}")
+            from . import build as _build
+            _build.build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, F, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
+        lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, P]
+        lib.fa_fwd.restype = I
+        lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, P, SZ, P]
+        lib.fa_bwd.restype = I
+        lib.fa_bwd_workspace_size.argtypes = [I, I, I, I]
+        lib.fa_bwd_workspace_size.restype = SZ
+        lib.fa_dropout_mask.argtypes = [P, I, I, I, F, U64, P]
+        lib.fa_dropout_mask.restype = I
+        lib.fa_check_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+        lib.fa_check_device_status.restype = I
+        lib.fa_status_string.argtypes = [I]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_set_kernel_path.argtypes = [I]
+        lib.fa_set_kernel_path.restype = I
+        lib.fa_launch_count.argtypes = []
+        lib.fa_launch_count.restype = ctypes.c_uint64
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------------------
+# C ABI, same names and argument order as include/fa.h.
+# ---------------------------------------------------------------------------
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, block_mask, dropout_p, seed, dtype, kv_len, stream):
+    return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, int(causal), block_mask, dropout_p,
+                                 seed & 0xFFFFFFFFFFFFFFFF, dtype, kv_len, stream)
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, block_mask, dropout_p, seed, dtype,
+           kv_len, workspace, workspace_bytes, stream):
+    return load_library().fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, int(causal), block_mask,
+                                 dropout_p, seed & 0xFFFFFFFFFFFFFFFF, dtype, kv_len, workspace,
+                                 workspace_bytes, stream)
+
+
+def fa_bwd_workspace_size(B, H, N, d):
+    return load_library().fa_bwd_workspace_size(B, H, N, d)
+
+
+def fa_dropout_mask(keep, B, H, N, p, seed, stream):
+    return load_library().fa_dropout_mask(keep, B, H, N, p, seed & 0xFFFFFFFFFFFFFFFF, stream)
+
+
+def fa_check_device_status(stream):
+    """Returns (status, site)."""
+    site = ctypes.c_int(0)
+    st = load_library().fa_check_device_status(stream, ctypes.byref(site))
+    return st, site.value
+
+
+def fa_status_string(status):
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_set_kernel_path(path):
+    return load_library().fa_set_kernel_path(int(path))
+
+
+def fa_launch_count():
+    return int(load_library().fa_launch_count())
+
+
+# ---------------------------------------------------------------------------
+# Tensor plumbing (PyTorch for device memory and streams only).
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, like=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous [B,H,N,d]")
+    if like is not None and (t.shape != like.shape or t.dtype != like.dtype):
+        raise ValueError(f"{name} must match q in shape and dtype")
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def attention_fwd(q, k, v, scale=None, causal=False, block_mask=None, dropout_p=0.0, seed=0, kv_len=None,
+                  out=None, lse=None, stream=None):
+    """O, LSE = attention(q, k, v) for [B,H,N,d] CUDA tensors (bf16 or fp32)."""
+    torch = _torch()
+    _check(q, "q")
+    _check(k, "k", q)
+    _check(v, "v", q)
+    B, H, N, d = q.shape
+    scale = (1.0 / d ** 0.5) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    rc = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, scale, causal, _ptr(block_mask),
+                float(dropout_p), int(seed), _dtype_code(q), _ptr(kv_len), _stream(stream))
+    if rc != 0:
+        raise FaError(rc, "fa_fwd")
+    return o, l
+
+
+def attention_bwd(q, k, v, o, lse, do, scale=None, causal=False, block_mask=None, dropout_p=0.0, seed=0,
+                  kv_len=None, workspace=None, stream=None, dq=None, dk=None, dv=None):
+    """dQ, dK, dV for the forward above (same masks, scale and dropout)."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check(t, name, q)
+    B, H, N, d = q.shape
+    scale = (1.0 / d ** 0.5) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    rc = fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                B, H, N, d, scale, causal, _ptr(block_mask), float(dropout_p), int(seed), _dtype_code(q),
+                _ptr(kv_len), _ptr(ws), ws.numel(), _stream(stream))
+    if rc != 0:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def dropout_mask(B, H, N, p, seed, device="cuda", stream=None):
+    """The keep mask Z (uint8 [B,H,N,N]) the kernels apply for (p, seed)."""
+    torch = _torch()
+    z = torch.empty((B, H, N, N), dtype=torch.uint8, device=device)
+    rc = fa_dropout_mask(_ptr(z), B, H, N, float(p), int(seed), _stream(stream))
+    if rc != 0:
+        raise FaError(rc, "fa_dropout_mask")
+    return z
+
+
+def _make_autograd():
+    torch = _torch()
+
+    class FlashAttention(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v, scale, causal, block_mask, dropout_p, seed, kv_len):
+            o, lse = attention_fwd(q, k, v, scale, causal, block_mask, dropout_p, seed, kv_len)
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.args = (scale, causal, block_mask, dropout_p, seed, kv_len)
+            return o
+
+        @staticmethod
+        def backward(ctx, do):
+            q, k, v, o, lse = ctx.saved_tensors
+            scale, causal, block_mask, dropout_p, seed, kv_len = ctx.args
+            dq, dk, dv = attention_bwd(q, k, v, o, lse, do.contiguous(), scale, causal, block_mask, dropout_p,
+                                       seed, kv_len)
+            return dq, dk, dv, None, None, None, None, None, None
+
+    return FlashAttention
+
+
+_autograd_cls = None
+
+
+def __getattr__(name):
+    global _autograd_cls
+    if name == "FlashAttention":
+        if _autograd_cls is None:
+            _autograd_cls = _make_autograd()
+        return _autograd_cls
+    raise AttributeError(name)
+
+
+def attention(q, k, v, scale=None, causal=False, block_mask=None, dropout_p=0.0, seed=0, kv_len=None):
+    """Differentiable exact attention (autograd over the library's kernels)."""
+    B, H, N, d = q.shape
+    scale = (1.0 / d ** 0.5) if scale is None else float(scale)
+    return __getattr__("FlashAttention").apply(q, k, v, scale, causal, block_mask, dropout_p, seed, kv_len)

@@ -1,0 +1,194 @@
+// C entry points of the attention library: argument validation, workspace
+// layout, kernel selection and the device status word. See include/fa.h for
+// the contract of each call.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+// Device status word: kernels whose bounded waits run out write
+// FA_ERR_DEVICE_TIMEOUT (and the id of the wait) here instead of trapping.
+__device__ int g_status[2];
+
+int g_kernel_path = 0;  // 0 = default, 1 = CUDA-core kernels only
+std::atomic<uint64_t> g_launches{0};
+
+int status_ptr(int** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    static int* cached[64] = {nullptr};
+    if (dev < 0 || dev >= 64) return FA_ERR_CUDA;
+    if (!cached[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return FA_ERR_CUDA;
+        cached[dev] = static_cast<int*>(ptr);
+    }
+    *out = cached[dev];
+    return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+uint32_t keep_threshold(float p) {
+    const double t = std::floor((double)p * 4294967296.0);
+    if (t <= 0.0) return 0u;
+    if (t >= 4294967295.0) return 0xffffffffu;
+    return (uint32_t)t;
+}
+
+int check_common(int B, int H, int N, int d, float scale, float dropout_p, fa_dtype dtype) {
+    if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (!(dropout_p >= 0.f && dropout_p < 1.f)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if ((long long)B * H > 65535) return FA_ERR_UNSUPPORTED;
+    if (N > (1 << 24)) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+void fill_common(Problem& p, int B, int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
+                 float dropout_p, uint64_t seed, fa_dtype dtype, const int32_t* kv_len, void* stream) {
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.d = d;
+    p.scale = scale;
+    p.causal = causal ? 1 : 0;
+    p.block_mask = block_mask;
+    p.nb = (N + kMaskBlock - 1) / kMaskBlock;
+    p.dropout_p = dropout_p;
+    p.drop_threshold = keep_threshold(dropout_p);
+    p.seed = seed;
+    p.dtype = dtype;
+    p.kv_len = kv_len;
+    p.stream = static_cast<cudaStream_t>(stream);
+}
+
+int from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return FA_OK;
+    if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: CUDA error %s\n", cudaGetErrorString(e));
+    return FA_ERR_CUDA;
+}
+
+bool use_tensor_cores(const Problem& p) { return g_kernel_path == 0 && p.dtype == FA_BF16; }
+
+}  // namespace
+
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, const uint8_t* block_mask, float dropout_p, uint64_t seed, fa_dtype dtype,
+           const int32_t* kv_len, void* stream) {
+    int rc = check_common(B, H, N, d, scale, dropout_p, dtype);
+    if (rc != FA_OK) return rc;
+    if (N == 0) return FA_OK;
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+        return FA_ERR_INVALID_ARG;
+    Problem p{};
+    fill_common(p, B, H, N, d, scale, causal, block_mask, dropout_p, seed, dtype, kv_len, stream);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    rc = status_ptr(&p.status);
+    if (rc != FA_OK) return rc;
+    if (use_tensor_cores(p)) return launch_fwd_tc(p);
+    return from_cuda(launch_fwd_simt(p));
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 0 || (d != 64 && d != 128)) return 0;
+    const size_t rows = (size_t)B * H * N;
+    return round256(rows * sizeof(float)) + round256(rows * (size_t)d * sizeof(float));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+           void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
+           float dropout_p, uint64_t seed, fa_dtype dtype, const int32_t* kv_len, void* workspace,
+           size_t workspace_bytes, void* stream) {
+    int rc = check_common(B, H, N, d, scale, dropout_p, dtype);
+    if (rc != FA_OK) return rc;
+    if (N == 0) return FA_OK;
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+        !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+        return FA_ERR_INVALID_ARG;
+    const size_t need = fa_bwd_workspace_size(B, H, N, d);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return FA_ERR_WORKSPACE;
+    Problem p{};
+    fill_common(p, B, H, N, d, scale, causal, block_mask, dropout_p, seed, dtype, kv_len, stream);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = const_cast<void*>(o);
+    p.lse = const_cast<float*>(lse);
+    p.dO = dO;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    const size_t rows = (size_t)B * H * N;
+    p.delta = static_cast<float*>(workspace);
+    p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)));
+    rc = status_ptr(&p.status);
+    if (rc != FA_OK) return rc;
+    if (use_tensor_cores(p)) return launch_bwd_tc(p);
+    return from_cuda(launch_bwd_simt(p));
+}
+
+int fa_dropout_mask(uint8_t* keep, int B, int H, int N, float p, uint64_t seed, void* stream) {
+    if (B < 1 || H < 1 || N < 0 || !(p >= 0.f && p < 1.f)) return FA_ERR_INVALID_ARG;
+    if (N == 0) return FA_OK;
+    if (!keep) return FA_ERR_INVALID_ARG;
+    return from_cuda(launch_dropout_mask(keep, B, H, N, keep_threshold(p), seed, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_check_device_status(void* stream, int* site) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    int host[2] = {0, 0};
+    if (cudaMemcpyFromSymbol(host, g_status, sizeof(host)) != cudaSuccess) return FA_ERR_CUDA;
+    if (host[0] != 0) {
+        const int zero[2] = {0, 0};
+        if (cudaMemcpyToSymbol(g_status, zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    if (site) *site = host[1];
+    return host[0];
+}
+
+const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dim, dtype or size";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime error";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing, too small or misaligned";
+        case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a device-side bounded wait ran out";
+        default: return "unknown fa status";
+    }
+}
+
+uint64_t fa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int fa_set_kernel_path(int path) {
+    const int old = g_kernel_path;
+    g_kernel_path = (path == 1) ? 1 : 0;
+    return old;
+}
+
+}  // extern "C"

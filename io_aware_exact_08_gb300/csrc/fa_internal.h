@@ -1,0 +1,57 @@
+// Internal declarations shared by the library's translation units.
+// Not part of the public ABI (that is include/fa.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Everything a launch needs; filled and validated by the C entry points.
+struct Problem {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    const void* dO;
+    void* dq;
+    void* dk;
+    void* dv;
+    int B, H, N, d;
+    float scale;
+    int causal;
+    const uint8_t* block_mask;  // nb x nb or nullptr
+    int nb;                     // ceil(N / 128)
+    float dropout_p;
+    uint32_t drop_threshold;    // keep iff philox word >= drop_threshold
+    uint64_t seed;
+    fa_dtype dtype;
+    const int32_t* kv_len;      // [B] or nullptr
+    float* delta;               // workspace: rowsum(dO o O), fp32 [B,H,N]
+    float* dq_acc;              // workspace: fp32 [B,H,N,d]
+    int* status;                // device status word (timeouts)
+    cudaStream_t stream;
+};
+
+constexpr int kMaskBlock = 128;
+
+// Counts kernel launches for fa_launch_count (thread-safe).
+void note_launches(int n);
+
+// CUDA-core kernels (any dtype, d in {64,128}); implemented in fa_simt.cu.
+cudaError_t launch_fwd_simt(const Problem& p);
+cudaError_t launch_bwd_simt(const Problem& p);
+cudaError_t launch_bwd_preprocess(const Problem& p);
+cudaError_t launch_dropout_mask(uint8_t* keep, int B, int H, int N, uint32_t thr, uint64_t seed,
+                                cudaStream_t s);
+
+// tcgen05 kernels (bf16, d in {64,128}); implemented in fa_fwd_sm103.cu / fa_bwd_sm103.cu.
+int launch_fwd_tc(const Problem& p);
+int launch_bwd_tc(const Problem& p);
+
+}  // namespace fa

@@ -1,0 +1,79 @@
+"""Shared helpers for the GPU parity tests: run the library through its C ABI
+and the fp64 oracle on the same seeded inputs, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import io_aware_exact_08_gb300 as fa
+import oracle
+
+# Tolerances (max-abs), for bf16 inputs with fp32 accumulation and for fp32.
+TOL = {
+    "bf16": dict(o=1e-2, lse=1e-3, dq=3e-2, dk=3e-2, dv=3e-2),
+    "fp32": dict(o=1e-4, lse=1e-4, dq=1e-4, dk=1e-4, dv=1e-4),
+}
+
+
+def to_dev(x, device="cuda"):
+    return None if x is None else x.to(device).contiguous()
+
+
+def gpu_forward(inp, device="cuda"):
+    q, k, v = (to_dev(inp[n], device) for n in ("q", "k", "v"))
+    o, lse = fa.attention_fwd(q, k, v, scale=inp["scale"], causal=inp["causal"],
+                              block_mask=to_dev(inp["block_mask"], device), dropout_p=inp["dropout_p"],
+                              seed=inp["seed"], kv_len=to_dev(inp["kv_len"], device))
+    return q, k, v, o, lse
+
+
+def gpu_fwd_bwd(inp, device="cuda"):
+    q, k, v, o, lse = gpu_forward(inp, device)
+    do = to_dev(inp["do"], device)
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, lse, do, scale=inp["scale"], causal=inp["causal"],
+                                  block_mask=to_dev(inp["block_mask"], device), dropout_p=inp["dropout_p"],
+                                  seed=inp["seed"], kv_len=to_dev(inp["kv_len"], device))
+    torch.cuda.synchronize()
+    st, site = fa.fa_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == 0, f"device status {st} at site {site}"
+    return {n: t.float().cpu().numpy().astype(np.float64)
+            for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+
+
+def oracle_fwd_bwd(inp, heads=None, backward=True):
+    kw = dict(causal=inp["causal"], block_mask=inp["block_mask"], block=128, kv_len=inp["kv_len"],
+              dropout_p=inp["dropout_p"], seed=inp["seed"], heads=heads)
+    o, lse = oracle.attention_fwd(inp["q"], inp["k"], inp["v"], inp["scale"], **kw)
+    out = dict(o=o, lse=lse)
+    if backward:
+        dq, dk, dv = oracle.attention_bwd(inp["q"], inp["k"], inp["v"], inp["do"], inp["scale"], **kw)
+        out.update(dq=dq, dk=dk, dv=dv)
+    return out
+
+
+def max_err(got, ref, heads=None, H=None):
+    """Max-abs error; -inf entries (fully masked rows' LSE) must match exactly."""
+    if heads is not None:
+        B = got.shape[0]
+        g = got.reshape((-1,) + got.shape[2:])[list(heads)]
+        r = ref.reshape((-1,) + ref.shape[2:])[list(heads)]
+    else:
+        g, r = got, ref
+    inf_r = np.isneginf(r)
+    if inf_r.any():
+        assert np.array_equal(np.isneginf(g), inf_r), "masked-row -inf pattern differs"
+        g = np.where(inf_r, 0.0, g)
+        r = np.where(inf_r, 0.0, r)
+    assert np.all(np.isfinite(g)), "non-finite values in GPU output"
+    return float(np.max(np.abs(g - r))) if g.size else 0.0
+
+
+def compare(got, ref, dtype, keys=("o", "lse", "dq", "dk", "dv"), heads=None):
+    tol = TOL[dtype]
+    errs = {}
+    for key in keys:
+        if key in ref:
+            errs[key] = max_err(got[key], ref[key], heads)
+    bad = {k: (e, tol[k]) for k, e in errs.items() if not e <= tol[k]}
+    assert not bad, f"tolerance exceeded: {bad} (all errors: {errs})"
+    return errs

@@ -1,0 +1,99 @@
+"""The C ABI library loads without a GPU, exports every declared symbol and
+rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import io_aware_exact_08_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(fa_\w+)\s*\(", text))
+    return names
+
+
+def test_library_builds_and_loads():
+    from io_aware_exact_08_gb300 import build
+    path = build.build()
+    assert os.path.exists(path)
+    lib = fa.load_library()
+    assert lib is not None
+
+
+def test_every_declared_symbol_is_exported():
+    declared = _declared_symbols()
+    assert {"fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
+            "fa_check_device_status", "fa_status_string"} <= declared
+    lib = ctypes.CDLL(fa.library_path())
+    for name in declared:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.library_path()], capture_output=True, text=True)
+    exported = set(re.findall(r"\bT (fa_\w+)", out.stdout))
+    assert declared <= exported
+    assert set(fa.EXPORTED) <= exported
+
+
+def test_workspace_is_linear_in_n():
+    # O(B*H*N*d): rowsum plus fp32 dQ accumulator, each rounded to 256 bytes
+    for B, H, N, d in [(1, 1, 128, 64), (2, 16, 8192, 128), (32, 16, 512, 64), (1, 1, 1, 64)]:
+        rows = B * H * N
+        r256 = lambda x: (x + 255) // 256 * 256
+        assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(4 * rows) + r256(4 * rows * d)
+    assert fa.fa_bwd_workspace_size(1, 1, 16, 96) == 0
+    assert fa.fa_bwd_workspace_size(0, 1, 16, 64) == 0
+    w1 = fa.fa_bwd_workspace_size(1, 1, 4096, 128)
+    w2 = fa.fa_bwd_workspace_size(1, 1, 8192, 128)
+    assert w2 == 2 * w1
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null value; never dereferenced on these paths
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=96), -2), (dict(d=32), -2), (dict(B=0), -1), (dict(H=-1), -1), (dict(N=-5), -1),
+    (dict(dropout_p=1.0), -1), (dict(dropout_p=-0.1), -1), (dict(dtype=7), -2),
+    (dict(q=None), -1), (dict(lse=None), -1), (dict(o=FAKE + 8), -1), (dict(scale=float("inf")), -1),
+])
+def test_forward_argument_errors(kw, expect):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=16, d=64, scale=0.125, causal=0,
+                block_mask=None, dropout_p=0.0, seed=0, dtype=fa.FA_BF16, kv_len=None, stream=None)
+    args.update(kw)
+    assert fa.fa_fwd(**args) == expect
+
+
+def test_zero_length_is_a_noop():
+    assert fa.fa_fwd(None, None, None, None, None, 1, 1, 0, 64, 0.1, 0, None, 0.0, 0, fa.FA_BF16, None, None) == 0
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(workspace=None), -4), (dict(workspace_bytes=16), -4), (dict(workspace=FAKE + 16), -4),
+    (dict(dq=None), -1), (dict(d=80), -2), (dict(dropout_p=2.0), -1),
+])
+def test_backward_argument_errors(kw, expect):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dO=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, H=1, N=16,
+                d=64, scale=0.125, causal=0, block_mask=None, dropout_p=0.0, seed=0, dtype=fa.FA_BF16,
+                kv_len=None, workspace=FAKE, workspace_bytes=1 << 20, stream=None)
+    args.update(kw)
+    assert fa.fa_bwd(**args) == expect
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, -5):
+        s = fa.fa_status_string(code)
+        assert s.startswith("FA_")
+    assert "unknown" in fa.fa_status_string(12345)
+
+
+def test_kernel_path_switch_roundtrips():
+    old = fa.fa_set_kernel_path(1)
+    assert fa.fa_set_kernel_path(old) == 1
