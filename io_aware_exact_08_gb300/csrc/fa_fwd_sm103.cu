@@ -1,5 +1,497 @@
-// Placeholder: forward tensor-core path routes to the CUDA-core kernel.
+// Forward attention on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// One CTA computes one 128-row query tile Q_i of one (batch, head) and walks
+// the key/value tiles K_j, V_j (128 keys each) that are not masked out,
+// following the per-block update of "FlashAttention: Fast and
+// Memory-Efficient Exact Attention with IO-Awareness" (section "Metode",
+// steps 1-4): S_ij = Q_i K_j^T, running row max m and row sum l, and
+// O_i <- e^{m_old - m_new} O_i + P~_ij V_j, with the division by l deferred
+// to the end (FlashAttention-2 section of the "Flash Attention" guide).
+// Fully masked tiles are skipped (causal future, key padding, zero blocks of
+// the block-sparse mask, "Ekstensi: Block-Sparse FlashAttention").
+//
+// Roles (192 threads, warp specialised as in the FlashAttention-3 section):
+//   warps 0-3  softmax: thread r owns query row r. It reads S from TMEM,
+//              masks, updates (m, l), writes P as bf16 back into the same
+//              TMEM columns, applies dropout, and does the epilogue.
+//   warp 4     producer: TMA loads of Q once, then K_0, K_1, V_0, K_2, V_1,
+//              ... through a ring of shared-memory stages.
+//   warp 5     MMA issuer: one thread issues tcgen05.mma for S_j = Q K_j^T
+//              (double-buffered in TMEM so S_{j+1} overlaps the softmax of
+//              S_j) and O += P_j V_j (P read from TMEM), and owns the TMEM
+//              allocation.
+//
+// The running max is only raised when a row's new maximum exceeds the one
+// in use by more than 2^8 (log2 units); between raises P <= 2^8, which fp32
+// accumulation holds exactly enough, and the final O/l and LSE use the same
+// m, so the result is unchanged while most O rescales are skipped.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "fa_device.cuh"
 #include "fa_internal.h"
+#include "fa_sm103.cuh"
+
 namespace fa {
-int launch_fwd_tc(const Problem& p) { return launch_fwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+namespace {
+
+using namespace sm103;
+
+constexpr int kBlockM = 128;  // query rows per CTA
+constexpr int kBlockN = 128;  // keys per tile
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kStages = (D == 128) ? 5 : 8;
+    static constexpr int kTileBytes = kBlockN * D * 2;   // one K or V tile, bf16
+    static constexpr int kQBytes = kBlockM * D * 2;
+    static constexpr int kBoxes = D / 64;                // 64-column TMA boxes per tile
+    static constexpr int kBoxBytes = kBlockN * 128;      // 128 rows x 128 bytes
+    static constexpr int kSmem = 1024 /*alignment slack*/ + kQBytes + kStages * kTileBytes + 256;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+};
+
+struct FwdParams {
+    float* lse;
+    void* o;
+    const uint8_t* block_mask;
+    const int32_t* kv_len;
+    int* status;
+    int H, N, nb, n_qtiles;
+    float scale_log2;
+    float out_scale;  // 1/(1-p)
+    uint32_t drop_thr;
+    int dropout;
+    int causal;
+    uint64_t seed;
+};
+
+struct SharedState {
+    uint64_t kv_full[8];
+    uint64_t kv_empty[8];
+    uint64_t q_full;
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t pv_done;
+    uint64_t teardown;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Whether key tile j is visited by query tile qt, and its element mask type.
+struct TileSched {
+    int nkt;       // key tiles in the sequence
+    int L;         // visible keys: min(kv_len[b], N)
+    int qt;
+    int causal;
+    const uint8_t* bm_row;  // block-mask row of this query tile or nullptr
+
+    __device__ bool active(int j) const {
+        const int k0 = j * kBlockN;
+        if (k0 >= L) return false;
+        if (causal && k0 > qt * kBlockM + kBlockM - 1) return false;
+        if (bm_row && !bm_row[j]) return false;
+        return true;
+    }
+    __device__ int end() const {
+        int e = (L + kBlockN - 1) / kBlockN;
+        if (causal) e = min(e, qt + 1);
+        return min(e, nkt);
+    }
+    // next active tile index >= j, or end()
+    __device__ int next(int j) const {
+        const int e = end();
+        while (j < e && !active(j)) ++j;
+        return j;
+    }
+    __device__ int count() const {
+        int c = 0;
+        for (int j = next(0); j < end(); j = next(j + 1)) ++c;
+        return c;
+    }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using Cfg = FwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sKV = smem + Cfg::kQBytes;
+    SharedState* st = reinterpret_cast<SharedState*>(sKV + Cfg::kStages * Cfg::kTileBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.y;
+    const int b = bh / p.H, h = bh % p.H;
+    // heaviest query tiles first (causal work grows with the tile index)
+    const int qt = p.causal ? (p.n_qtiles - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    const int row0 = qt * kBlockM;
+
+    TileSched sched;
+    sched.nkt = (p.N + kBlockN - 1) / kBlockN;
+    sched.L = p.kv_len ? min(max(p.kv_len[b], 0), p.N) : p.N;
+    sched.qt = qt;
+    sched.causal = p.causal;
+    sched.bm_row = p.block_mask ? p.block_mask + (size_t)qt * p.nb : nullptr;
+
+    WaitCtx wctx{&st->abort_flag, p.status};
+
+    if (tid == 0) {
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            mbar_init(&st->kv_full[s], 1);
+            mbar_init(&st->kv_empty[s], 1);
+        }
+        mbar_init(&st->q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&st->s_full[i], 1);
+            mbar_init(&st->p_full[i], kSoftmaxThreads);
+        }
+        mbar_init(&st->pv_done, 1);
+        mbar_init(&st->teardown, 1);
+        st->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&st->tmem_base, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = st->tmem_base;
+    const int n_active = sched.count();
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n_active > 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(&st->q_full, Cfg::kQBytes);
+#pragma unroll
+            for (int x = 0; x < Cfg::kBoxes; ++x)
+                tma_load_3d(sQ + x * Cfg::kBoxBytes, &tm_q, &st->q_full, x * 64, row0, bh);
+            uint32_t issued_phase[Cfg::kStages];
+            bool issued_any[Cfg::kStages];
+            for (int s = 0; s < Cfg::kStages; ++s) issued_any[s] = false;
+            int t = 0;  // load counter
+            auto load = [&](const CUtensorMap* map, int j) -> bool {
+                const int s = t % Cfg::kStages;
+                const uint32_t ph = (t / Cfg::kStages) & 1;
+                if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 1)) return false;
+                mbar_arrive_expect_tx(&st->kv_full[s], Cfg::kTileBytes);
+                uint8_t* dst = sKV + s * Cfg::kTileBytes;
+#pragma unroll
+                for (int x = 0; x < Cfg::kBoxes; ++x)
+                    tma_load_3d(dst + x * Cfg::kBoxBytes, map, &st->kv_full[s], x * 64, j * kBlockN, bh);
+                issued_phase[s] = ph;
+                issued_any[s] = true;
+                ++t;
+                return true;
+            };
+            // order: K(a0), K(a1), V(a0), K(a2), V(a1), ... (a = active tiles)
+            const int e = sched.end();
+            int ja = sched.next(0);
+            int jb = (ja < e) ? sched.next(ja + 1) : e;
+            bool ok = load(&tm_k, ja);
+            if (ok && jb < e) ok = load(&tm_k, jb);
+            int jc = (jb < e) ? sched.next(jb + 1) : e;
+            while (ok && ja < e) {
+                ok = load(&tm_v, ja);
+                if (ok && jc < e) ok = load(&tm_k, jc);
+                ja = jb;
+                jb = jc;
+                jc = (jc < e) ? sched.next(jc + 1) : e;
+            }
+            // drain: every issued copy has landed before the CTA may exit
+            for (int s = 0; s < Cfg::kStages; ++s)
+                if (issued_any[s]) mbar_wait(&st->kv_full[s], issued_phase[s], wctx, 2);
+            mbar_wait(&st->q_full, 0, wctx, 3);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n_active > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBlockM, D, 0, 1);
+            const uint32_t q_base = smem_u32(sQ);
+            const uint32_t kv_base = smem_u32(sKV);
+            int t = 0;  // consume counter, same order as the producer
+            bool ok = mbar_wait(&st->q_full, 0, wctx, 10);
+            tc_fence_after();
+            auto wait_tile = [&](uint32_t& addr) -> bool {
+                const int s = t % Cfg::kStages;
+                if (!mbar_wait(&st->kv_full[s], (t / Cfg::kStages) & 1, wctx, 11)) return false;
+                tc_fence_after();
+                addr = kv_base + s * Cfg::kTileBytes;
+                return true;
+            };
+            auto release_tile = [&]() {
+                mma_commit(&st->kv_empty[t % Cfg::kStages]);
+                ++t;
+            };
+            auto issue_s = [&](int buf) -> bool {
+                uint32_t kaddr;
+                if (!wait_tile(kaddr)) return false;
+                const uint32_t d = tmem + (buf ? Cfg::kColS1 : Cfg::kColS0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                    mma_ss(d, smem_desc_sw128(q_base + off, 16, 1024), smem_desc_sw128(kaddr + off, 16, 1024),
+                           idesc_s, kk > 0);
+                }
+                mma_commit(&st->s_full[buf]);
+                release_tile();
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            if (ok && n_active > 1) ok = issue_s(1);
+            for (int j = 0; ok && j < n_active; ++j) {
+                const int buf = j & 1;
+                if (!mbar_wait(&st->p_full[buf], (j >> 1) & 1, wctx, 12)) break;
+                tc_fence_after();
+                uint32_t vaddr;
+                if (!wait_tile(vaddr)) break;
+                const uint32_t a_tmem = tmem + (buf ? Cfg::kColS1 : Cfg::kColS0);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    // P: 16 keys = 8 TMEM columns of bf16 pairs; V: 16 rows of 128 bytes
+                    mma_ts(tmem + Cfg::kColO, a_tmem + kk * 8,
+                           smem_desc_sw128(vaddr + kk * 16 * 128, Cfg::kBoxBytes, 1024), idesc_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                release_tile();
+                mma_commit(&st->pv_done);
+                if (j + 2 < n_active) ok = issue_s(buf);
+            }
+            // every MMA this thread issued has completed before TMEM is freed
+            mma_commit(&st->teardown);
+            mbar_wait(&st->teardown, 0, wctx, 13);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int r = tid;  // row within the tile == TMEM lane
+        const int i = row0 + r;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float m = -INFINITY;  // running max in use (log2 units)
+        float l = 0.f;
+        bool ok = true;
+        int j = sched.next(0);
+        for (int it = 0; it < n_active; ++it, j = sched.next(j + 1)) {
+            const int buf = it & 1;
+            const uint32_t sbase = tmem + lane_base + (buf ? Cfg::kColS1 : Cfg::kColS0);
+            if (!mbar_wait(&st->s_full[buf], (it >> 1) & 1, wctx, 20)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(sbase + c * 32, sr[c]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+            float s[kBlockN];
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sr[c / 32][c % 32]);
+            // element mask: visible keys of this tile form a prefix [0, lim)
+            const int k0 = j * kBlockN;
+            int lim = min(kBlockN, sched.L - k0);
+            if (p.causal) lim = min(lim, i - k0 + 1);
+            if (lim < kBlockN) {
+#pragma unroll
+                for (int c = 0; c < kBlockN; ++c)
+                    if (c >= lim) s[c] = -INFINITY;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, s[c]);
+            const float mt = mx * p.scale_log2;  // scale_log2 > 0
+            const bool raise = mt > m + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, raise) && it > 0) {
+                // O must hold P_{it-1} V_{it-1} before it is rescaled
+                if (!mbar_wait(&st->pv_done, (it - 1) & 1, wctx, 21)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float alpha = raise ? ex2_approx(m - mt) : 1.f;
+                const uint32_t obase = tmem + lane_base + Cfg::kColO;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(obase + c * 32, orr);
+                    tmem_ld_wait();
+                    reg_fence(orr);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) orr[x] = __float_as_uint(__uint_as_float(orr[x]) * alpha);
+                    tmem_st32(obase + c * 32, orr);
+                }
+                if (raise) l *= alpha;
+            }
+            if (raise) m = mt;
+            const float mref = (m == -INFINITY) ? 0.f : m;
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c) {
+                const float pe = ex2_approx(fmaf(s[c], p.scale_log2, -mref));
+                s[c] = pe;
+                rs += pe;
+            }
+            l += rs;
+            if (p.dropout) {
+#pragma unroll
+                for (int g = 0; g < kBlockN / 4; ++g) {
+                    const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, i, (k0 >> 2) + g);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                        if (!((bits >> w) & 1u)) s[4 * g + w] = 0.f;
+                }
+            }
+            uint32_t pk[2][32];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) pk[c / 32][c % 32] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
+            tmem_st32(sbase, pk[0]);
+            tmem_st32(sbase + 32, pk[1]);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&st->p_full[buf]);
+        }
+        // epilogue
+        __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N) * D;
+        if (ok && n_active > 0) {
+            if (mbar_wait(&st->pv_done, (n_active - 1) & 1, wctx, 22)) {
+                tc_fence_after();
+                const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+                const uint32_t obase = tmem + lane_base + Cfg::kColO;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(obase + c * 32, orr);
+                    tmem_ld_wait();
+                    reg_fence(orr);
+                    if (i < p.N) {
+                        uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w4;
+                            w4.x = pack_bf16x2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
+                            w4.y = pack_bf16x2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
+                            w4.z = pack_bf16x2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
+                            w4.w = pack_bf16x2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
+                            dst[v] = w4;
+                        }
+                    }
+                }
+                if (i < p.N) p.lse[(size_t)bh * p.N + i] = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+            }
+        } else if (n_active == 0 && i < p.N) {
+            uint4 z = make_uint4(0, 0, 0, 0);
+            uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D);
+#pragma unroll
+            for (int v = 0; v < D / 8; ++v) dst[v] = z;
+            p.lse[(size_t)bh * p.N + i] = -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, Cfg::kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+}  // namespace
+
+// [B*H, N, d] bf16 viewed as a 3-D tensor (d fastest); boxes of 64 x rows.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D>
+int launch_fwd_tc_d(const Problem& pr) {
+    using Cfg = FwdCfg<D>;
+    CUtensorMap tq, tk, tv;
+    const int BH = pr.B * pr.H;
+    if (!make_tmap_bf16(&tq, pr.q, BH, pr.N, D, kBlockM) || !make_tmap_bf16(&tk, pr.k, BH, pr.N, D, kBlockN) ||
+        !make_tmap_bf16(&tv, pr.v, BH, pr.N, D, kBlockN))
+        return FA_ERR_CUDA;
+    FwdParams p{};
+    p.lse = pr.lse;
+    p.o = pr.o;
+    p.block_mask = pr.block_mask;
+    p.kv_len = pr.kv_len;
+    p.status = pr.status;
+    p.H = pr.H;
+    p.N = pr.N;
+    p.nb = pr.nb;
+    p.n_qtiles = (pr.N + kBlockM - 1) / kBlockM;
+    p.scale_log2 = pr.scale * kLog2e;
+    p.out_scale = 1.0f / (1.0f - pr.dropout_p);
+    p.drop_thr = pr.drop_threshold;
+    p.dropout = pr.dropout_p > 0.f;
+    p.causal = pr.causal;
+    p.seed = pr.seed;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem) !=
+            cudaSuccess)
+            return FA_ERR_CUDA;
+        attr_set = true;
+    }
+    dim3 grid(p.n_qtiles, BH);
+    fwd_tc_kernel<D><<<grid, kThreads, Cfg::kSmem, pr.stream>>>(tq, tk, tv, p);
+    note_launches(1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: fwd_tc launch: %s\n", cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+int launch_fwd_tc(const Problem& p) {
+    if (!(p.scale > 0.f)) return launch_fwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return p.d == 64 ? launch_fwd_tc_d<64>(p) : launch_fwd_tc_d<128>(p);
+}
+
 }  // namespace fa
