@@ -82,6 +82,7 @@ struct SharedState {
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t pv_done;
+    uint64_t o_final;
     uint64_t teardown;
     uint32_t tmem_base;
     int abort_flag;
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&st->p_full[i], kSoftmaxThreads);
         }
         mbar_init(&st->pv_done, 1);
+        mbar_init(&st->o_final, 1);
         mbar_init(&st->teardown, 1);
         st->abort_flag = 0;
         fence_mbar_init();
@@ -272,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 release_tile();
                 mma_commit(&st->pv_done);
+                if (j + 1 == n_active) mma_commit(&st->o_final);
                 if (j + 2 < n_active) ok = issue_s(buf);
             }
             // every MMA this thread issued has completed before TMEM is freed
@@ -319,7 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mt = mx * p.scale_log2;  // scale_log2 > 0
             const bool raise = mt > m + kRescaleThreshold;
             if (__any_sync(0xffffffffu, raise) && it > 0) {
-                // O must hold P_{it-1} V_{it-1} before it is rescaled
+                // O must hold P_{it-1} V_{it-1} before it is rescaled. S_it
+                // was committed after P_{it-2} V_{it-2}, so pv_done has
+                // completed it-1 or it phases and the parity is unambiguous.
                 if (!mbar_wait(&st->pv_done, (it - 1) & 1, wctx, 21)) {
                     ok = false;
                     break;
@@ -370,7 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue
         __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N) * D;
         if (ok && n_active > 0) {
-            if (mbar_wait(&st->pv_done, (n_active - 1) & 1, wctx, 22)) {
+            // pv_done may still be two phases behind here (the last S MMA
+            // was issued before the second-to-last P V), so the final O has
+            // its own single-phase barrier
+            if (mbar_wait(&st->o_final, 0, wctx, 22)) {
                 tc_fence_after();
                 const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
                 const uint32_t obase = tmem + lane_base + Cfg::kColO;
