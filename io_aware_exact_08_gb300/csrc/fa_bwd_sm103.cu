@@ -1,5 +1,558 @@
-// Placeholder: backward tensor-core path routes to the CUDA-core kernels.
+// Backward attention on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// The backward keeps only O and the per-row log-sum-exp from the forward and
+// recomputes S and P tile by tile on chip ("FlashAttention: Fast and
+// Memory-Efficient Exact Attention with IO-Awareness", section "Ide Utama",
+// third point; "FlashAttention" blog post, section "Recomputation"). With
+// P^ = P o Z/(1-p) the dropped-out probabilities, the gradients are
+//   dV = P^T dO,  dP = (dO V^T) o Z/(1-p),  dS = P o (dP - rowsum(dO o O)),
+//   dK = scale dS^T Q,  dQ = scale dS K.
+//
+// Three launches:
+//   1. preprocess: delta_i = sum_c dO_ic O_ic (fp32) and dQacc = 0;
+//   2. main: one CTA per (128-key tile K_j/V_j, batch*head), looping over the
+//      query tiles i that see it. Per tile, on tensor cores:
+//        S^T = K_j Q_i^T,  dP^T = V_j dO_i^T          (TMEM, fp32)
+//      eight compute warps (thread = key row, half of the 128 query columns
+//      each) rebuild P^T = exp(S^T - LSE), apply masks and dropout, and form
+//      dS^T = P^T o (dP^T - delta); P^T (bf16) goes back into TMEM and dS^T
+//      (bf16) into a swizzled shared-memory tile, then
+//        dV_j += P^T dO_i  (A from TMEM),  dK_j += dS^T Q_i,
+//        dQ_i  = dS K_j    (the same dS^T tile read MN-major)
+//      and the compute warps add dQ_i into the fp32 accumulator in global
+//      memory with vector atomics. dK_j, dV_j stay in TMEM until the end.
+//   3. convert: dq = dtype(scale * dQacc).
+// Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "fa_device.cuh"
 #include "fa_internal.h"
+#include "fa_sm103.cuh"
+
 namespace fa {
-int launch_bwd_tc(const Problem& p) { return launch_bwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
+
+namespace {
+
+using namespace sm103;
+
+constexpr int kTile = 128;          // keys per CTA, queries per step
+constexpr int kComputeThreads = 256;
+constexpr int kThreads = 320;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kStages = (D == 128) ? 2 : 3;
+    static constexpr int kTileBytes = kTile * D * 2;  // one 128 x D bf16 tile
+    static constexpr int kBoxBytes = kTile * 128;     // 128 rows x 64 columns
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kStageBytes = 2 * kTileBytes;  // Q_i and dO_i
+    static constexpr int kDsBytes = kTile * kTile * 2;  // dS^T, 128 x 128 bf16
+    static constexpr int kSmem =
+        1024 + 2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBytes + 2 * kTile * 4 /*lse, delta*/ + 256;
+    static constexpr uint32_t kColS = 0, kColDP = 128;
+    static constexpr uint32_t kColDQ = (D == 128) ? 128 : 256;  // aliases dP^T at D = 128
+    static constexpr uint32_t kColDV = (D == 128) ? 256 : 320;
+    static constexpr uint32_t kColDK = (D == 128) ? 384 : 384;
+};
+
+struct BwdParams {
+    const float* lse;
+    const float* delta;
+    float* dq_acc;
+    void* dk;
+    void* dv;
+    const uint8_t* block_mask;
+    const int32_t* kv_len;
+    int* status;
+    int H, N, nb;
+    float scale;
+    float scale_log2;
+    float keep_scale;  // 1/(1-p)
+    uint32_t drop_thr;
+    int dropout;
+    int causal;
+    uint64_t seed;
+};
+
+struct BwdShared {
+    uint64_t kv_full;
+    uint64_t st_full[3];
+    uint64_t st_empty[3];
+    uint64_t s_full;
+    uint64_t p_ready;
+    uint64_t dq_full;
+    uint64_t dq_free;
+    uint64_t acc_done;
+    uint64_t teardown;
+    uint64_t lse_ready;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Query tiles that see key tile j, in increasing order.
+struct QSched {
+    int jt, nqt, L, causal, nb;
+    const uint8_t* bm;
+    __device__ bool key_tile_live() const { return jt * kTile < L; }
+    __device__ bool active(int i) const {
+        if (causal && i * kTile + kTile - 1 < jt * kTile) return false;
+        if (bm && !bm[(size_t)i * nb + jt]) return false;
+        return true;
+    }
+    __device__ int next(int i) const {
+        while (i < nqt && !active(i)) ++i;
+        return i;
+    }
+    __device__ int count() const {
+        if (!key_tile_live()) return 0;
+        int c = 0;
+        for (int i = next(0); i < nqt; i = next(i + 1)) ++c;
+        return c;
+    }
+};
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdParams p) {
+    using Cfg = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sK = smem;
+    uint8_t* sV = sK + Cfg::kTileBytes;
+    uint8_t* sStages = sV + Cfg::kTileBytes;
+    uint8_t* sDS = sStages + Cfg::kStages * Cfg::kStageBytes;
+    float* sLse = reinterpret_cast<float*>(sDS + Cfg::kDsBytes);
+    float* sDelta = sLse + kTile;
+    BwdShared* st = reinterpret_cast<BwdShared*>(sDelta + kTile);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.y;
+    const int b = bh / p.H, h = bh % p.H;
+    const int jt = blockIdx.x;
+    const int j0 = jt * kTile;
+
+    QSched sched;
+    sched.jt = jt;
+    sched.nqt = (p.N + kTile - 1) / kTile;
+    sched.L = p.kv_len ? min(max(p.kv_len[b], 0), p.N) : p.N;
+    sched.causal = p.causal;
+    sched.nb = p.nb;
+    sched.bm = p.block_mask;
+    WaitCtx wctx{&st->abort_flag, p.status};
+
+    if (tid == 0) {
+        mbar_init(&st->kv_full, 1);
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            mbar_init(&st->st_full[s], 1);
+            mbar_init(&st->st_empty[s], 1);
+        }
+        mbar_init(&st->s_full, 1);
+        mbar_init(&st->p_ready, kComputeThreads);
+        mbar_init(&st->dq_full, 1);
+        mbar_init(&st->dq_free, kComputeThreads);
+        mbar_init(&st->acc_done, 1);
+        mbar_init(&st->teardown, 1);
+        mbar_init(&st->lse_ready, kComputeThreads);
+        st->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(&st->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = st->tmem_base;
+    const int n_active = sched.count();
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n_active > 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(&st->kv_full, 2 * Cfg::kTileBytes);
+#pragma unroll
+            for (int x = 0; x < Cfg::kBoxes; ++x) {
+                tma_load_3d(sK + x * Cfg::kBoxBytes, &tm_k, &st->kv_full, x * 64, j0, bh);
+                tma_load_3d(sV + x * Cfg::kBoxBytes, &tm_v, &st->kv_full, x * 64, j0, bh);
+            }
+            uint32_t issued_phase[Cfg::kStages];
+            bool issued_any[Cfg::kStages];
+            for (int s = 0; s < Cfg::kStages; ++s) issued_any[s] = false;
+            int t = 0;
+            for (int i = sched.next(0); i < sched.nqt; i = sched.next(i + 1), ++t) {
+                const int s = t % Cfg::kStages;
+                const uint32_t ph = (t / Cfg::kStages) & 1;
+                if (!mbar_wait(&st->st_empty[s], ph ^ 1, wctx, 101)) break;
+                mbar_arrive_expect_tx(&st->st_full[s], Cfg::kStageBytes);
+                uint8_t* dq = sStages + s * Cfg::kStageBytes;
+                uint8_t* ddo = dq + Cfg::kTileBytes;
+#pragma unroll
+                for (int x = 0; x < Cfg::kBoxes; ++x) {
+                    tma_load_3d(dq + x * Cfg::kBoxBytes, &tm_q, &st->st_full[s], x * 64, i * kTile, bh);
+                    tma_load_3d(ddo + x * Cfg::kBoxBytes, &tm_do, &st->st_full[s], x * 64, i * kTile, bh);
+                }
+                issued_phase[s] = ph;
+                issued_any[s] = true;
+            }
+            for (int s = 0; s < Cfg::kStages; ++s)
+                if (issued_any[s]) mbar_wait(&st->st_full[s], issued_phase[s], wctx, 102);
+            mbar_wait(&st->kv_full, 0, wctx, 103);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n_active > 0) {
+            constexpr uint32_t id_sq = idesc_bf16_f32(kTile, kTile, 0, 0);  // S^T, dP^T
+            constexpr uint32_t id_dv = idesc_bf16_f32(kTile, D, 0, 1);      // dV (A tmem), dK (A K-major)
+            constexpr uint32_t id_dq = idesc_bf16_f32(kTile, D, 1, 1);      // dQ (A MN-major)
+            const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
+            bool ok = mbar_wait(&st->kv_full, 0, wctx, 110);
+            tc_fence_after();
+            for (int it = 0; ok && it < n_active; ++it) {
+                const int s = it % Cfg::kStages;
+                if (!mbar_wait(&st->st_full[s], (it / Cfg::kStages) & 1, wctx, 111)) break;
+                tc_fence_after();
+                const uint32_t q_base = smem_u32(sStages + s * Cfg::kStageBytes);
+                const uint32_t do_base = q_base + Cfg::kTileBytes;
+                // S^T = K_j Q_i^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                    mma_ss(tmem + Cfg::kColS, smem_desc_sw128(k_base + off, 16, 1024),
+                           smem_desc_sw128(q_base + off, 16, 1024), id_sq, kk > 0);
+                }
+                // dP^T = V_j dO_i^T (at D = 128 it overwrites the previous dQ)
+                if (D == 128 && it > 0) {
+                    if (!mbar_wait(&st->dq_free, (it - 1) & 1, wctx, 112)) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                    mma_ss(tmem + Cfg::kColDP, smem_desc_sw128(v_base + off, 16, 1024),
+                           smem_desc_sw128(do_base + off, 16, 1024), id_sq, kk > 0);
+                }
+                mma_commit(&st->s_full);
+                if (!mbar_wait(&st->p_ready, it & 1, wctx, 113)) break;
+                tc_fence_after();
+                // dV += P^T dO_i: P^T (bf16) sits in TMEM, queries 0-63 at
+                // columns 0-31 and queries 64-127 at columns 64-95
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    const uint32_t a_col = Cfg::kColS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+                    mma_ts(tmem + Cfg::kColDV, tmem + a_col,
+                           smem_desc_sw128(do_base + kk * 2048, Cfg::kBoxBytes, 1024), id_dv,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                // dK += dS^T Q_i (dS^T K-major over queries)
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
+                    mma_ss(tmem + Cfg::kColDK, smem_desc_sw128(ds_base + off, 16, 1024),
+                           smem_desc_sw128(q_base + kk * 2048, Cfg::kBoxBytes, 1024), id_dv,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&st->st_empty[s]);
+                // dQ_i = dS K_j (the same tile read MN-major: M = queries)
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    mma_ss(tmem + Cfg::kColDQ, smem_desc_sw128(ds_base + kk * 2048, kTile * 128, 1024),
+                           smem_desc_sw128(k_base + kk * 2048, Cfg::kBoxBytes, 1024), id_dq, kk > 0);
+                }
+                mma_commit(&st->dq_full);
+            }
+            mma_commit(&st->acc_done);
+            mma_commit(&st->teardown);
+            mbar_wait(&st->teardown, 0, wctx, 114);
+        }
+    } else {
+        // ------------------------------------------------------------ compute
+        const int quarter = warp & 3;      // TMEM lane quarter
+        const int half = warp >> 2;        // query columns [64*half, 64*half + 64)
+        const int r = quarter * 32 + lane;  // key row within the tile
+        const int jrow = j0 + r;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const bool key_ok = jrow < sched.L;
+        bool ok = true;
+        int it = 0;
+        for (int i = sched.next(0); n_active > 0 && i < sched.nqt; i = sched.next(i + 1), ++it) {
+            const int i0 = i * kTile;
+            // per-query LSE (log2 units; +inf for masked rows so P = 0) and delta
+            {
+                const int c = tid & 127;
+                const int qi = i0 + c;
+                if (tid < 128) {
+                    float l = (qi < p.N) ? p.lse[(size_t)bh * p.N + qi] : -INFINITY;
+                    sLse[c] = (l == -INFINITY) ? INFINITY : l * kLog2e;
+                } else {
+                    sDelta[c] = (qi < p.N) ? p.delta[(size_t)bh * p.N + qi] : 0.f;
+                }
+            }
+            // (an mbarrier rather than a named barrier, so the wait is bounded)
+            mbar_arrive(&st->lse_ready);
+            if (!mbar_wait(&st->lse_ready, it & 1, wctx, 123)) {
+                ok = false;
+                break;
+            }
+            if (!mbar_wait(&st->s_full, it & 1, wctx, 120)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // visible queries of this key row form a suffix [cmin, 128) of the tile
+            int cmin = 0;
+            if (p.causal) cmin = max(0, jrow - i0);
+            const int cmax = key_ok ? min(kTile, p.N - i0) : 0;
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                const int cb = half * 64 + ch * 32;  // first query column of this chunk
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_base + Cfg::kColS + cb, sr);
+                tmem_ld32(tmem + lane_base + Cfg::kColDP + cb, dr);
+                tmem_ld_wait();
+                reg_fence(sr);
+                reg_fence(dr);
+                uint32_t keep = 0xffffffffu;
+                if (p.dropout) {
+                    keep = 0;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        // lane (4a + w) draws the 4 keep bits of keys 4a..4a+3
+                        // for query cb + 4g + w; the group exchanges them
+                        const int qi = i0 + cb + 4 * g + (lane & 3);
+                        const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, qi, jrow >> 2);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t v = __shfl_sync(0xffffffffu, bits, (lane & ~3) | q);
+                            keep |= ((v >> (lane & 3)) & 1u) << (4 * g + q);
+                        }
+                    }
+                }
+                uint32_t pk[16];
+                uint32_t dsk[16];
+#pragma unroll
+                for (int x = 0; x < 32; x += 2) {
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int y = 0; y < 2; ++y) {
+                        const int c = cb + x + y;
+                        const bool vis = (c >= cmin) && (c < cmax);
+                        const float pe =
+                            vis ? ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -sLse[c])) : 0.f;
+                        const float zk = ((keep >> (x + y)) & 1u) ? p.keep_scale : 0.f;
+                        pv[y] = pe * zk;
+                        dsv[y] = pe * (__uint_as_float(dr[x + y]) * zk - sDelta[c]);
+                    }
+                    pk[x / 2] = pack_bf16x2(pv[0], pv[1]);
+                    dsk[x / 2] = pack_bf16x2(dsv[0], dsv[1]);
+                }
+                // P^T into TMEM columns this warp has already read
+                tmem_st16(tmem + lane_base + Cfg::kColS + half * 64 + ch * 16, pk);
+                // dS^T row r, queries cb..cb+31: 4 swizzled 16-byte chunks
+                uint8_t* row = sDS + half * (kTile * 128) + r * 128;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int chunk = ch * 4 + v;
+                    uint4 w4 = make_uint4(dsk[4 * v], dsk[4 * v + 1], dsk[4 * v + 2], dsk[4 * v + 3]);
+                    *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = w4;
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&st->p_ready);
+            // dQ_i: this warp's 32 query rows, half of the D columns
+            if (!mbar_wait(&st->dq_full, it & 1, wctx, 121)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            {
+                const int qrow = i0 + r;  // TMEM lane = query row for dQ
+                float* dst = p.dq_acc + ((size_t)bh * p.N + qrow) * D + half * (D / 2);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t qr[32];
+                    tmem_ld32(tmem + lane_base + Cfg::kColDQ + half * (D / 2) + c * 32, qr);
+                    tmem_ld_wait();
+                    reg_fence(qr);
+                    if (qrow < p.N) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            float4 a = make_float4(__uint_as_float(qr[4 * v]), __uint_as_float(qr[4 * v + 1]),
+                                                   __uint_as_float(qr[4 * v + 2]), __uint_as_float(qr[4 * v + 3]));
+                            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + 4 * v), a);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&st->dq_free);
+        }
+        // epilogue: dK = scale * acc, dV = acc, rows of this key tile
+        __nv_bfloat16* dK = static_cast<__nv_bfloat16*>(p.dk) + ((size_t)bh * p.N) * D;
+        __nv_bfloat16* dV = static_cast<__nv_bfloat16*>(p.dv) + ((size_t)bh * p.N) * D;
+        const bool have = ok && n_active > 0 && mbar_wait(&st->acc_done, 0, wctx, 122);
+        if (have) tc_fence_after();
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            __nv_bfloat16* out = which ? dV : dK;
+            const float mul = which ? 1.f : p.scale;
+            const uint32_t col0 = (which ? Cfg::kColDV : Cfg::kColDK) + half * (D / 2);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t ar[32];
+                if (have) {
+                    tmem_ld32(tmem + lane_base + col0 + c * 32, ar);
+                    tmem_ld_wait();
+                    reg_fence(ar);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) ar[x] = 0u;
+                }
+                if (jrow < p.N) {
+                    uint4* dst = reinterpret_cast<uint4*>(out + (size_t)jrow * D + half * (D / 2) + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w4;
+                        w4.x = pack_bf16x2(__uint_as_float(ar[8 * v + 0]) * mul, __uint_as_float(ar[8 * v + 1]) * mul);
+                        w4.y = pack_bf16x2(__uint_as_float(ar[8 * v + 2]) * mul, __uint_as_float(ar[8 * v + 3]) * mul);
+                        w4.z = pack_bf16x2(__uint_as_float(ar[8 * v + 4]) * mul, __uint_as_float(ar[8 * v + 5]) * mul);
+                        w4.w = pack_bf16x2(__uint_as_float(ar[8 * v + 6]) * mul, __uint_as_float(ar[8 * v + 7]) * mul);
+                        dst[v] = w4;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+// delta_i = sum_c dO_ic O_ic and dQacc = 0 (one warp per row, bf16 inputs).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_tc_kernel(const __nv_bfloat16* __restrict__ O,
+                                                         const __nv_bfloat16* __restrict__ dO,
+                                                         float* __restrict__ delta, float* __restrict__ dq_acc,
+                                                         size_t rows) {
+    const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    constexpr int PER = D / 32;  // elements per lane (2 or 4)
+    float s = 0.f;
+    const __nv_bfloat16* o = O + row * D + lane * PER;
+    const __nv_bfloat16* g = dO + row * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) s = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), s);
+    s = warp_sum(s);
+    if (lane == 0) delta[row] = s;
+    float* acc = dq_acc + row * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+}
+
+// dq = bf16(scale * dQacc), 4 elements per thread.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
+                                                         float scale, size_t n4) {
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n4) return;
+    const float4 a = acc[idx];
+    uint2 w;
+    w.x = pack_bf16x2(a.x * scale, a.y * scale);
+    w.y = pack_bf16x2(a.z * scale, a.w * scale);
+    dq[idx] = w;
+}
+
+template <int D>
+int launch_bwd_tc_d(const Problem& pr) {
+    using Cfg = BwdCfg<D>;
+    const int BH = pr.B * pr.H;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_bf16(&tq, pr.q, BH, pr.N, D, kTile) || !make_tmap_bf16(&tk, pr.k, BH, pr.N, D, kTile) ||
+        !make_tmap_bf16(&tv, pr.v, BH, pr.N, D, kTile) || !make_tmap_bf16(&tdo, pr.dO, BH, pr.N, D, kTile))
+        return FA_ERR_CUDA;
+    const size_t rows = (size_t)BH * pr.N;
+    bwd_pre_tc_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, pr.stream>>>(
+        static_cast<const __nv_bfloat16*>(pr.o), static_cast<const __nv_bfloat16*>(pr.dO), pr.delta, pr.dq_acc,
+        rows);
+    note_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+
+    BwdParams p{};
+    p.lse = pr.lse;
+    p.delta = pr.delta;
+    p.dq_acc = pr.dq_acc;
+    p.dk = pr.dk;
+    p.dv = pr.dv;
+    p.block_mask = pr.block_mask;
+    p.kv_len = pr.kv_len;
+    p.status = pr.status;
+    p.H = pr.H;
+    p.N = pr.N;
+    p.nb = pr.nb;
+    p.scale = pr.scale;
+    p.scale_log2 = pr.scale * kLog2e;
+    p.keep_scale = 1.0f / (1.0f - pr.dropout_p);
+    p.drop_thr = pr.drop_threshold;
+    p.dropout = pr.dropout_p > 0.f;
+    p.causal = pr.causal;
+    p.seed = pr.seed;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem) !=
+            cudaSuccess)
+            return FA_ERR_CUDA;
+        attr_set = true;
+    }
+    dim3 grid((pr.N + kTile - 1) / kTile, BH);
+    bwd_tc_kernel<D><<<grid, kThreads, Cfg::kSmem, pr.stream>>>(tq, tk, tv, tdo, p);
+    note_launches(1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: bwd_tc launch: %s\n", cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    }
+    const size_t n4 = rows * D / 4;
+    dq_convert_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, pr.stream>>>(
+        reinterpret_cast<const float4*>(pr.dq_acc), static_cast<uint2*>(pr.dq), pr.scale, n4);
+    note_launches(1);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_bwd_tc(const Problem& p) {
+    if (!(p.scale > 0.f)) return launch_bwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return p.d == 64 ? launch_bwd_tc_d<64>(p) : launch_bwd_tc_d<128>(p);
+}
+
 }  // namespace fa
