@@ -89,6 +89,31 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward for callers that cannot allocate device memory (a framework whose
+ * allocator already owns the device, a latency-bound path where cudaMalloc
+ * is not allowed, a plugin given only its tensors). The paper has no
+ * counterpart: this is a packaging of fa_bwd, with the same arguments and
+ * results minus the workspace. The workspace comes from a fixed array of
+ * FA_BWD_NOALLOC_SCRATCH_BYTES in device memory that the library holds on
+ * every GPU it is loaded on until exit; nothing is allocated per call.
+ *  - Returns FA_ERR_WORKSPACE, without launching, when
+ *    fa_bwd_workspace_size(B,H,N,d) exceeds that size (about
+ *    B*H*N*(d+1)*4 bytes).
+ *  - Calls share the array: calls whose kernels may overlap on the GPU
+ *    (unordered streams) race and give wrong results. Each call clears the
+ *    parts that must start at zero.
+ *  - The first call on a device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv,
+                   int B, int H, int N, int d, float scale, int causal,
+                   const uint8_t* block_mask, float dropout_p, uint64_t seed,
+                   fa_dtype dtype, const int32_t* kv_len, void* stream);
+
+/*
  * Bytes of backward workspace: rowsum(dO o O) (fp32 [B,H,N]) plus the fp32
  * dQ accumulator ([B,H,N,d]), each rounded up to 256 bytes. O(B*H*N*d): the
  * backward keeps no N x N state. Returns 0 for invalid sizes.

@@ -23,7 +23,7 @@ __all__ = [
     "FA_BF16", "FA_FP32", "FaError", "load_library", "library_path",
     "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
     "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
-    "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
+    "fa_bwd_noalloc", "FA_BWD_NOALLOC_SCRATCH_BYTES", "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
 ]
 
 FA_BF16 = 0
@@ -35,7 +35,11 @@ _lib = None
 _lock = threading.Lock()
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
-            "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count")
+            "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
+            "fa_bwd_noalloc")
+
+# Size of the fixed device array fa_bwd_noalloc takes its workspace from.
+FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 class FaError(RuntimeError):
@@ -75,6 +79,8 @@ def load_library(build_if_missing: bool = True):
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_set_kernel_path.argtypes = [I]
         lib.fa_set_kernel_path.restype = I
+        lib.fa_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, P]
+        lib.fa_bwd_noalloc.restype = I
         lib.fa_launch_count.argtypes = []
         lib.fa_launch_count.restype = ctypes.c_uint64
         _lib = lib
@@ -95,6 +101,17 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, block_mas
     return load_library().fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, int(causal), block_mask,
                                  dropout_p, seed & 0xFFFFFFFFFFFFFFFF, dtype, kv_len, workspace,
                                  workspace_bytes, stream)
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, block_mask, dropout_p, seed,
+                   dtype, kv_len, stream):
+    """fa_bwd without a caller-provided workspace: for callers that cannot
+    allocate device memory (their framework's allocator owns the device, or
+    allocation is not allowed on their path). The workspace is a fixed
+    FA_BWD_NOALLOC_SCRATCH_BYTES array inside the library; larger problems
+    are refused with FA_ERR_WORKSPACE, and overlapping calls race on it."""
+    return load_library().fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, int(causal),
+                                         block_mask, dropout_p, seed & 0xFFFFFFFFFFFFFFFF, dtype, kv_len, stream)
 
 
 def fa_bwd_workspace_size(B, H, N, d):
