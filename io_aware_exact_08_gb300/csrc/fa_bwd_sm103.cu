@@ -123,6 +123,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// dst[0..3] += v (fp32, no return value, relaxed, L2).
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -301,19 +307,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool key_ok = jrow < sched.L;
         bool ok = true;
         int it = 0;
-        for (int i = sched.next(0); n_active > 0 && i < sched.nqt; i = sched.next(i + 1), ++it) {
+        // thread t < 128 stages LSE of query column t, thread t >= 128 delta
+        // of column t - 128; the value for the next tile is loaded early
+        auto load_col = [&](int i) -> float {
+            const int qi = i * kTile + (tid & 127);
+            if (i >= sched.nqt || qi >= p.N) return tid < 128 ? -INFINITY : 0.f;
+            return tid < 128 ? p.lse[(size_t)bh * p.N + qi] : p.delta[(size_t)bh * p.N + qi];
+        };
+        int i_cur = sched.next(0);
+        float col_val = (n_active > 0) ? load_col(i_cur) : 0.f;
+        for (int i = i_cur; n_active > 0 && i < sched.nqt; ++it) {
             const int i0 = i * kTile;
+            const int i_next = sched.next(i + 1);
             // per-query LSE (log2 units; +inf for masked rows so P = 0) and delta
-            {
-                const int c = tid & 127;
-                const int qi = i0 + c;
-                if (tid < 128) {
-                    float l = (qi < p.N) ? p.lse[(size_t)bh * p.N + qi] : -INFINITY;
-                    sLse[c] = (l == -INFINITY) ? INFINITY : l * kLog2e;
-                } else {
-                    sDelta[c] = (qi < p.N) ? p.delta[(size_t)bh * p.N + qi] : 0.f;
-                }
-            }
+            if (tid < 128)
+                sLse[tid] = (col_val == -INFINITY) ? INFINITY : col_val * kLog2e;
+            else
+                sDelta[tid - 128] = col_val;
+            col_val = load_col(i_next);
             // (an mbarrier rather than a named barrier, so the wait is bounded)
             mbar_arrive(&st->lse_ready);
             if (!mbar_wait(&st->lse_ready, it & 1, wctx, 123)) {
@@ -354,6 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                float lsev[32], delv[32];
+#pragma unroll
+                for (int x = 0; x < 32; x += 4) {
+                    const float4 a = *reinterpret_cast<const float4*>(sLse + cb + x);
+                    const float4 d4 = *reinterpret_cast<const float4*>(sDelta + cb + x);
+                    lsev[x] = a.x, lsev[x + 1] = a.y, lsev[x + 2] = a.z, lsev[x + 3] = a.w;
+                    delv[x] = d4.x, delv[x + 1] = d4.y, delv[x + 2] = d4.z, delv[x + 3] = d4.w;
+                }
+                const bool edge = (cmin > cb) || (cmax < cb + 32);
                 uint32_t pk[16];
                 uint32_t dsk[16];
 #pragma unroll
@@ -362,12 +382,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int y = 0; y < 2; ++y) {
                         const int c = cb + x + y;
-                        const bool vis = (c >= cmin) && (c < cmax);
-                        const float pe =
-                            vis ? ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -sLse[c])) : 0.f;
-                        const float zk = ((keep >> (x + y)) & 1u) ? p.keep_scale : 0.f;
-                        pv[y] = pe * zk;
-                        dsv[y] = pe * (__uint_as_float(dr[x + y]) * zk - sDelta[c]);
+                        float pe = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lsev[x + y]));
+                        if (edge && !((c >= cmin) && (c < cmax))) pe = 0.f;
+                        if (p.dropout) {
+                            const float zk = ((keep >> (x + y)) & 1u) ? p.keep_scale : 0.f;
+                            pv[y] = pe * zk;
+                            dsv[y] = pe * fmaf(__uint_as_float(dr[x + y]), zk, -delv[x + y]);
+                        } else {
+                            pv[y] = pe;
+                            dsv[y] = pe * (__uint_as_float(dr[x + y]) - delv[x + y]);
+                        }
                     }
                     pk[x / 2] = pack_bf16x2(pv[0], pv[1]);
                     dsk[x / 2] = pack_bf16x2(dsv[0], dsv[1]);
@@ -404,16 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     reg_fence(qr);
                     if (qrow < p.N) {
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            float4 a = make_float4(__uint_as_float(qr[4 * v]), __uint_as_float(qr[4 * v + 1]),
-                                                   __uint_as_float(qr[4 * v + 2]), __uint_as_float(qr[4 * v + 3]));
-                            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + 4 * v), a);
-                        }
+                        for (int v = 0; v < 8; ++v)
+                            red_add_v4(dst + c * 32 + 4 * v, __uint_as_float(qr[4 * v]), __uint_as_float(qr[4 * v + 1]),
+                                       __uint_as_float(qr[4 * v + 2]), __uint_as_float(qr[4 * v + 3]));
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&st->dq_free);
+            i = i_next;
         }
         // epilogue: dK = scale * acc, dV = acc, rows of this key tile
         __nv_bfloat16* dK = static_cast<__nv_bfloat16*>(p.dk) + ((size_t)bh * p.N) * D;

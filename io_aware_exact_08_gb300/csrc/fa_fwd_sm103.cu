@@ -316,10 +316,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBlockN; ++c)
                     if (c >= lim) s[c] = -INFINITY;
             }
-            float mx = -INFINITY;
+            // row max as a tree of 16 independent partial maxima (a single
+            // running max would be a 128-long dependent chain)
+            float pm[16];
 #pragma unroll
-            for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, s[c]);
-            const float mt = mx * p.scale_log2;  // scale_log2 > 0
+            for (int c = 0; c < 16; ++c) pm[c] = fmaxf(s[c], s[c + 16]);
+#pragma unroll
+            for (int c = 32; c < kBlockN; c += 16) {
+#pragma unroll
+                for (int x = 0; x < 16; ++x) pm[x] = fmaxf(pm[x], s[c + x]);
+            }
+#pragma unroll
+            for (int w = 8; w > 0; w >>= 1) {
+#pragma unroll
+                for (int x = 0; x < w; ++x) pm[x] = fmaxf(pm[x], pm[x + w]);
+            }
+            const float mt = pm[0] * p.scale_log2;  // scale_log2 > 0
             const bool raise = mt > m + kRescaleThreshold;
             if (__any_sync(0xffffffffu, raise) && it > 0) {
                 // O must hold P_{it-1} V_{it-1} before it is rescaled. S_it
@@ -346,14 +358,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (raise) m = mt;
             const float mref = (m == -INFINITY) ? 0.f : m;
-            float rs = 0.f;
+            // exponentials and row sum, 8 independent partial sums
+            float ps[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) ps[x] = 0.f;
 #pragma unroll
             for (int c = 0; c < kBlockN; ++c) {
                 const float pe = ex2_approx(fmaf(s[c], p.scale_log2, -mref));
                 s[c] = pe;
-                rs += pe;
+                ps[c & 7] += pe;
             }
-            l += rs;
+#pragma unroll
+            for (int w = 4; w > 0; w >>= 1) {
+#pragma unroll
+                for (int x = 0; x < w; ++x) ps[x] += ps[x + w];
+            }
+            l += ps[0];
             if (p.dropout) {
 #pragma unroll
                 for (int g = 0; g < kBlockN / 4; ++g) {
