@@ -18,9 +18,11 @@
 //      dS^T = P^T o (dP^T - delta); P^T (bf16) goes back into TMEM and dS^T
 //      (bf16) into a swizzled shared-memory tile, then
 //        dV_j += P^T dO_i  (A from TMEM),  dK_j += dS^T Q_i,
-//        dQ_i  = dS K_j    (the same dS^T tile read MN-major)
-//      and the compute warps add dQ_i into the fp32 accumulator in global
-//      memory with vector atomics. dK_j, dV_j stay in TMEM until the end.
+//        dQ_i^T = K_j^T dS^T (both operands read MN-major)
+//      (at D = 128 computed transposed, dQ_i^T = K_j^T dS^T, so that a
+//      warp's reduction covers 32 consecutive floats of one row) and the
+//      compute warps add it into the fp32 accumulator in global memory.
+//      dK_j, dV_j stay in TMEM until the end.
 //   3. convert: dq = dtype(scale * dQacc).
 // Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer.
 #include <cmath>
@@ -58,9 +60,12 @@ struct BwdCfg {
     static constexpr int kSmem =
         1024 + 2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBytes + 2 * kTile * 4 /*lse, delta*/ + 256;
     static constexpr uint32_t kColS = 0, kColDP = 128;
-    static constexpr uint32_t kColDQ = (D == 128) ? 128 : 256;  // aliases dP^T at D = 128
+    // dQ accumulator. D = 128: dQ^T (lanes = head-dim rows, 128 query
+    // columns), aliasing dP^T. D = 64: dQ (lanes = query rows, 64 columns).
+    static constexpr bool kDqTransposed = (D == 128);
+    static constexpr uint32_t kColDQ = (D == 128) ? 128 : 256;
     static constexpr uint32_t kColDV = (D == 128) ? 256 : 320;
-    static constexpr uint32_t kColDK = (D == 128) ? 384 : 384;
+    static constexpr uint32_t kColDK = 384;
 };
 
 struct BwdParams {
@@ -123,20 +128,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// dst[0..3] += v (fp32, no return value, relaxed, L2).
+// dst[0..3] += (a, b, c, d) (fp32, no return value, relaxed, L2).
 __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
+// *dst += a (fp32, no return value, relaxed, L2).
+__device__ __forceinline__ void red_add_f32(float* dst, float a) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(a) : "memory");
 }
+
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -236,7 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && n_active > 0) {
             constexpr uint32_t id_sq = idesc_bf16_f32(kTile, kTile, 0, 0);  // S^T, dP^T
             constexpr uint32_t id_dv = idesc_bf16_f32(kTile, D, 0, 1);      // dV (A tmem), dK (A K-major)
-            constexpr uint32_t id_dq = idesc_bf16_f32(kTile, D, 1, 1);      // dQ (A MN-major)
+            constexpr uint32_t id_dqt = idesc_bf16_f32(kTile, kTile, 1, 1);  // dQ^T (A, B MN-major)
+            constexpr uint32_t id_dq = idesc_bf16_f32(kTile, D, 1, 1);       // dQ (A, B MN-major)
             const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
             bool ok = mbar_wait(&st->kv_full, 0, wctx, 110);
             tc_fence_after();
@@ -285,11 +288,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                            (it > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&st->st_empty[s]);
-                // dQ_i = dS K_j (the same tile read MN-major: M = queries)
+                if (Cfg::kDqTransposed) {
+                    // dQ_i^T = K_j^T dS^T: A = K_j read MN-major (M = head
+                    // dim), B = the dS^T tile read MN-major (N = queries).
+                    // Lane = head-dim index, so a warp's lanes hold 32
+                    // consecutive dQ elements of one query row.
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    mma_ss(tmem + Cfg::kColDQ, smem_desc_sw128(ds_base + kk * 2048, kTile * 128, 1024),
-                           smem_desc_sw128(k_base + kk * 2048, Cfg::kBoxBytes, 1024), id_dq, kk > 0);
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        mma_ss(tmem + Cfg::kColDQ, smem_desc_sw128(k_base + kk * 2048, kTile * 128, 1024),
+                               smem_desc_sw128(ds_base + kk * 2048, kTile * 128, 1024), id_dqt, kk > 0);
+                    }
+                } else {
+                    // dQ_i = dS K_j: A = the dS^T tile read MN-major (M =
+                    // queries), B = K_j read MN-major (N = head dim).
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        mma_ss(tmem + Cfg::kColDQ, smem_desc_sw128(ds_base + kk * 2048, kTile * 128, 1024),
+                               smem_desc_sw128(k_base + kk * 2048, Cfg::kBoxBytes, 1024), id_dq, kk > 0);
+                    }
                 }
                 mma_commit(&st->dq_full);
             }
@@ -417,25 +433,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            // Both layouts: read this warp's 64 dQ values into registers,
+            // release the TMEM (the next dP^T may overwrite it), then reduce.
             {
-                const int qrow = i0 + r;  // TMEM lane = query row for dQ
-                float* dst = p.dq_acc + ((size_t)bh * p.N + qrow) * D + half * (D / 2);
+                uint32_t qa[32], qb[32];
+                if (Cfg::kDqTransposed) {
+                    tmem_ld32(tmem + lane_base + Cfg::kColDQ + half * 64, qa);
+                    tmem_ld32(tmem + lane_base + Cfg::kColDQ + half * 64 + 32, qb);
+                } else {
+                    tmem_ld32(tmem + lane_base + Cfg::kColDQ + half * 32, qa);
+                }
+                tmem_ld_wait();
+                reg_fence(qa);
+                if (Cfg::kDqTransposed) reg_fence(qb);
+                tc_fence_before();
+                mbar_arrive(&st->dq_free);
+                if (Cfg::kDqTransposed) {
+                    // lane = head-dim index r; one reduction instruction covers
+                    // 32 consecutive floats of one query row
+                    float* dst = p.dq_acc + ((size_t)bh * p.N + i0) * D + r;
+                    const int nvalid = min(kTile, p.N - i0);
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t qr[32];
-                    tmem_ld32(tmem + lane_base + Cfg::kColDQ + half * (D / 2) + c * 32, qr);
-                    tmem_ld_wait();
-                    reg_fence(qr);
+                    for (int x = 0; x < 32; ++x)
+                        if (half * 64 + x < nvalid) red_add_f32(dst + (size_t)(half * 64 + x) * D, __uint_as_float(qa[x]));
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        if (half * 64 + 32 + x < nvalid)
+                            red_add_f32(dst + (size_t)(half * 64 + 32 + x) * D, __uint_as_float(qb[x]));
+                } else {
+                    // lane = query row; 32 consecutive columns of that row
+                    const int qrow = i0 + r;
+                    float* dst = p.dq_acc + ((size_t)bh * p.N + qrow) * D + half * 32;
                     if (qrow < p.N) {
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
-                            red_add_v4(dst + c * 32 + 4 * v, __uint_as_float(qr[4 * v]), __uint_as_float(qr[4 * v + 1]),
-                                       __uint_as_float(qr[4 * v + 2]), __uint_as_float(qr[4 * v + 3]));
+                            red_add_v4(dst + 4 * v, __uint_as_float(qa[4 * v]), __uint_as_float(qa[4 * v + 1]),
+                                       __uint_as_float(qa[4 * v + 2]), __uint_as_float(qa[4 * v + 3]));
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&st->dq_free);
             i = i_next;
         }
         // epilogue: dK = scale * acc, dV = acc, rows of this key tile
