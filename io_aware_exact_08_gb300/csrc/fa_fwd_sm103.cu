@@ -438,6 +438,346 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 5) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
+
+// ---------------------------------------------------------------------------
+// Two query tiles per CTA (256 rows), one softmax warpgroup per tile, sharing
+// one K/V stream. The MMA warp issues, per key tile u,
+//     P_0(u) V_u, S_0(u+1), P_1(u) V_u, S_1(u+1)
+// so the softmax of one tile runs while the tensor core works on the other
+// (the ping-pong of the FlashAttention-4 design). Used when both tiles visit
+// the same key tiles up to their own count (no block mask): tile t visits
+// key tiles 0 .. n_t - 1.
+// Roles (320 threads): warps 0-3 softmax of tile 0, warps 4-7 softmax of
+// tile 1, warp 8 TMA producer, warp 9 MMA issuer.
+// ---------------------------------------------------------------------------
+constexpr int kThreadsPP = 320;
+
+template <int D>
+struct FwdPPCfg {
+    static constexpr int kStages = (D == 128) ? 4 : 8;
+    static constexpr int kTileBytes = kBlockN * D * 2;
+    static constexpr int kQBytes = kBlockM * D * 2;  // per query tile
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kBoxBytes = kBlockN * 128;
+    static constexpr int kSmem = 1024 + 2 * kQBytes + kStages * kTileBytes + 256;
+    static constexpr uint32_t kTmemCols = 512;
+    // S_t at columns 128 t, O_t at 256 + D t
+};
+
+struct SharedPP {
+    uint64_t kv_full[8];
+    uint64_t kv_empty[8];
+    uint64_t q_full;
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_final[2];
+    uint64_t teardown;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsPP, 1)
+    fwd_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using Cfg = FwdPPCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;  // tile t at t * kQBytes
+    uint8_t* sKV = smem + 2 * Cfg::kQBytes;
+    SharedPP* st = reinterpret_cast<SharedPP*>(sKV + Cfg::kStages * Cfg::kTileBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.y;
+    const int b = bh / p.H, h = bh % p.H;
+    const int n_pairs = (p.n_qtiles + 1) / 2;
+    const int pair = p.causal ? (n_pairs - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    const int L = p.kv_len ? min(max(p.kv_len[b], 0), p.N) : p.N;
+    const int nkt = (L + kBlockN - 1) / kBlockN;  // key tiles with a visible key
+    // key tiles visited by query tile t of this CTA (0 if the tile is past N)
+    int n_t[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int qt = 2 * pair + t;
+        n_t[t] = (qt < p.n_qtiles) ? (p.causal ? min(nkt, qt + 1) : nkt) : 0;
+    }
+    const int n_max = max(n_t[0], n_t[1]);
+    WaitCtx wctx{&st->abort_flag, p.status};
+
+    if (tid == 0) {
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            mbar_init(&st->kv_full[s], 1);
+            mbar_init(&st->kv_empty[s], 1);
+        }
+        mbar_init(&st->q_full, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&st->s_full[t], 1);
+            mbar_init(&st->p_full[t], kSoftmaxThreads);
+            mbar_init(&st->o_final[t], 1);
+        }
+        mbar_init(&st->teardown, 1);
+        st->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(&st->tmem_base, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = st->tmem_base;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n_max > 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            const int nq = (n_t[1] > 0) ? 2 : 1;
+            mbar_arrive_expect_tx(&st->q_full, nq * Cfg::kQBytes);
+            for (int t = 0; t < nq; ++t)
+#pragma unroll
+                for (int x = 0; x < Cfg::kBoxes; ++x)
+                    tma_load_3d(sQ + t * Cfg::kQBytes + x * Cfg::kBoxBytes, &tm_q, &st->q_full, x * 64,
+                                (2 * pair + t) * kBlockM, bh);
+            uint32_t issued_phase[Cfg::kStages];
+            bool issued_any[Cfg::kStages];
+            for (int s = 0; s < Cfg::kStages; ++s) issued_any[s] = false;
+            // load index 2u = K_u, 2u + 1 = V_u
+            bool ok = true;
+            for (int t = 0; ok && t < 2 * n_max; ++t) {
+                const int s = t % Cfg::kStages;
+                const uint32_t ph = (t / Cfg::kStages) & 1;
+                if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 61)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&st->kv_full[s], Cfg::kTileBytes);
+                uint8_t* dst = sKV + s * Cfg::kTileBytes;
+                const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
+#pragma unroll
+                for (int x = 0; x < Cfg::kBoxes; ++x)
+                    tma_load_3d(dst + x * Cfg::kBoxBytes, map, &st->kv_full[s], x * 64, (t >> 1) * kBlockN, bh);
+                issued_phase[s] = ph;
+                issued_any[s] = true;
+            }
+            for (int s = 0; s < Cfg::kStages; ++s)
+                if (issued_any[s]) mbar_wait(&st->kv_full[s], issued_phase[s], wctx, 62);
+            mbar_wait(&st->q_full, 0, wctx, 63);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n_max > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBlockM, D, 0, 1);
+            const uint32_t kv_base = smem_u32(sKV);
+            bool ok = mbar_wait(&st->q_full, 0, wctx, 70);
+            tc_fence_after();
+            // every load index is waited on once, before its first use
+            auto tile_addr = [&](int t_load, bool first_use) -> int {
+                const int s = t_load % Cfg::kStages;
+                if (first_use) {
+                    if (!mbar_wait(&st->kv_full[s], (t_load / Cfg::kStages) & 1, wctx, 71)) return -1;
+                    tc_fence_after();
+                }
+                return (int)(kv_base + s * Cfg::kTileBytes);
+            };
+            auto issue_s = [&](int t, int u, bool first_use, bool last_use) -> bool {
+                const int ka = tile_addr(2 * u, first_use);
+                if (ka < 0) return false;
+                const uint32_t q_base = smem_u32(sQ + t * Cfg::kQBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                    mma_ss(tmem + t * 128, smem_desc_sw128(q_base + off, 16, 1024),
+                           smem_desc_sw128((uint32_t)ka + off, 16, 1024), idesc_s, kk > 0);
+                }
+                mma_commit(&st->s_full[t]);
+                if (last_use) mma_commit(&st->kv_empty[(2 * u) % Cfg::kStages]);
+                return true;
+            };
+            auto issue_pv = [&](int t, int u, bool first_use, bool last_use) -> bool {
+                if (!mbar_wait(&st->p_full[t], u & 1, wctx, 72)) return false;
+                tc_fence_after();
+                const int va = tile_addr(2 * u + 1, first_use);
+                if (va < 0) return false;
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
+                           smem_desc_sw128((uint32_t)va + kk * 16 * 128, Cfg::kBoxBytes, 1024), idesc_o,
+                           (u > 0 || kk > 0) ? 1u : 0u);
+                if (last_use) mma_commit(&st->kv_empty[(2 * u + 1) % Cfg::kStages]);
+                if (u + 1 == n_t[t]) mma_commit(&st->o_final[t]);
+                return true;
+            };
+            // K_0 for both tiles
+            if (ok && n_t[0] > 0) ok = issue_s(0, 0, true, n_t[1] == 0);
+            if (ok && n_t[1] > 0) ok = issue_s(1, 0, n_t[0] == 0, true);
+            for (int u = 0; ok && u < n_max; ++u) {
+                const bool a0 = u < n_t[0], a1 = u < n_t[1];
+                const bool n0 = u + 1 < n_t[0], n1 = u + 1 < n_t[1];
+                if (a0) {
+                    ok = issue_pv(0, u, true, !a1);
+                    if (ok && n0) ok = issue_s(0, u + 1, true, !n1);
+                }
+                if (ok && a1) {
+                    ok = issue_pv(1, u, !a0, true);
+                    if (ok && n1) ok = issue_s(1, u + 1, !n0, true);
+                }
+            }
+            mma_commit(&st->teardown);
+            mbar_wait(&st->teardown, 0, wctx, 73);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int t = warp >> 2;  // query tile of this warpgroup
+        const int r = tid & 127;
+        const int i = (2 * pair + t) * kBlockM + r;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t sbase = tmem + lane_base + t * 128;
+        const uint32_t obase = tmem + lane_base + 256 + t * D;
+        const int n = n_t[t];
+        float m = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+        for (int u = 0; u < n; ++u) {
+            // dropout keep bits of this row's 128 keys (bit x of keep[c] is
+            // key 32c + x), drawn before S arrives
+            uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+            if (p.dropout) {
+#pragma unroll 1
+                for (int g = 0; g < 32; ++g) {
+                    const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, i, u * (kBlockN / 4) + g);
+                    if (g == 0) keep[0] = keep[1] = keep[2] = keep[3] = 0;
+                    const uint32_t sh = bits << (4 * (g & 7));
+                    if ((g >> 3) == 0) keep[0] |= sh;
+                    else if ((g >> 3) == 1) keep[1] |= sh;
+                    else if ((g >> 3) == 2) keep[2] |= sh;
+                    else keep[3] |= sh;
+                }
+            }
+            if (!mbar_wait(&st->s_full[t], u & 1, wctx, 80)) {
+                ok = false;
+                break;
+            }
+            // S_t(u) was issued after P_t(u-1) V: O_t is complete here
+            tc_fence_after();
+            const int k0 = u * kBlockN;
+            int lim = min(kBlockN, L - k0);
+            if (p.causal) lim = min(lim, i - k0 + 1);
+            const bool full = lim >= kBlockN;
+            // the whole row of S in registers, one TMEM wait
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(sbase + c * 32, sr[c]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+            if (!full) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        if (c * 32 + x >= lim) sr[c][x] = __float_as_uint(-INFINITY);
+            }
+            float pm[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) pm[x] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int x = 0; x < 32; ++x) pm[x & 7] = fmaxf(pm[x & 7], __uint_as_float(sr[c][x]));
+#pragma unroll
+            for (int w = 4; w > 0; w >>= 1) {
+#pragma unroll
+                for (int x = 0; x < w; ++x) pm[x] = fmaxf(pm[x], pm[x + w]);
+            }
+            const float mt = pm[0] * p.scale_log2;
+            const bool raise = mt > m + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, raise) && u > 0) {
+                const float alpha = raise ? ex2_approx(m - mt) : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 8; ++c) {
+                    uint32_t orr[8];
+                    tmem_ld8(obase + c * 8, orr);
+                    tmem_ld_wait();
+                    reg_fence8(orr);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) orr[x] = __float_as_uint(__uint_as_float(orr[x]) * alpha);
+                    tmem_st8(obase + c * 8, orr);
+                }
+                if (raise) l *= alpha;
+            }
+            if (raise) m = mt;
+            const float mref = (m == -INFINITY) ? 0.f : m;
+            float ps[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) ps[x] = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                // exponentials packed in place: pair x/2 overwrites word x/2,
+                // which has already been consumed
+#pragma unroll
+                for (int x = 0; x < 32; x += 2) {
+                    const float e0 = ex2_approx(fmaf(__uint_as_float(sr[c][x]), p.scale_log2, -mref));
+                    const float e1 = ex2_approx(fmaf(__uint_as_float(sr[c][x + 1]), p.scale_log2, -mref));
+                    ps[(x >> 1) & 3] += e0 + e1;
+                    sr[c][x >> 1] =
+                        pack_bf16x2(((keep[c] >> x) & 1u) ? e0 : 0.f, ((keep[c] >> (x + 1)) & 1u) ? e1 : 0.f);
+                }
+                // P chunk c lands in columns 16c..16c+15, already read
+                tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
+            }
+            ps[0] += ps[2];
+            ps[1] += ps[3];
+            ps[0] += ps[1];
+            l += ps[0];
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&st->p_full[t]);
+        }
+        __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N) * D;
+        if (ok && n > 0) {
+            if (mbar_wait(&st->o_final[t], 0, wctx, 81)) {
+                tc_fence_after();
+                const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(obase + c * 32, orr);
+                    tmem_ld_wait();
+                    reg_fence(orr);
+                    if (i < p.N) {
+                        uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w4;
+                            w4.x = pack_bf16x2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
+                            w4.y = pack_bf16x2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
+                            w4.z = pack_bf16x2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
+                            w4.w = pack_bf16x2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
+                            dst[v] = w4;
+                        }
+                    }
+                }
+                if (i < p.N) p.lse[(size_t)bh * p.N + i] = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+            }
+        } else if (n == 0 && i < p.N) {
+            uint4 z = make_uint4(0, 0, 0, 0);
+            uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D);
+#pragma unroll
+            for (int v = 0; v < D / 8; ++v) dst[v] = z;
+            p.lse[(size_t)bh * p.N + i] = -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem, Cfg::kTmemCols);
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -475,9 +815,10 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int BH, int N, int d, in
     return r == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool kPingPong>
 int launch_fwd_tc_d(const Problem& pr) {
-    using Cfg = FwdCfg<D>;
+    constexpr int kSmem = kPingPong ? FwdPPCfg<D>::kSmem : FwdCfg<D>::kSmem;
+    constexpr int kBlock = kPingPong ? kThreadsPP : kThreads;
     CUtensorMap tq, tk, tv;
     const int BH = pr.B * pr.H;
     if (!make_tmap_bf16(&tq, pr.q, BH, pr.N, D, kBlockM) || !make_tmap_bf16(&tk, pr.k, BH, pr.N, D, kBlockN) ||
@@ -499,15 +840,15 @@ int launch_fwd_tc_d(const Problem& pr) {
     p.dropout = pr.dropout_p > 0.f;
     p.causal = pr.causal;
     p.seed = pr.seed;
+    auto kernel = kPingPong ? fwd_pp_kernel<D> : fwd_tc_kernel<D>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
             return FA_ERR_CUDA;
         attr_set = true;
     }
-    dim3 grid(p.n_qtiles, BH);
-    fwd_tc_kernel<D><<<grid, kThreads, Cfg::kSmem, pr.stream>>>(tq, tk, tv, p);
+    dim3 grid(kPingPong ? (p.n_qtiles + 1) / 2 : p.n_qtiles, BH);
+    kernel<<<grid, kBlock, kSmem, pr.stream>>>(tq, tk, tv, p);
     note_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -519,7 +860,10 @@ int launch_fwd_tc_d(const Problem& pr) {
 
 int launch_fwd_tc(const Problem& p) {
     if (!(p.scale > 0.f)) return launch_fwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
-    return p.d == 64 ? launch_fwd_tc_d<64>(p) : launch_fwd_tc_d<128>(p);
+    // the two-tile kernel needs both tiles' key lists to be prefixes of one
+    // list (no block mask); block-sparse runs one query tile per CTA
+    if (p.block_mask) return p.d == 64 ? launch_fwd_tc_d<64, false>(p) : launch_fwd_tc_d<128, false>(p);
+    return p.d == 64 ? launch_fwd_tc_d<64, true>(p) : launch_fwd_tc_d<128, true>(p);
 }
 
 }  // namespace fa
