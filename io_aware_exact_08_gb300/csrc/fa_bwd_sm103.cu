@@ -241,6 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t id_dqt = idesc_bf16_f32(kTile, kTile, 1, 1);  // dQ^T (A, B MN-major)
             constexpr uint32_t id_dq = idesc_bf16_f32(kTile, D, 1, 1);       // dQ (A, B MN-major)
             const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
+            // descriptors built once, advanced by constants per MMA
+            const uint64_t kd_k = smem_desc_sw128(k_base, 16, 1024);         // K, K-major
+            const uint64_t vd_k = smem_desc_sw128(v_base, 16, 1024);         // V, K-major
+            const uint64_t dsd_k = smem_desc_sw128(ds_base, 16, 1024);       // dS^T, K-major
+            const uint64_t dsd_mn = smem_desc_sw128(ds_base, kTile * 128, 1024);  // dS^T, MN-major
+            const uint64_t kd_mn = smem_desc_sw128(k_base, Cfg::kBoxBytes, 1024);  // K, MN-major (N = d)
+            const uint64_t kd_mn2 = smem_desc_sw128(k_base, kTile * 128, 1024);    // K, MN-major (M = d)
             bool ok = mbar_wait(&st->kv_full, 0, wctx, 110);
             tc_fence_after();
             for (int it = 0; ok && it < n_active; ++it) {
@@ -249,12 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t q_base = smem_u32(sStages + s * Cfg::kStageBytes);
                 const uint32_t do_base = q_base + Cfg::kTileBytes;
+                const uint64_t qd_k = smem_desc_sw128(q_base, 16, 1024);
+                const uint64_t dod_k = smem_desc_sw128(do_base, 16, 1024);
+                const uint64_t qd_mn = smem_desc_sw128(q_base, Cfg::kBoxBytes, 1024);
+                const uint64_t dod_mn = smem_desc_sw128(do_base, Cfg::kBoxBytes, 1024);
                 // S^T = K_j Q_i^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                    mma_ss(tmem + Cfg::kColS, smem_desc_sw128(k_base + off, 16, 1024),
-                           smem_desc_sw128(q_base + off, 16, 1024), id_sq, kk > 0);
+                    mma_ss(tmem + Cfg::kColS, desc_add(kd_k, off), desc_add(qd_k, off), id_sq, kk > 0);
                 }
                 // dP^T = V_j dO_i^T (at D = 128 it overwrites the previous dQ)
                 if (D == 128 && it > 0) {
@@ -264,8 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                    mma_ss(tmem + Cfg::kColDP, smem_desc_sw128(v_base + off, 16, 1024),
-                           smem_desc_sw128(do_base + off, 16, 1024), id_sq, kk > 0);
+                    mma_ss(tmem + Cfg::kColDP, desc_add(vd_k, off), desc_add(dod_k, off), id_sq, kk > 0);
                 }
                 mma_commit(&st->s_full);
                 if (!mbar_wait(&st->p_ready, it & 1, wctx, 113)) break;
@@ -276,15 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     const uint32_t a_col = Cfg::kColS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
                     mma_ts(tmem + Cfg::kColDV, tmem + a_col,
-                           smem_desc_sw128(do_base + kk * 2048, Cfg::kBoxBytes, 1024), id_dv,
+                           desc_add(dod_mn, kk * 2048), id_dv,
                            (it > 0 || kk > 0) ? 1u : 0u);
                 }
                 // dK += dS^T Q_i (dS^T K-major over queries)
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-                    mma_ss(tmem + Cfg::kColDK, smem_desc_sw128(ds_base + off, 16, 1024),
-                           smem_desc_sw128(q_base + kk * 2048, Cfg::kBoxBytes, 1024), id_dv,
+                    mma_ss(tmem + Cfg::kColDK, desc_add(dsd_k, off), desc_add(qd_mn, kk * 2048), id_dv,
                            (it > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&st->st_empty[s]);
@@ -295,16 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // consecutive dQ elements of one query row.
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk) {
-                        mma_ss(tmem + Cfg::kColDQ, smem_desc_sw128(k_base + kk * 2048, kTile * 128, 1024),
-                               smem_desc_sw128(ds_base + kk * 2048, kTile * 128, 1024), id_dqt, kk > 0);
+                        mma_ss(tmem + Cfg::kColDQ, desc_add(kd_mn2, kk * 2048), desc_add(dsd_mn, kk * 2048), id_dqt,
+                               kk > 0);
                     }
                 } else {
                     // dQ_i = dS K_j: A = the dS^T tile read MN-major (M =
                     // queries), B = K_j read MN-major (N = head dim).
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk) {
-                        mma_ss(tmem + Cfg::kColDQ, smem_desc_sw128(ds_base + kk * 2048, kTile * 128, 1024),
-                               smem_desc_sw128(k_base + kk * 2048, Cfg::kBoxBytes, 1024), id_dq, kk > 0);
+                        mma_ss(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048), id_dq,
+                               kk > 0);
                     }
                 }
                 mma_commit(&st->dq_full);

@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBlockM, D, 0, 1);
             const uint32_t q_base = smem_u32(sQ);
             const uint32_t kv_base = smem_u32(sKV);
+            const uint64_t qd = smem_desc_sw128(q_base, 16, 1024);
             int t = 0;  // consume counter, same order as the producer
             bool ok = mbar_wait(&st->q_full, 0, wctx, 10);
             tc_fence_after();
@@ -246,11 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t kaddr;
                 if (!wait_tile(kaddr)) return false;
                 const uint32_t d = tmem + (buf ? Cfg::kColS1 : Cfg::kColS0);
+                const uint64_t kd = smem_desc_sw128(kaddr, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                    mma_ss(d, smem_desc_sw128(q_base + off, 16, 1024), smem_desc_sw128(kaddr + off, 16, 1024),
-                           idesc_s, kk > 0);
+                    mma_ss(d, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0);
                 }
                 mma_commit(&st->s_full[buf]);
                 release_tile();
@@ -265,11 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t vaddr;
                 if (!wait_tile(vaddr)) break;
                 const uint32_t a_tmem = tmem + (buf ? Cfg::kColS1 : Cfg::kColS0);
+                const uint64_t vd = smem_desc_sw128(vaddr, Cfg::kBoxBytes, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk) {
                     // P: 16 keys = 8 TMEM columns of bf16 pairs; V: 16 rows of 128 bytes
-                    mma_ts(tmem + Cfg::kColO, a_tmem + kk * 8,
-                           smem_desc_sw128(vaddr + kk * 16 * 128, Cfg::kBoxBytes, 1024), idesc_o,
+                    mma_ts(tmem + Cfg::kColO, a_tmem + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 release_tile();
@@ -541,29 +542,22 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                 for (int x = 0; x < Cfg::kBoxes; ++x)
                     tma_load_3d(sQ + t * Cfg::kQBytes + x * Cfg::kBoxBytes, &tm_q, &st->q_full, x * 64,
                                 (2 * pair + t) * kBlockM, bh);
-            uint32_t issued_phase[Cfg::kStages];
-            bool issued_any[Cfg::kStages];
-            for (int s = 0; s < Cfg::kStages; ++s) issued_any[s] = false;
             // load index 2u = K_u, 2u + 1 = V_u
-            bool ok = true;
-            for (int t = 0; ok && t < 2 * n_max; ++t) {
+            int t = 0;
+            for (; t < 2 * n_max; ++t) {
                 const int s = t % Cfg::kStages;
                 const uint32_t ph = (t / Cfg::kStages) & 1;
-                if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 61)) {
-                    ok = false;
-                    break;
-                }
+                if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 61)) break;
                 mbar_arrive_expect_tx(&st->kv_full[s], Cfg::kTileBytes);
                 uint8_t* dst = sKV + s * Cfg::kTileBytes;
                 const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
 #pragma unroll
                 for (int x = 0; x < Cfg::kBoxes; ++x)
                     tma_load_3d(dst + x * Cfg::kBoxBytes, map, &st->kv_full[s], x * 64, (t >> 1) * kBlockN, bh);
-                issued_phase[s] = ph;
-                issued_any[s] = true;
             }
-            for (int s = 0; s < Cfg::kStages; ++s)
-                if (issued_any[s]) mbar_wait(&st->kv_full[s], issued_phase[s], wctx, 62);
+            // drain: the last load issued into each stage has landed
+            for (int l = max(0, t - Cfg::kStages); l < t; ++l)
+                mbar_wait(&st->kv_full[l % Cfg::kStages], (l / Cfg::kStages) & 1, wctx, 62);
             mbar_wait(&st->q_full, 0, wctx, 63);
         }
     } else if (warp == 9) {
@@ -572,59 +566,89 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBlockM, D, 0, 1);
             const uint32_t kv_base = smem_u32(sKV);
+            const uint64_t qd0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t qd1 = smem_desc_sw128(smem_u32(sQ + Cfg::kQBytes), 16, 1024);
             bool ok = mbar_wait(&st->q_full, 0, wctx, 70);
             tc_fence_after();
-            // every load index is waited on once, before its first use
-            auto tile_addr = [&](int t_load, bool first_use) -> int {
-                const int s = t_load % Cfg::kStages;
-                if (first_use) {
-                    if (!mbar_wait(&st->kv_full[s], (t_load / Cfg::kStages) & 1, wctx, 71)) return -1;
-                    tc_fence_after();
-                }
-                return (int)(kv_base + s * Cfg::kTileBytes);
-            };
-            auto issue_s = [&](int t, int u, bool first_use, bool last_use) -> bool {
-                const int ka = tile_addr(2 * u, first_use);
-                if (ka < 0) return false;
-                const uint32_t q_base = smem_u32(sQ + t * Cfg::kQBytes);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                    mma_ss(tmem + t * 128, smem_desc_sw128(q_base + off, 16, 1024),
-                           smem_desc_sw128((uint32_t)ka + off, 16, 1024), idesc_s, kk > 0);
-                }
-                mma_commit(&st->s_full[t]);
-                if (last_use) mma_commit(&st->kv_empty[(2 * u) % Cfg::kStages]);
-                return true;
-            };
-            auto issue_pv = [&](int t, int u, bool first_use, bool last_use) -> bool {
-                if (!mbar_wait(&st->p_full[t], u & 1, wctx, 72)) return false;
+            // Straight-line issue code with every counter in registers: the
+            // single issuing thread has about 64 cycles per MMA to spare.
+            // Each load index is waited on once, before its first use.
+            const int c0 = n_t[0], c1 = n_t[1];
+            const uint64_t kvd_k = smem_desc_sw128(kv_base, 16, 1024);              // K tiles, K-major
+            const uint64_t kvd_v = smem_desc_sw128(kv_base, Cfg::kBoxBytes, 1024);  // V tiles, MN-major
+            constexpr uint32_t kStageUnits = Cfg::kTileBytes >> 4;
+            // S_t(0) = Q_t K_0^T
+            if (ok) {
+                ok = mbar_wait(&st->kv_full[0], 0, wctx, 71);
                 tc_fence_after();
-                const int va = tile_addr(2 * u + 1, first_use);
-                if (va < 0) return false;
+            }
+            if (ok) {
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
-                           smem_desc_sw128((uint32_t)va + kk * 16 * 128, Cfg::kBoxBytes, 1024), idesc_o,
-                           (u > 0 || kk > 0) ? 1u : 0u);
-                if (last_use) mma_commit(&st->kv_empty[(2 * u + 1) % Cfg::kStages]);
-                if (u + 1 == n_t[t]) mma_commit(&st->o_final[t]);
-                return true;
-            };
-            // K_0 for both tiles
-            if (ok && n_t[0] > 0) ok = issue_s(0, 0, true, n_t[1] == 0);
-            if (ok && n_t[1] > 0) ok = issue_s(1, 0, n_t[0] == 0, true);
+                for (int t = 0; t < 2; ++t) {
+                    if ((t ? c1 : c0) == 0) continue;
+                    const uint64_t qd = t ? qd1 : qd0;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                        mma_ss(tmem + t * 128, desc_add(qd, off), desc_add(kvd_k, off), idesc_s, kk > 0);
+                    }
+                    mma_commit(&st->s_full[t]);
+                }
+                mma_commit(&st->kv_empty[0]);
+            }
             for (int u = 0; ok && u < n_max; ++u) {
-                const bool a0 = u < n_t[0], a1 = u < n_t[1];
-                const bool n0 = u + 1 < n_t[0], n1 = u + 1 < n_t[1];
-                if (a0) {
-                    ok = issue_pv(0, u, true, !a1);
-                    if (ok && n0) ok = issue_s(0, u + 1, true, !n1);
+                const int lv = 2 * u + 1, lk = 2 * u + 2;  // load indices of V_u and K_{u+1}
+                const int sv = lv % Cfg::kStages, sk = lk % Cfg::kStages;
+                const uint64_t vd = kvd_v + (uint64_t)(sv * kStageUnits);
+                const uint64_t kd = kvd_k + (uint64_t)(sk * kStageUnits);
+                const bool need_k = (u + 1 < c0) || (u + 1 < c1);
+                bool v_ready = false, k_ready = false;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int ct = t ? c1 : c0;
+                    if (u >= ct) continue;
+                    // P_t(u) V_u
+                    if (!mbar_wait(&st->p_full[t], u & 1, wctx, 72)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (!v_ready) {
+                        if (!mbar_wait(&st->kv_full[sv], (lv / Cfg::kStages) & 1, wctx, 74)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        v_ready = true;
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < kBlockN / 16; ++kk)
+                        mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
+                               (u > 0 || kk > 0) ? 1u : 0u);
+                    if (u + 1 == ct) mma_commit(&st->o_final[t]);
+                    // S_t(u+1) = Q_t K_{u+1}^T over the S/P columns just read
+                    if (u + 1 < ct) {
+                        if (!k_ready) {
+                            if (!mbar_wait(&st->kv_full[sk], (lk / Cfg::kStages) & 1, wctx, 75)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            k_ready = true;
+                        }
+                        const uint64_t qd = t ? qd1 : qd0;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                            mma_ss(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0);
+                        }
+                        mma_commit(&st->s_full[t]);
+                    }
                 }
-                if (ok && a1) {
-                    ok = issue_pv(1, u, !a0, true);
-                    if (ok && n1) ok = issue_s(1, u + 1, !n0, true);
-                }
+                if (!ok) break;
+                // V_u and K_{u+1} are released after their last MMA
+                mma_commit(&st->kv_empty[sv]);
+                if (need_k) mma_commit(&st->kv_empty[sk]);
             }
             mma_commit(&st->teardown);
             mbar_wait(&st->teardown, 0, wctx, 73);

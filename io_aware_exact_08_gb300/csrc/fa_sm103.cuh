@@ -246,6 +246,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t start, uint32_t lbo
     return d;
 }
 
+// The descriptor of base's matrix moved by `bytes` (a multiple of 16): the
+// start-address field is the low 14 bits of address/16 and shared-memory
+// addresses stay below 2^18, so a plain add cannot carry into other fields.
+// Building each tile's descriptor once and advancing it by constants keeps
+// the single MMA-issuing thread fast enough to keep the tensor core fed.
+__device__ __forceinline__ uint64_t desc_add(uint64_t base, uint32_t bytes) { return base + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
 // Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B
 // format (1 = bf16), 15 A major (0 = K, 1 = MN), 16 B major, [17,23) N>>3,
