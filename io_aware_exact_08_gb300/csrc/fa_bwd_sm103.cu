@@ -178,12 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&st->st_empty[s], 1);
         }
         mbar_init(&st->s_full, 1);
-        mbar_init(&st->p_ready, kComputeThreads);
+        mbar_init(&st->p_ready, kComputeThreads / 32);
         mbar_init(&st->dq_full, 1);
-        mbar_init(&st->dq_free, kComputeThreads);
+        mbar_init(&st->dq_free, kComputeThreads / 32);
         mbar_init(&st->acc_done, 1);
         mbar_init(&st->teardown, 1);
-        mbar_init(&st->lse_ready, kComputeThreads);
+        mbar_init(&st->lse_ready, kComputeThreads / 32);
         st->abort_flag = 0;
         fence_mbar_init();
     }
@@ -350,12 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sDelta[tid - 128] = col_val;
             col_val = load_col(i_next);
             // (an mbarrier rather than a named barrier, so the wait is bounded)
-            mbar_arrive(&st->lse_ready);
-            if (!mbar_wait(&st->lse_ready, it & 1, wctx, 123)) {
+            mbar_arrive_warp(&st->lse_ready);
+            if (!mbar_wait_warp(&st->lse_ready, it & 1, wctx, 123)) {
                 ok = false;
                 break;
             }
-            if (!mbar_wait(&st->s_full, it & 1, wctx, 120)) {
+            if (!mbar_wait_warp(&st->s_full, it & 1, wctx, 120)) {
                 ok = false;
                 break;
             }
@@ -434,9 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&st->p_ready);
+            mbar_arrive_warp(&st->p_ready);
             // dQ_i: this warp's 32 query rows, half of the D columns
-            if (!mbar_wait(&st->dq_full, it & 1, wctx, 121)) {
+            if (!mbar_wait_warp(&st->dq_full, it & 1, wctx, 121)) {
                 ok = false;
                 break;
             }
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reg_fence(qa);
                 if (Cfg::kDqTransposed) reg_fence(qb);
                 tc_fence_before();
-                mbar_arrive(&st->dq_free);
+                mbar_arrive_warp(&st->dq_free);
                 if (Cfg::kDqTransposed) {
                     // lane = head-dim index r; one reduction instruction covers
                     // 32 consecutive floats of one query row
@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue: dK = scale * acc, dV = acc, rows of this key tile
         __nv_bfloat16* dK = static_cast<__nv_bfloat16*>(p.dk) + ((size_t)bh * p.N) * D;
         __nv_bfloat16* dV = static_cast<__nv_bfloat16*>(p.dv) + ((size_t)bh * p.N) * D;
-        const bool have = ok && n_active > 0 && mbar_wait(&st->acc_done, 0, wctx, 122);
+        const bool have = ok && n_active > 0 && mbar_wait_warp(&st->acc_done, 0, wctx, 122);
         if (have) tc_fence_after();
 #pragma unroll
         for (int which = 0; which < 2; ++which) {

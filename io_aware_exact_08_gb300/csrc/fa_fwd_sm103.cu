@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&st->q_full, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&st->s_full[i], 1);
-            mbar_init(&st->p_full[i], kSoftmaxThreads);
+            mbar_init(&st->p_full[i], kSoftmaxThreads / 32);
         }
         mbar_init(&st->pv_done, 1);
         mbar_init(&st->o_final, 1);
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < n_active; ++it, j = sched.next(j + 1)) {
             const int buf = it & 1;
             const uint32_t sbase = tmem + lane_base + (buf ? Cfg::kColS1 : Cfg::kColS0);
-            if (!mbar_wait(&st->s_full[buf], (it >> 1) & 1, wctx, 20)) {
+            if (!mbar_wait_warp(&st->s_full[buf], (it >> 1) & 1, wctx, 20)) {
                 ok = false;
                 break;
             }
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // O must hold P_{it-1} V_{it-1} before it is rescaled. S_it
                 // was committed after P_{it-2} V_{it-2}, so pv_done has
                 // completed it-1 or it phases and the parity is unambiguous.
-                if (!mbar_wait(&st->pv_done, (it - 1) & 1, wctx, 21)) {
+                if (!mbar_wait_warp(&st->pv_done, (it - 1) & 1, wctx, 21)) {
                     ok = false;
                     break;
                 }
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(sbase + 32, pk[1]);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&st->p_full[buf]);
+            mbar_arrive_warp(&st->p_full[buf]);
         }
         // epilogue
         __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N) * D;
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // pv_done may still be two phases behind here (the last S MMA
             // was issued before the second-to-last P V), so the final O has
             // its own single-phase barrier
-            if (mbar_wait(&st->o_final, 0, wctx, 22)) {
+            if (mbar_wait_warp(&st->o_final, 0, wctx, 22)) {
                 tc_fence_after();
                 const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
                 const uint32_t obase = tmem + lane_base + Cfg::kColO;
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         mbar_init(&st->q_full, 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(&st->s_full[t], 1);
-            mbar_init(&st->p_full[t], kSoftmaxThreads);
+            mbar_init(&st->p_full[t], kSoftmaxThreads / 32);
             mbar_init(&st->o_final[t], 1);
         }
         mbar_init(&st->teardown, 1);
@@ -681,7 +681,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                     else keep[3] |= sh;
                 }
             }
-            if (!mbar_wait(&st->s_full[t], u & 1, wctx, 80)) {
+            if (!mbar_wait_warp(&st->s_full[t], u & 1, wctx, 80)) {
                 ok = false;
                 break;
             }
@@ -759,11 +759,11 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             l += ps[0];
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&st->p_full[t]);
+            mbar_arrive_warp(&st->p_full[t]);
         }
         __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N) * D;
         if (ok && n > 0) {
-            if (mbar_wait(&st->o_final[t], 0, wctx, 81)) {
+            if (mbar_wait_warp(&st->o_final[t], 0, wctx, 81)) {
                 tc_fence_after();
                 const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
 #pragma unroll

@@ -41,6 +41,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrival per warp: every lane has finished its own writes (and, for
+// TMEM, its tcgen05.wait::st and tcgen05.fence::before_thread_sync); the warp
+// synchronises and lane 0 arrives with release semantics. The barrier is
+// initialised with the number of warps, not threads.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
@@ -84,6 +93,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
             }
         }
     }
+}
+
+// mbar_wait for warp-collective code: every lane waits, and the warp agrees
+// on the outcome (a lane that gave up makes the whole warp give up), so the
+// lanes never split around a later __syncwarp or .sync.aligned instruction.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitCtx& w, int site) {
+    const bool ok = mbar_wait(bar, parity, w, site);
+    return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------------------
