@@ -91,13 +91,13 @@ struct BwdShared {
     uint64_t kv_full;
     uint64_t st_full[3];
     uint64_t st_empty[3];
-    uint64_t s_full;
-    uint64_t p_ready;
-    uint64_t dq_full;
-    uint64_t dq_free;
+    uint64_t s_full[2];    // per 64-query half h: S^T_h and dP^T_h in TMEM
+    uint64_t p_ready[2];   // P^T_h in TMEM and dS^T_h in shared memory
+    uint64_t dq_full[2];   // dQ of half h (D = 128) / of the tile (D = 64, [0])
+    uint64_t dq_free[2];   // dQ^T_h read out of TMEM (D = 128)
     uint64_t acc_done;
     uint64_t teardown;
-    uint64_t lse_ready;
+    uint64_t lse_ready[2];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -177,13 +177,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&st->st_full[s], 1);
             mbar_init(&st->st_empty[s], 1);
         }
-        mbar_init(&st->s_full, 1);
-        mbar_init(&st->p_ready, kComputeThreads / 32);
-        mbar_init(&st->dq_full, 1);
-        mbar_init(&st->dq_free, kComputeThreads / 32);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&st->s_full[h], 1);
+            mbar_init(&st->p_ready[h], kComputeThreads / 64);
+            mbar_init(&st->dq_full[h], 1);
+            mbar_init(&st->dq_free[h], kComputeThreads / 64);
+            mbar_init(&st->lse_ready[h], kComputeThreads / 64);
+        }
         mbar_init(&st->acc_done, 1);
         mbar_init(&st->teardown, 1);
-        mbar_init(&st->lse_ready, kComputeThreads / 32);
         st->abort_flag = 0;
         fence_mbar_init();
     }
@@ -236,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n_active > 0) {
-            constexpr uint32_t id_sq = idesc_bf16_f32(kTile, kTile, 0, 0);  // S^T, dP^T
+            constexpr uint32_t id_sh = idesc_bf16_f32(kTile, 64, 0, 0);      // S^T_h, dP^T_h (N = 64)
             constexpr uint32_t id_dv = idesc_bf16_f32(kTile, D, 0, 1);      // dV (A tmem), dK (A K-major)
-            constexpr uint32_t id_dqt = idesc_bf16_f32(kTile, kTile, 1, 1);  // dQ^T (A, B MN-major)
+            constexpr uint32_t id_dqt_h = idesc_bf16_f32(kTile, 64, 1, 1);   // dQ^T_h (A, B MN-major, N = 64)
             constexpr uint32_t id_dq = idesc_bf16_f32(kTile, D, 1, 1);       // dQ (A, B MN-major)
             const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
             // descriptors built once, advanced by constants per MMA
@@ -260,62 +262,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dod_k = smem_desc_sw128(do_base, 16, 1024);
                 const uint64_t qd_mn = smem_desc_sw128(q_base, Cfg::kBoxBytes, 1024);
                 const uint64_t dod_mn = smem_desc_sw128(do_base, Cfg::kBoxBytes, 1024);
-                // S^T = K_j Q_i^T
+                // Per 64-query half h (h = 0, 1): S^T_h = K_j Q_{i,h}^T and
+                // dP^T_h = V_j dO_{i,h}^T (N = 64). Half 1's products run
+                // while the compute warps of half 0 work, and half 0's
+                // gradient MMAs while half 1's do.
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                    mma_ss(tmem + Cfg::kColS, desc_add(kd_k, off), desc_add(qd_k, off), id_sq, kk > 0);
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                        mma_ss(tmem + Cfg::kColS + 64 * h, desc_add(kd_k, off), desc_add(qd_k, off + 8192 * h), id_sh,
+                               kk > 0);
+                    }
+                    // at D = 128, dP^T_h overwrites the previous tile's dQ^T_h
+                    if (D == 128 && it > 0) {
+                        if (!mbar_wait(&st->dq_free[h], (it - 1) & 1, wctx, 112)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                        mma_ss(tmem + Cfg::kColDP + 64 * h, desc_add(vd_k, off), desc_add(dod_k, off + 8192 * h), id_sh,
+                               kk > 0);
+                    }
+                    mma_commit(&st->s_full[h]);
                 }
-                // dP^T = V_j dO_i^T (at D = 128 it overwrites the previous dQ)
-                if (D == 128 && it > 0) {
-                    if (!mbar_wait(&st->dq_free, (it - 1) & 1, wctx, 112)) break;
+                if (!ok) break;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (!mbar_wait(&st->p_ready[h], it & 1, wctx, 113)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                }
+                    // dV += P^T_h dO_h: P^T_h (bf16) in TMEM columns 64h..64h+31
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                    mma_ss(tmem + Cfg::kColDP, desc_add(vd_k, off), desc_add(dod_k, off), id_sq, kk > 0);
-                }
-                mma_commit(&st->s_full);
-                if (!mbar_wait(&st->p_ready, it & 1, wctx, 113)) break;
-                tc_fence_after();
-                // dV += P^T dO_i: P^T (bf16) sits in TMEM, queries 0-63 at
-                // columns 0-31 and queries 64-127 at columns 64-95
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
+                               desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
+                    // dK += dS^T_h Q_h (dS^T half h is shared-memory box h)
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint32_t a_col = Cfg::kColS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-                    mma_ts(tmem + Cfg::kColDV, tmem + a_col,
-                           desc_add(dod_mn, kk * 2048), id_dv,
-                           (it > 0 || kk > 0) ? 1u : 0u);
-                }
-                // dK += dS^T Q_i (dS^T K-major over queries)
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
+                               desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
+                    if (h == 1) mma_commit(&st->st_empty[s]);
+                    if (Cfg::kDqTransposed) {
+                        // dQ^T_h = K_j^T dS^T_h (M = head dim, N = 64 queries):
+                        // lane = head-dim index, so one reduction instruction
+                        // covers 32 consecutive floats of a dQ row
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-                    mma_ss(tmem + Cfg::kColDK, desc_add(dsd_k, off), desc_add(qd_mn, kk * 2048), id_dv,
-                           (it > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(&st->st_empty[s]);
-                if (Cfg::kDqTransposed) {
-                    // dQ_i^T = K_j^T dS^T: A = K_j read MN-major (M = head
-                    // dim), B = the dS^T tile read MN-major (N = queries).
-                    // Lane = head-dim index, so a warp's lanes hold 32
-                    // consecutive dQ elements of one query row.
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ss(tmem + Cfg::kColDQ + 64 * h, desc_add(kd_mn2, kk * 2048),
+                                   desc_add(dsd_mn, h * (kTile * 128) + kk * 2048), id_dqt_h, kk > 0);
+                        mma_commit(&st->dq_full[h]);
+                    } else if (h == 1) {
+                        // dQ = dS K_j over the whole tile (M = 128 queries, lane = query)
 #pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
-                        mma_ss(tmem + Cfg::kColDQ, desc_add(kd_mn2, kk * 2048), desc_add(dsd_mn, kk * 2048), id_dqt,
-                               kk > 0);
-                    }
-                } else {
-                    // dQ_i = dS K_j: A = the dS^T tile read MN-major (M =
-                    // queries), B = K_j read MN-major (N = head dim).
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
-                        mma_ss(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048), id_dq,
-                               kk > 0);
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ss(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048), id_dq,
+                                   kk > 0);
+                        mma_commit(&st->dq_full[0]);
                     }
                 }
-                mma_commit(&st->dq_full);
             }
             mma_commit(&st->acc_done);
             mma_commit(&st->teardown);
@@ -331,31 +342,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool key_ok = jrow < sched.L;
         bool ok = true;
         int it = 0;
-        // thread t < 128 stages LSE of query column t, thread t >= 128 delta
-        // of column t - 128; the value for the next tile is loaded early
-        auto load_col = [&](int i) -> float {
-            const int qi = i * kTile + (tid & 127);
-            if (i >= sched.nqt || qi >= p.N) return tid < 128 ? -INFINITY : 0.f;
-            return tid < 128 ? p.lse[(size_t)bh * p.N + qi] : p.delta[(size_t)bh * p.N + qi];
-        };
+        // each warpgroup stages its own 64 query columns: row r < 64 the LSE
+        // of column 64 half + r, row r >= 64 the delta of column
+        // 64 half + r - 64; the value for the next tile is loaded early
+        const int col = 64 * half + (r & 63);
+        const bool stage_lse = r < 64;
+        const float* col_src = (stage_lse ? p.lse : p.delta) + (size_t)bh * p.N;
+        const int nqt = sched.nqt;
         int i_cur = sched.next(0);
-        float col_val = (n_active > 0) ? load_col(i_cur) : 0.f;
+        float col_val = 0.f;
+        if (n_active > 0) {
+            const int qi = i_cur * kTile + col;
+            col_val = (qi < p.N) ? col_src[qi] : (stage_lse ? -INFINITY : 0.f);
+        }
         for (int i = i_cur; n_active > 0 && i < sched.nqt; ++it) {
             const int i0 = i * kTile;
             const int i_next = sched.next(i + 1);
             // per-query LSE (log2 units; +inf for masked rows so P = 0) and delta
-            if (tid < 128)
-                sLse[tid] = (col_val == -INFINITY) ? INFINITY : col_val * kLog2e;
+            if (stage_lse)
+                sLse[col] = (col_val == -INFINITY) ? INFINITY : col_val * kLog2e;
             else
-                sDelta[tid - 128] = col_val;
-            col_val = load_col(i_next);
+                sDelta[col] = col_val;
+            {
+                const int qi = i_next * kTile + col;
+                col_val = (i_next < nqt && qi < p.N) ? col_src[qi] : (stage_lse ? -INFINITY : 0.f);
+            }
             // (an mbarrier rather than a named barrier, so the wait is bounded)
-            mbar_arrive_warp(&st->lse_ready);
-            if (!mbar_wait_warp(&st->lse_ready, it & 1, wctx, 123)) {
+            mbar_arrive_warp(&st->lse_ready[half]);
+            if (!mbar_wait_warp(&st->lse_ready[half], it & 1, wctx, 123)) {
                 ok = false;
                 break;
             }
-            if (!mbar_wait_warp(&st->s_full, it & 1, wctx, 120)) {
+            if (!mbar_wait_warp(&st->s_full[half], it & 1, wctx, 120)) {
                 ok = false;
                 break;
             }
@@ -434,9 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive_warp(&st->p_ready);
+            mbar_arrive_warp(&st->p_ready[half]);
             // dQ_i: this warp's 32 query rows, half of the D columns
-            if (!mbar_wait_warp(&st->dq_full, it & 1, wctx, 121)) {
+            if (!mbar_wait_warp(&st->dq_full[Cfg::kDqTransposed ? half : 0], it & 1, wctx, 121)) {
                 ok = false;
                 break;
             }
@@ -455,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reg_fence(qa);
                 if (Cfg::kDqTransposed) reg_fence(qb);
                 tc_fence_before();
-                mbar_arrive_warp(&st->dq_free);
+                if (Cfg::kDqTransposed) mbar_arrive_warp(&st->dq_free[half]);
                 if (Cfg::kDqTransposed) {
                     // lane = head-dim index r; one reduction instruction covers
                     // 32 consecutive floats of one query row
