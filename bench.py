@@ -156,6 +156,13 @@ def max_over_ranks(value, device=None):
     return float(t.item())
 
 
+def whole_job_tflops(flops_per_rank, ms_per_rank, world_size, device=None):
+    """Whole-job throughput: the units every rank processed divided by the
+    slowest rank's time (each rank runs the same workload: weak scaling)."""
+    ms_max = max_over_ranks(ms_per_rank, device)
+    return flops_per_rank * world_size / (ms_max * 1e-3) / 1e12, ms_max
+
+
 def barrier(device=None):
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
@@ -266,7 +273,7 @@ def run_fa(args, w, ws, rank, device):
     fwd_ms = [a.elapsed_time(b) for a, b, c in ev]
     bwd_ms = [b.elapsed_time(c) for a, b, c in ev]
     step_ms = sum(f + g for f, g in zip(fwd_ms, bwd_ms)) / args.steps
-    step_ms_max = max_over_ranks(step_ms, device)
+    value, step_ms_max = whole_job_tflops(fwd_f + bwd_f, step_ms, ws, device)
     fwd_avg = max_over_ranks(sum(fwd_ms) / args.steps, device)
     bwd_avg = max_over_ranks(sum(bwd_ms) / args.steps, device)
 
@@ -293,7 +300,6 @@ def run_fa(args, w, ws, rank, device):
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / e2e_steps, device)
 
     total_f = (fwd_f + bwd_f) * ws
-    value = total_f / (step_ms_max * 1e-3) / 1e12
     e2e_value = total_f / (e2e_ms * 1e-3) / 1e12
     fwd_tflops = fwd_f * ws / (fwd_avg * 1e-3) / 1e12
     bwd_tflops = bwd_f * ws / (bwd_avg * 1e-3) / 1e12

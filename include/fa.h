@@ -143,6 +143,15 @@ const char* fa_status_string(int status);
 int fa_set_kernel_path(int path);
 
 /*
+ * Test hook for the device failure path: launches one small kernel whose
+ * bounded mbarrier wait (the same routine the tensor-core kernels use) waits
+ * on a barrier nothing arrives at, gives up after limit_ns nanoseconds,
+ * records FA_ERR_DEVICE_TIMEOUT with site 900 in the status word and returns.
+ * Nothing faults or hangs; read the result with fa_check_device_status.
+ */
+int fa_test_wait_timeout(uint64_t limit_ns, void* stream);
+
+/*
  * Diagnostic: number of CUDA kernels this library has launched in the
  * calling process (all devices, all entry points).
  */

@@ -36,7 +36,7 @@ _lock = threading.Lock()
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
             "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
-            "fa_bwd_noalloc")
+            "fa_bwd_noalloc", "fa_test_wait_timeout")
 
 # Size of the fixed device array fa_bwd_noalloc takes its workspace from.
 FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -81,6 +81,8 @@ def load_library(build_if_missing: bool = True):
         lib.fa_set_kernel_path.restype = I
         lib.fa_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, P]
         lib.fa_bwd_noalloc.restype = I
+        lib.fa_test_wait_timeout.argtypes = [U64, P]
+        lib.fa_test_wait_timeout.restype = I
         lib.fa_launch_count.argtypes = []
         lib.fa_launch_count.restype = ctypes.c_uint64
         _lib = lib
@@ -135,6 +137,11 @@ def fa_status_string(status):
 
 def fa_set_kernel_path(path):
     return load_library().fa_set_kernel_path(int(path))
+
+
+def fa_test_wait_timeout(limit_ns, stream):
+    """Runs the bounded-wait failure path once (see include/fa.h)."""
+    return load_library().fa_test_wait_timeout(int(limit_ns), stream)
 
 
 def fa_launch_count():

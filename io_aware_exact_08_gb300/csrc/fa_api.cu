@@ -19,20 +19,6 @@ __device__ int g_status[2];
 int g_kernel_path = 0;  // 0 = default, 1 = CUDA-core kernels only
 std::atomic<uint64_t> g_launches{0};
 
-int status_ptr(int** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-    static int* cached[64] = {nullptr};
-    if (dev < 0 || dev >= 64) return FA_ERR_CUDA;
-    if (!cached[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return FA_ERR_CUDA;
-        cached[dev] = static_cast<int*>(ptr);
-    }
-    *out = cached[dev];
-    return FA_OK;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -85,6 +71,22 @@ bool use_tensor_cores(const Problem& p) { return g_kernel_path == 0 && p.dtype =
 
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+int status_address(int** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    static int* cached[64] = {nullptr};
+    if (dev < 0 || dev >= 64) return FA_ERR_CUDA;
+    if (!cached[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return FA_ERR_CUDA;
+        cached[dev] = static_cast<int*>(ptr);
+    }
+    *out = cached[dev];
+    return FA_OK;
+}
+
+
+
 }  // namespace fa
 
 using namespace fa;
@@ -107,7 +109,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     p.v = v;
     p.o = o;
     p.lse = lse;
-    rc = status_ptr(&p.status);
+    rc = status_address(&p.status);
     if (rc != FA_OK) return rc;
     if (use_tensor_cores(p)) return launch_fwd_tc(p);
     return from_cuda(launch_fwd_simt(p));
@@ -146,7 +148,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     const size_t rows = (size_t)B * H * N;
     p.delta = static_cast<float*>(workspace);
     p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)));
-    rc = status_ptr(&p.status);
+    rc = status_address(&p.status);
     if (rc != FA_OK) return rc;
     if (use_tensor_cores(p)) return launch_bwd_tc(p);
     return from_cuda(launch_bwd_simt(p));

@@ -43,6 +43,10 @@ constexpr int kMaskBlock = 128;
 // Counts kernel launches for fa_launch_count (thread-safe).
 void note_launches(int n);
 
+// Device address of the status word on the current device (looked up once
+// per device).
+int status_address(int** out);
+
 // CUDA-core kernels (any dtype, d in {64,128}); implemented in fa_simt.cu.
 cudaError_t launch_fwd_simt(const Problem& p);
 cudaError_t launch_bwd_simt(const Problem& p);

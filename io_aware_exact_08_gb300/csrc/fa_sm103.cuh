@@ -71,6 +71,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 struct WaitCtx {
     volatile int* abort_flag;  // shared memory
     int* status;               // global: [0] = status, [1] = site
+    uint64_t limit_ns = kWaitLimitNs;
 };
 
 __device__ __forceinline__ void raise_timeout(const WaitCtx& w, int site) {
@@ -87,7 +88,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 31u) == 0) {
             if (*w.abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > w.limit_ns) {
                 raise_timeout(w, site);
                 return false;
             }
