@@ -407,36 +407,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                float lsev[32], delv[32];
-#pragma unroll
-                for (int x = 0; x < 32; x += 4) {
-                    const float4 a = *reinterpret_cast<const float4*>(sLse + cb + x);
-                    const float4 d4 = *reinterpret_cast<const float4*>(sDelta + cb + x);
-                    lsev[x] = a.x, lsev[x + 1] = a.y, lsev[x + 2] = a.z, lsev[x + 3] = a.w;
-                    delv[x] = d4.x, delv[x + 1] = d4.y, delv[x + 2] = d4.z, delv[x + 3] = d4.w;
-                }
                 const bool edge = (cmin > cb) || (cmax < cb + 32);
                 uint32_t pk[16];
                 uint32_t dsk[16];
 #pragma unroll
-                for (int x = 0; x < 32; x += 2) {
-                    float pv[2], dsv[2];
+                for (int x = 0; x < 32; x += 4) {
+                    // per-column LSE and delta, read four at a time (broadcast)
+                    const float4 l4 = *reinterpret_cast<const float4*>(sLse + cb + x);
+                    const float4 d4 = *reinterpret_cast<const float4*>(sDelta + cb + x);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pv[4], dsv[4];
 #pragma unroll
-                    for (int y = 0; y < 2; ++y) {
+                    for (int y = 0; y < 4; ++y) {
                         const int c = cb + x + y;
-                        float pe = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lsev[x + y]));
+                        float pe = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lv[y]));
                         if (edge && !((c >= cmin) && (c < cmax))) pe = 0.f;
                         if (p.dropout) {
                             const float zk = ((keep >> (x + y)) & 1u) ? p.keep_scale : 0.f;
                             pv[y] = pe * zk;
-                            dsv[y] = pe * fmaf(__uint_as_float(dr[x + y]), zk, -delv[x + y]);
+                            dsv[y] = pe * fmaf(__uint_as_float(dr[x + y]), zk, -dv4[y]);
                         } else {
                             pv[y] = pe;
-                            dsv[y] = pe * (__uint_as_float(dr[x + y]) - delv[x + y]);
+                            dsv[y] = pe * (__uint_as_float(dr[x + y]) - dv4[y]);
                         }
                     }
                     pk[x / 2] = pack_bf16x2(pv[0], pv[1]);
+                    pk[x / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
                     dsk[x / 2] = pack_bf16x2(dsv[0], dsv[1]);
+                    dsk[x / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
                 }
                 // P^T into TMEM columns this warp has already read
                 tmem_st16(tmem + lane_base + Cfg::kColS + half * 64 + ch * 16, pk);
