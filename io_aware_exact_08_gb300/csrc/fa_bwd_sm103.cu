@@ -410,32 +410,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool edge = (cmin > cb) || (cmax < cb + 32);
                 uint32_t pk[16];
                 uint32_t dsk[16];
+                // columns outside [cmin, cmax) (causal diagonal, key padding,
+                // sequence end) are zeroed in S first, so the element loop
+                // below carries no per-element mask test
+                if (edge) {
 #pragma unroll
-                for (int x = 0; x < 32; x += 4) {
-                    // per-column LSE and delta, read four at a time (broadcast)
-                    const float4 l4 = *reinterpret_cast<const float4*>(sLse + cb + x);
-                    const float4 d4 = *reinterpret_cast<const float4*>(sDelta + cb + x);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pv[4], dsv[4];
+                    for (int x = 0; x < 32; ++x)
+                        if (cb + x < cmin || cb + x >= cmax) sr[x] = __float_as_uint(-INFINITY);
+                }
+                if (!p.dropout) {
 #pragma unroll
-                    for (int y = 0; y < 4; ++y) {
-                        const int c = cb + x + y;
-                        float pe = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lv[y]));
-                        if (edge && !((c >= cmin) && (c < cmax))) pe = 0.f;
-                        if (p.dropout) {
+                    for (int x = 0; x < 32; x += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(sLse + cb + x);
+                        const float4 d4 = *reinterpret_cast<const float4*>(sDelta + cb + x);
+                        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[x + 0]), p.scale_log2, -l4.x));
+                        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[x + 1]), p.scale_log2, -l4.y));
+                        const float e2 = ex2_approx(fmaf(__uint_as_float(sr[x + 2]), p.scale_log2, -l4.z));
+                        const float e3 = ex2_approx(fmaf(__uint_as_float(sr[x + 3]), p.scale_log2, -l4.w));
+                        pk[x / 2] = pack_bf16x2(e0, e1);
+                        pk[x / 2 + 1] = pack_bf16x2(e2, e3);
+                        dsk[x / 2] = pack_bf16x2(e0 * (__uint_as_float(dr[x + 0]) - d4.x),
+                                                 e1 * (__uint_as_float(dr[x + 1]) - d4.y));
+                        dsk[x / 2 + 1] = pack_bf16x2(e2 * (__uint_as_float(dr[x + 2]) - d4.z),
+                                                     e3 * (__uint_as_float(dr[x + 3]) - d4.w));
+                    }
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(sLse + cb + x);
+                        const float4 d4 = *reinterpret_cast<const float4*>(sDelta + cb + x);
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pv[4], dsv[4];
+#pragma unroll
+                        for (int y = 0; y < 4; ++y) {
+                            const float pe = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lv[y]));
                             const float zk = ((keep >> (x + y)) & 1u) ? p.keep_scale : 0.f;
                             pv[y] = pe * zk;
                             dsv[y] = pe * fmaf(__uint_as_float(dr[x + y]), zk, -dv4[y]);
-                        } else {
-                            pv[y] = pe;
-                            dsv[y] = pe * (__uint_as_float(dr[x + y]) - dv4[y]);
                         }
+                        pk[x / 2] = pack_bf16x2(pv[0], pv[1]);
+                        pk[x / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+                        dsk[x / 2] = pack_bf16x2(dsv[0], dsv[1]);
+                        dsk[x / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
                     }
-                    pk[x / 2] = pack_bf16x2(pv[0], pv[1]);
-                    pk[x / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-                    dsk[x / 2] = pack_bf16x2(dsv[0], dsv[1]);
-                    dsk[x / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
                 }
                 // P^T into TMEM columns this warp has already read
                 tmem_st16(tmem + lane_base + Cfg::kColS + half * 64 + ch * 16, pk);
