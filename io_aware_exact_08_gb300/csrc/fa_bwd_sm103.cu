@@ -152,9 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sV = sK + Cfg::kTileBytes;
     uint8_t* sStages = sV + Cfg::kTileBytes;
     uint8_t* sDS = sStages + Cfg::kStages * Cfg::kStageBytes;
-    float* sLse = reinterpret_cast<float*>(sDS + Cfg::kDsBytes);
-    float* sDelta = sLse + kTile;
-    BwdShared* st = reinterpret_cast<BwdShared*>(sDelta + kTile);
+    float* sNegLse = reinterpret_cast<float*>(sDS + Cfg::kDsBytes);  // -LSE (log2 units)
+    float* sNegDelta = sNegLse + kTile;                                // -delta
+    BwdShared* st = reinterpret_cast<BwdShared*>(sNegDelta + kTile);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.y;
@@ -358,11 +358,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = i_cur; n_active > 0 && i < sched.nqt; ++it) {
             const int i0 = i * kTile;
             const int i_next = sched.next(i + 1);
-            // per-query LSE (log2 units; +inf for masked rows so P = 0) and delta
+            // per-query -LSE (log2 units; -inf for masked rows so P = 0) and
+            // -delta, negated so that each pair of columns takes one paired
+            // fma / add
             if (stage_lse)
-                sLse[col] = (col_val == -INFINITY) ? INFINITY : col_val * kLog2e;
+                sNegLse[col] = (col_val == -INFINITY) ? -INFINITY : -(col_val * kLog2e);
             else
-                sDelta[col] = col_val;
+                sNegDelta[col] = -col_val;
             {
                 const int qi = i_next * kTile + col;
                 col_val = (i_next < nqt && qi < p.N) ? col_src[qi] : (stage_lse ? -INFINITY : 0.f);
@@ -418,41 +420,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int x = 0; x < 32; ++x)
                         if (cb + x < cmin || cb + x >= cmax) sr[x] = __float_as_uint(-INFINITY);
                 }
+                const float sl2 = p.scale_log2;
                 if (!p.dropout) {
 #pragma unroll
                     for (int x = 0; x < 32; x += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4*>(sLse + cb + x);
-                        const float4 d4 = *reinterpret_cast<const float4*>(sDelta + cb + x);
-                        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[x + 0]), p.scale_log2, -l4.x));
-                        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[x + 1]), p.scale_log2, -l4.y));
-                        const float e2 = ex2_approx(fmaf(__uint_as_float(sr[x + 2]), p.scale_log2, -l4.z));
-                        const float e3 = ex2_approx(fmaf(__uint_as_float(sr[x + 3]), p.scale_log2, -l4.w));
-                        pk[x / 2] = pack_bf16x2(e0, e1);
-                        pk[x / 2 + 1] = pack_bf16x2(e2, e3);
-                        dsk[x / 2] = pack_bf16x2(e0 * (__uint_as_float(dr[x + 0]) - d4.x),
-                                                 e1 * (__uint_as_float(dr[x + 1]) - d4.y));
-                        dsk[x / 2 + 1] = pack_bf16x2(e2 * (__uint_as_float(dr[x + 2]) - d4.z),
-                                                     e3 * (__uint_as_float(dr[x + 3]) - d4.w));
+                        const float4 l4 = *reinterpret_cast<const float4*>(sNegLse + cb + x);
+                        const float4 d4 = *reinterpret_cast<const float4*>(sNegDelta + cb + x);
+                        float a[4], e[4], t[4], g[4];
+                        ffma2(a[0], a[1], __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), sl2, sl2, l4.x, l4.y);
+                        ffma2(a[2], a[3], __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]), sl2, sl2, l4.z, l4.w);
+#pragma unroll
+                        for (int y = 0; y < 4; ++y) e[y] = ex2_approx(a[y]);
+                        // dS = P (dP - delta)
+                        fadd2(t[0], t[1], __uint_as_float(dr[x]), __uint_as_float(dr[x + 1]), d4.x, d4.y);
+                        fadd2(t[2], t[3], __uint_as_float(dr[x + 2]), __uint_as_float(dr[x + 3]), d4.z, d4.w);
+                        fmul2(g[0], g[1], e[0], e[1], t[0], t[1]);
+                        fmul2(g[2], g[3], e[2], e[3], t[2], t[3]);
+                        pk[x / 2] = pack_bf16x2(e[0], e[1]);
+                        pk[x / 2 + 1] = pack_bf16x2(e[2], e[3]);
+                        dsk[x / 2] = pack_bf16x2(g[0], g[1]);
+                        dsk[x / 2 + 1] = pack_bf16x2(g[2], g[3]);
                     }
                 } else {
 #pragma unroll
                     for (int x = 0; x < 32; x += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4*>(sLse + cb + x);
-                        const float4 d4 = *reinterpret_cast<const float4*>(sDelta + cb + x);
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-                        float pv[4], dsv[4];
+                        const float4 l4 = *reinterpret_cast<const float4*>(sNegLse + cb + x);
+                        const float4 d4 = *reinterpret_cast<const float4*>(sNegDelta + cb + x);
+                        float a[4], e[4], z[4], t[4], g[4], pv[4];
+                        ffma2(a[0], a[1], __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), sl2, sl2, l4.x, l4.y);
+                        ffma2(a[2], a[3], __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]), sl2, sl2, l4.z, l4.w);
 #pragma unroll
                         for (int y = 0; y < 4; ++y) {
-                            const float pe = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lv[y]));
-                            const float zk = ((keep >> (x + y)) & 1u) ? p.keep_scale : 0.f;
-                            pv[y] = pe * zk;
-                            dsv[y] = pe * fmaf(__uint_as_float(dr[x + y]), zk, -dv4[y]);
+                            e[y] = ex2_approx(a[y]);
+                            z[y] = ((keep >> (x + y)) & 1u) ? p.keep_scale : 0.f;
                         }
+                        // P^ = P Z/(1-p);  dS = P (dP Z/(1-p) - delta)
+                        fmul2(pv[0], pv[1], e[0], e[1], z[0], z[1]);
+                        fmul2(pv[2], pv[3], e[2], e[3], z[2], z[3]);
+                        ffma2(t[0], t[1], __uint_as_float(dr[x]), __uint_as_float(dr[x + 1]), z[0], z[1], d4.x, d4.y);
+                        ffma2(t[2], t[3], __uint_as_float(dr[x + 2]), __uint_as_float(dr[x + 3]), z[2], z[3], d4.z, d4.w);
+                        fmul2(g[0], g[1], e[0], e[1], t[0], t[1]);
+                        fmul2(g[2], g[3], e[2], e[3], t[2], t[3]);
                         pk[x / 2] = pack_bf16x2(pv[0], pv[1]);
                         pk[x / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-                        dsk[x / 2] = pack_bf16x2(dsv[0], dsv[1]);
-                        dsk[x / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+                        dsk[x / 2] = pack_bf16x2(g[0], g[1]);
+                        dsk[x / 2 + 1] = pack_bf16x2(g[2], g[3]);
                     }
                 }
                 // P^T into TMEM columns this warp has already read

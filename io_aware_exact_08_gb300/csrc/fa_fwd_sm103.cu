@@ -711,12 +711,13 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int x = 0; x < 32; ++x) pm[x & 7] = fmaxf(pm[x & 7], __uint_as_float(sr[c][x]));
-#pragma unroll
-            for (int w = 4; w > 0; w >>= 1) {
-#pragma unroll
-                for (int x = 0; x < w; ++x) pm[x] = fmaxf(pm[x], pm[x + w]);
-            }
+                for (int x = 0; x < 32; x += 2)
+                    pm[(x >> 1) & 7] =
+                        fmax3(pm[(x >> 1) & 7], __uint_as_float(sr[c][x]), __uint_as_float(sr[c][x + 1]));
+            pm[0] = fmax3(pm[0], pm[1], pm[2]);
+            pm[3] = fmax3(pm[3], pm[4], pm[5]);
+            pm[6] = fmaxf(pm[6], pm[7]);
+            pm[0] = fmax3(pm[0], pm[3], pm[6]);
             const float mt = pm[0] * p.scale_log2;
             const bool raise = mt > m + kRescaleThreshold;
             if (__any_sync(0xffffffffu, raise) && u > 0) {
@@ -734,29 +735,50 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                 if (raise) l *= alpha;
             }
             if (raise) m = mt;
-            const float mref = (m == -INFINITY) ? 0.f : m;
-            float ps[4];
+            const float nmref = (m == -INFINITY) ? 0.f : -m;
+            const float sl2 = p.scale_log2;
+            // row-sum partials, four pairs
+            float ps[8];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) ps[x] = 0.f;
+            for (int x = 0; x < 8; ++x) ps[x] = 0.f;
+            // exponentials packed in place: pair x/2 overwrites word x/2,
+            // which has already been consumed; P chunk c lands in columns
+            // 16c..16c+15, already read. The sum takes every exponential,
+            // the dropout mask only what goes to P.
+            if (!p.dropout) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                // exponentials packed in place: pair x/2 overwrites word x/2,
-                // which has already been consumed
+                for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                for (int x = 0; x < 32; x += 2) {
-                    const float e0 = ex2_approx(fmaf(__uint_as_float(sr[c][x]), p.scale_log2, -mref));
-                    const float e1 = ex2_approx(fmaf(__uint_as_float(sr[c][x + 1]), p.scale_log2, -mref));
-                    ps[(x >> 1) & 3] += e0 + e1;
-                    sr[c][x >> 1] =
-                        pack_bf16x2(((keep[c] >> x) & 1u) ? e0 : 0.f, ((keep[c] >> (x + 1)) & 1u) ? e1 : 0.f);
+                    for (int x = 0; x < 32; x += 2) {
+                        float a0, a1;
+                        ffma2(a0, a1, __uint_as_float(sr[c][x]), __uint_as_float(sr[c][x + 1]), sl2, sl2, nmref, nmref);
+                        const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+                        const int k = (x >> 1) & 3;
+                        fadd2(ps[2 * k], ps[2 * k + 1], ps[2 * k], ps[2 * k + 1], e0, e1);
+                        sr[c][x >> 1] = pack_bf16x2(e0, e1);
+                    }
+                    tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
                 }
-                // P chunk c lands in columns 16c..16c+15, already read
-                tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 2) {
+                        float a0, a1;
+                        ffma2(a0, a1, __uint_as_float(sr[c][x]), __uint_as_float(sr[c][x + 1]), sl2, sl2, nmref, nmref);
+                        const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+                        const int k = (x >> 1) & 3;
+                        fadd2(ps[2 * k], ps[2 * k + 1], ps[2 * k], ps[2 * k + 1], e0, e1);
+                        sr[c][x >> 1] =
+                            pack_bf16x2(((keep[c] >> x) & 1u) ? e0 : 0.f, ((keep[c] >> (x + 1)) & 1u) ? e1 : 0.f);
+                    }
+                    tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
+                }
             }
-            ps[0] += ps[2];
-            ps[1] += ps[3];
-            ps[0] += ps[1];
-            l += ps[0];
+            fadd2(ps[0], ps[1], ps[0], ps[1], ps[4], ps[5]);
+            fadd2(ps[2], ps[3], ps[2], ps[3], ps[6], ps[7]);
+            fadd2(ps[0], ps[1], ps[0], ps[1], ps[2], ps[3]);
+            l += ps[0] + ps[1];
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive_warp(&st->p_full[t]);
