@@ -21,10 +21,12 @@
 //        dQ_i^T = K_j^T dS^T (both operands read MN-major)
 //      (at D = 128 computed transposed, dQ_i^T = K_j^T dS^T, so that a
 //      warp's reduction covers 32 consecutive floats of one row) and the
-//      compute warps add it into the fp32 accumulator in global memory.
+//      reduction warps add it into the fp32 accumulator in global memory.
 //      dK_j, dV_j stay in TMEM until the end.
 //   3. convert: dq = dtype(scale * dQacc).
-// Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer.
+// Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer, warps
+// 10-13 dQ reduction (one per TMEM lane quarter), so that the compute warps
+// never wait for the dQ product or for the reductions to drain into L2.
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -47,7 +49,8 @@ using namespace sm103;
 
 constexpr int kTile = 128;          // keys per CTA, queries per step
 constexpr int kComputeThreads = 256;
-constexpr int kThreads = 320;
+constexpr int kReduceWarp0 = 10;
+constexpr int kThreads = 448;
 
 template <int D>
 struct BwdCfg {
@@ -57,8 +60,10 @@ struct BwdCfg {
     static constexpr int kBoxes = D / 64;
     static constexpr int kStageBytes = 2 * kTileBytes;  // Q_i and dO_i
     static constexpr int kDsBytes = kTile * kTile * 2;  // dS^T, 128 x 128 bf16
+    // (no alignment slack: the dynamic shared memory window starts 1024-byte
+    // aligned, which the kernel checks)
     static constexpr int kSmem =
-        1024 + 2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBytes + 2 * kTile * 4 /*lse, delta*/ + 256;
+        2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBytes + 2 * 2 * kTile * 4 /*lse, delta x2*/ + 256;
     static constexpr uint32_t kColS = 0, kColDP = 128;
     // dQ accumulator. D = 128: dQ^T (lanes = head-dim rows, 128 query
     // columns), aliasing dP^T. D = 64: dQ (lanes = query rows, 64 columns).
@@ -94,7 +99,7 @@ struct BwdShared {
     uint64_t s_full[2];    // per 64-query half h: S^T_h and dP^T_h in TMEM
     uint64_t p_ready[2];   // P^T_h in TMEM and dS^T_h in shared memory
     uint64_t dq_full[2];   // dQ of half h (D = 128) / of the tile (D = 64, [0])
-    uint64_t dq_free[2];   // dQ^T_h read out of TMEM (D = 128)
+    uint64_t dq_free[2];   // that dQ read out of TMEM by the reduction warps
     uint64_t acc_done;
     uint64_t teardown;
     uint64_t lse_ready[2];
@@ -147,14 +152,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const BwdParams p) {
     using Cfg = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sK = smem;
+    if (smem_u32(smem_raw) & 1023u) {  // swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0 && atomicCAS(p.status, 0, (int)FA_ERR_CUDA) == 0) atomicExch(p.status + 1, 130);
+        return;
+    }
+    uint8_t* sK = smem_raw;
     uint8_t* sV = sK + Cfg::kTileBytes;
     uint8_t* sStages = sV + Cfg::kTileBytes;
     uint8_t* sDS = sStages + Cfg::kStages * Cfg::kStageBytes;
-    float* sNegLse = reinterpret_cast<float*>(sDS + Cfg::kDsBytes);  // -LSE (log2 units)
-    float* sNegDelta = sNegLse + kTile;                                // -delta
-    BwdShared* st = reinterpret_cast<BwdShared*>(sNegDelta + kTile);
+    // -LSE (log2 units) and -delta of the step's 128 queries, double-buffered
+    // by step parity: a warp may stage step it+1 while others still read it
+    float* sNegLse = reinterpret_cast<float*>(sDS + Cfg::kDsBytes);
+    float* sNegDelta = sNegLse + 2 * kTile;
+    BwdShared* st = reinterpret_cast<BwdShared*>(sNegDelta + 2 * kTile);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.y;
@@ -319,7 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    desc_add(dsd_mn, h * (kTile * 128) + kk * 2048), id_dqt_h, kk > 0);
                         mma_commit(&st->dq_full[h]);
                     } else if (h == 1) {
-                        // dQ = dS K_j over the whole tile (M = 128 queries, lane = query)
+                        // dQ = dS K_j over the whole tile (M = 128 queries, lane = query),
+                        // over the previous tile's dQ once it has been read out
+                        if (it > 0) {
+                            if (!mbar_wait(&st->dq_free[0], (it - 1) & 1, wctx, 115)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
                             mma_ss(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048), id_dq,
@@ -331,6 +349,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&st->acc_done);
             mma_commit(&st->teardown);
             mbar_wait(&st->teardown, 0, wctx, 114);
+        }
+    } else if (warp >= kReduceWarp0) {
+        // ------------------------------------------------------------ dQ reduction
+        // D = 128: dQ^T, lane = head-dim index, so one reduction instruction
+        // covers 32 consecutive floats of one query row. D = 64: dQ, lane =
+        // query row, 64 consecutive floats in 16-byte reductions.
+        const int quarter = warp & 3;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const int r = quarter * 32 + lane;
+        bool ok = n_active > 0;
+        int it = 0;
+        for (int i = sched.next(0); ok && i < sched.nqt; i = sched.next(i + 1), ++it) {
+            const int i0 = i * kTile;
+            const int nvalid = min(kTile, p.N - i0);
+#pragma unroll
+            for (int h = 0; h < (Cfg::kDqTransposed ? 2 : 1); ++h) {
+                if (!mbar_wait_warp(&st->dq_full[h], it & 1, wctx, 121)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // read out, release the TMEM (the next dP^T / dQ may
+                // overwrite it), then reduce
+                uint32_t qa[32], qb[32];
+                tmem_ld32(tmem + lane_base + Cfg::kColDQ + h * 64, qa);
+                tmem_ld32(tmem + lane_base + Cfg::kColDQ + h * 64 + 32, qb);
+                tmem_ld_wait();
+                reg_fence(qa);
+                reg_fence(qb);
+                tc_fence_before();
+                mbar_arrive_warp(&st->dq_free[h]);
+                if (Cfg::kDqTransposed) {
+                    float* dst = p.dq_acc + ((size_t)bh * p.N + i0 + h * 64) * D + r;
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        if (h * 64 + x < nvalid) red_add_f32(dst + (size_t)x * D, __uint_as_float(qa[x]));
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        if (h * 64 + 32 + x < nvalid) red_add_f32(dst + (size_t)(32 + x) * D, __uint_as_float(qb[x]));
+                } else if (r < nvalid) {
+                    float* dst = p.dq_acc + ((size_t)bh * p.N + i0 + r) * D;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        red_add_v4(dst + 4 * v, __uint_as_float(qa[4 * v]), __uint_as_float(qa[4 * v + 1]),
+                                   __uint_as_float(qa[4 * v + 2]), __uint_as_float(qa[4 * v + 3]));
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        red_add_v4(dst + 32 + 4 * v, __uint_as_float(qb[4 * v]), __uint_as_float(qb[4 * v + 1]),
+                                   __uint_as_float(qb[4 * v + 2]), __uint_as_float(qb[4 * v + 3]));
+                }
+            }
         }
     } else {
         // ------------------------------------------------------------ compute
@@ -361,10 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // per-query -LSE (log2 units; -inf for masked rows so P = 0) and
             // -delta, negated so that each pair of columns takes one paired
             // fma / add
+            const int lbuf = (it & 1) * kTile;
             if (stage_lse)
-                sNegLse[col] = (col_val == -INFINITY) ? -INFINITY : -(col_val * kLog2e);
+                sNegLse[lbuf + col] = (col_val == -INFINITY) ? -INFINITY : -(col_val * kLog2e);
             else
-                sNegDelta[col] = -col_val;
+                sNegDelta[lbuf + col] = -col_val;
             {
                 const int qi = i_next * kTile + col;
                 col_val = (i_next < nqt && qi < p.N) ? col_src[qi] : (stage_lse ? -INFINITY : 0.f);
@@ -424,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!p.dropout) {
 #pragma unroll
                     for (int x = 0; x < 32; x += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4*>(sNegLse + cb + x);
-                        const float4 d4 = *reinterpret_cast<const float4*>(sNegDelta + cb + x);
+                        const float4 l4 = *reinterpret_cast<const float4*>(sNegLse + lbuf + cb + x);
+                        const float4 d4 = *reinterpret_cast<const float4*>(sNegDelta + lbuf + cb + x);
                         float a[4], e[4], t[4], g[4];
                         ffma2(a[0], a[1], __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), sl2, sl2, l4.x, l4.y);
                         ffma2(a[2], a[3], __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]), sl2, sl2, l4.z, l4.w);
@@ -444,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
 #pragma unroll
                     for (int x = 0; x < 32; x += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4*>(sNegLse + cb + x);
-                        const float4 d4 = *reinterpret_cast<const float4*>(sNegDelta + cb + x);
+                        const float4 l4 = *reinterpret_cast<const float4*>(sNegLse + lbuf + cb + x);
+                        const float4 d4 = *reinterpret_cast<const float4*>(sNegDelta + lbuf + cb + x);
                         float a[4], e[4], z[4], t[4], g[4], pv[4];
                         ffma2(a[0], a[1], __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), sl2, sl2, l4.x, l4.y);
                         ffma2(a[2], a[3], __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]), sl2, sl2, l4.z, l4.w);
@@ -482,51 +552,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive_warp(&st->p_ready[half]);
-            // dQ_i: this warp's 32 query rows, half of the D columns
-            if (!mbar_wait_warp(&st->dq_full[Cfg::kDqTransposed ? half : 0], it & 1, wctx, 121)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // Both layouts: read this warp's 64 dQ values into registers,
-            // release the TMEM (the next dP^T may overwrite it), then reduce.
-            {
-                uint32_t qa[32], qb[32];
-                if (Cfg::kDqTransposed) {
-                    tmem_ld32(tmem + lane_base + Cfg::kColDQ + half * 64, qa);
-                    tmem_ld32(tmem + lane_base + Cfg::kColDQ + half * 64 + 32, qb);
-                } else {
-                    tmem_ld32(tmem + lane_base + Cfg::kColDQ + half * 32, qa);
-                }
-                tmem_ld_wait();
-                reg_fence(qa);
-                if (Cfg::kDqTransposed) reg_fence(qb);
-                tc_fence_before();
-                if (Cfg::kDqTransposed) mbar_arrive_warp(&st->dq_free[half]);
-                if (Cfg::kDqTransposed) {
-                    // lane = head-dim index r; one reduction instruction covers
-                    // 32 consecutive floats of one query row
-                    float* dst = p.dq_acc + ((size_t)bh * p.N + i0) * D + r;
-                    const int nvalid = min(kTile, p.N - i0);
-#pragma unroll
-                    for (int x = 0; x < 32; ++x)
-                        if (half * 64 + x < nvalid) red_add_f32(dst + (size_t)(half * 64 + x) * D, __uint_as_float(qa[x]));
-#pragma unroll
-                    for (int x = 0; x < 32; ++x)
-                        if (half * 64 + 32 + x < nvalid)
-                            red_add_f32(dst + (size_t)(half * 64 + 32 + x) * D, __uint_as_float(qb[x]));
-                } else {
-                    // lane = query row; 32 consecutive columns of that row
-                    const int qrow = i0 + r;
-                    float* dst = p.dq_acc + ((size_t)bh * p.N + qrow) * D + half * 32;
-                    if (qrow < p.N) {
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            red_add_v4(dst + 4 * v, __uint_as_float(qa[4 * v]), __uint_as_float(qa[4 * v + 1]),
-                                       __uint_as_float(qa[4 * v + 2]), __uint_as_float(qa[4 * v + 3]));
-                    }
-                }
-            }
             i = i_next;
         }
         // epilogue: dK = scale * acc, dV = acc, rows of this key tile
