@@ -71,6 +71,30 @@ struct BwdCfg {
     static constexpr uint32_t kColDQ = (D == 128) ? 128 : 256;
     static constexpr uint32_t kColDV = (D == 128) ? 256 : 320;
     static constexpr uint32_t kColDK = 384;
+    // MMA issue by the whole warp with one elected lane (measured faster at
+    // D = 64) or by lane 0 alone (measured faster at D = 128)
+    static constexpr bool kWarpIssue = (D == 64);
+};
+
+// The MMA issuer's calls in either form (see kWarpIssue).
+template <bool kWarp>
+struct Issue {
+    static __device__ __forceinline__ void ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (kWarp) mma_ss_warp(d, a, b, id, acc);
+        else mma_ss(d, a, b, id, acc);
+    }
+    static __device__ __forceinline__ void ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (kWarp) mma_ts_warp(d, a, b, id, acc);
+        else mma_ts(d, a, b, id, acc);
+    }
+    static __device__ __forceinline__ void commit(uint64_t* bar) {
+        if constexpr (kWarp) mma_commit_warp(bar);
+        else mma_commit(bar);
+    }
+    static __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, const WaitCtx& w, int site) {
+        if constexpr (kWarp) return mbar_wait_warp(bar, parity, w, site);
+        else return mbar_wait(bar, parity, w, site);
+    }
 };
 
 struct BwdParams {
@@ -247,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_active > 0) {
+        if ((Cfg::kWarpIssue || lane == 0) && n_active > 0) {
+            using I = Issue<Cfg::kWarpIssue>;
             constexpr uint32_t id_sh = idesc_bf16_f32(kTile, 64, 0, 0);      // S^T_h, dP^T_h (N = 64)
             constexpr uint32_t id_dv = idesc_bf16_f32(kTile, D, 0, 1);      // dV (A tmem), dK (A K-major)
             constexpr uint32_t id_dqt_h = idesc_bf16_f32(kTile, 64, 1, 1);   // dQ^T_h (A, B MN-major, N = 64)
@@ -260,11 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dsd_mn = smem_desc_sw128(ds_base, kTile * 128, 1024);  // dS^T, MN-major
             const uint64_t kd_mn = smem_desc_sw128(k_base, Cfg::kBoxBytes, 1024);  // K, MN-major (N = d)
             const uint64_t kd_mn2 = smem_desc_sw128(k_base, kTile * 128, 1024);    // K, MN-major (M = d)
-            bool ok = mbar_wait(&st->kv_full, 0, wctx, 110);
+            bool ok = I::wait(&st->kv_full, 0, wctx, 110);
             tc_fence_after();
             for (int it = 0; ok && it < n_active; ++it) {
                 const int s = it % Cfg::kStages;
-                if (!mbar_wait(&st->st_full[s], (it / Cfg::kStages) & 1, wctx, 111)) break;
+                if (!I::wait(&st->st_full[s], (it / Cfg::kStages) & 1, wctx, 111)) break;
                 tc_fence_after();
                 const uint32_t q_base = smem_u32(sStages + s * Cfg::kStageBytes);
                 const uint32_t do_base = q_base + Cfg::kTileBytes;
@@ -281,12 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                        mma_ss(tmem + Cfg::kColS + 64 * h, desc_add(kd_k, off), desc_add(qd_k, off + 8192 * h), id_sh,
+                        I::ss(tmem + Cfg::kColS + 64 * h, desc_add(kd_k, off), desc_add(qd_k, off + 8192 * h), id_sh,
                                kk > 0);
                     }
                     // at D = 128, dP^T_h overwrites the previous tile's dQ^T_h
                     if (D == 128 && it > 0) {
-                        if (!mbar_wait(&st->dq_free[h], (it - 1) & 1, wctx, 112)) {
+                        if (!I::wait(&st->dq_free[h], (it - 1) & 1, wctx, 112)) {
                             ok = false;
                             break;
                         }
@@ -295,15 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                        mma_ss(tmem + Cfg::kColDP + 64 * h, desc_add(vd_k, off), desc_add(dod_k, off + 8192 * h), id_sh,
+                        I::ss(tmem + Cfg::kColDP + 64 * h, desc_add(vd_k, off), desc_add(dod_k, off + 8192 * h), id_sh,
                                kk > 0);
                     }
-                    mma_commit(&st->s_full[h]);
+                    I::commit(&st->s_full[h]);
                 }
                 if (!ok) break;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    if (!mbar_wait(&st->p_ready[h], it & 1, wctx, 113)) {
+                    if (!I::wait(&st->p_ready[h], it & 1, wctx, 113)) {
                         ok = false;
                         break;
                     }
@@ -311,28 +336,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // dV += P^T_h dO_h: P^T_h (bf16) in TMEM columns 64h..64h+31
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
+                        I::ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
                                desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
                     // dK += dS^T_h Q_h (dS^T half h is shared-memory box h)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
+                        I::ss(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
                                desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                    if (h == 1) mma_commit(&st->st_empty[s]);
+                    if (h == 1) I::commit(&st->st_empty[s]);
                     if (Cfg::kDqTransposed) {
                         // dQ^T_h = K_j^T dS^T_h (M = head dim, N = 64 queries):
                         // lane = head-dim index, so one reduction instruction
                         // covers 32 consecutive floats of a dQ row
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ss(tmem + Cfg::kColDQ + 64 * h, desc_add(kd_mn2, kk * 2048),
+                            I::ss(tmem + Cfg::kColDQ + 64 * h, desc_add(kd_mn2, kk * 2048),
                                    desc_add(dsd_mn, h * (kTile * 128) + kk * 2048), id_dqt_h, kk > 0);
-                        mma_commit(&st->dq_full[h]);
+                        I::commit(&st->dq_full[h]);
                     } else if (h == 1) {
                         // dQ = dS K_j over the whole tile (M = 128 queries, lane = query),
                         // over the previous tile's dQ once it has been read out
                         if (it > 0) {
-                            if (!mbar_wait(&st->dq_free[0], (it - 1) & 1, wctx, 115)) {
+                            if (!I::wait(&st->dq_free[0], (it - 1) & 1, wctx, 115)) {
                                 ok = false;
                                 break;
                             }
@@ -340,15 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ss(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048), id_dq,
+                            I::ss(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048), id_dq,
                                    kk > 0);
-                        mma_commit(&st->dq_full[0]);
+                        I::commit(&st->dq_full[0]);
                     }
                 }
             }
-            mma_commit(&st->acc_done);
-            mma_commit(&st->teardown);
-            mbar_wait(&st->teardown, 0, wctx, 114);
+            I::commit(&st->acc_done);
+            I::commit(&st->teardown);
+            I::wait(&st->teardown, 0, wctx, 114);
         }
     } else if (warp >= kReduceWarp0) {
         // ------------------------------------------------------------ dQ reduction

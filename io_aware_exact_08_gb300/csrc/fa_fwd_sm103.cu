@@ -16,7 +16,7 @@
 //              TMEM columns, applies dropout, and does the epilogue.
 //   warp 4     producer: TMA loads of Q once, then K_0, K_1, V_0, K_2, V_1,
 //              ... through a ring of shared-memory stages.
-//   warp 5     MMA issuer: one thread issues tcgen05.mma for S_j = Q K_j^T
+//   warp 5     MMA issuer: one elected lane issues tcgen05.mma for S_j = Q K_j^T
 //              (double-buffered in TMEM so S_{j+1} overlaps the softmax of
 //              S_j) and O += P_j V_j (P read from TMEM), and owns the TMEM
 //              allocation.
@@ -223,24 +223,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_active > 0) {
+        if (n_active > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBlockM, D, 0, 1);
             const uint32_t q_base = smem_u32(sQ);
             const uint32_t kv_base = smem_u32(sKV);
             const uint64_t qd = smem_desc_sw128(q_base, 16, 1024);
             int t = 0;  // consume counter, same order as the producer
-            bool ok = mbar_wait(&st->q_full, 0, wctx, 10);
+            bool ok = mbar_wait_warp(&st->q_full, 0, wctx, 10);
             tc_fence_after();
             auto wait_tile = [&](uint32_t& addr) -> bool {
                 const int s = t % Cfg::kStages;
-                if (!mbar_wait(&st->kv_full[s], (t / Cfg::kStages) & 1, wctx, 11)) return false;
+                if (!mbar_wait_warp(&st->kv_full[s], (t / Cfg::kStages) & 1, wctx, 11)) return false;
                 tc_fence_after();
                 addr = kv_base + s * Cfg::kTileBytes;
                 return true;
             };
             auto release_tile = [&]() {
-                mma_commit(&st->kv_empty[t % Cfg::kStages]);
+                mma_commit_warp(&st->kv_empty[t % Cfg::kStages]);
                 ++t;
             };
             auto issue_s = [&](int buf) -> bool {
@@ -251,9 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                    mma_ss(d, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0);
+                    mma_ss_warp(d, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0);
                 }
-                mma_commit(&st->s_full[buf]);
+                mma_commit_warp(&st->s_full[buf]);
                 release_tile();
                 return true;
             };
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && n_active > 1) ok = issue_s(1);
             for (int j = 0; ok && j < n_active; ++j) {
                 const int buf = j & 1;
-                if (!mbar_wait(&st->p_full[buf], (j >> 1) & 1, wctx, 12)) break;
+                if (!mbar_wait_warp(&st->p_full[buf], (j >> 1) & 1, wctx, 12)) break;
                 tc_fence_after();
                 uint32_t vaddr;
                 if (!wait_tile(vaddr)) break;
@@ -270,17 +270,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk) {
                     // P: 16 keys = 8 TMEM columns of bf16 pairs; V: 16 rows of 128 bytes
-                    mma_ts(tmem + Cfg::kColO, a_tmem + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
+                    mma_ts_warp(tmem + Cfg::kColO, a_tmem + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 release_tile();
-                mma_commit(&st->pv_done);
-                if (j + 1 == n_active) mma_commit(&st->o_final);
+                mma_commit_warp(&st->pv_done);
+                if (j + 1 == n_active) mma_commit_warp(&st->o_final);
                 if (j + 2 < n_active) ok = issue_s(buf);
             }
             // every MMA this thread issued has completed before TMEM is freed
-            mma_commit(&st->teardown);
-            mbar_wait(&st->teardown, 0, wctx, 13);
+            mma_commit_warp(&st->teardown);
+            mbar_wait_warp(&st->teardown, 0, wctx, 13);
         }
     } else {
         // ------------------------------------------------------------ softmax
@@ -562,16 +562,17 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_max > 0) {
+        if (n_max > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBlockM, D, 0, 1);
             const uint32_t kv_base = smem_u32(sKV);
             const uint64_t qd0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t qd1 = smem_desc_sw128(smem_u32(sQ + Cfg::kQBytes), 16, 1024);
-            bool ok = mbar_wait(&st->q_full, 0, wctx, 70);
+            bool ok = mbar_wait_warp(&st->q_full, 0, wctx, 70);
             tc_fence_after();
-            // Straight-line issue code with every counter in registers: the
-            // single issuing thread has about 64 cycles per MMA to spare.
+            // Straight-line issue code with every counter in registers, run
+            // by the whole warp (one elected lane issues): the issuing path
+            // has about 64 cycles per MMA to spare.
             // Each load index is waited on once, before its first use.
             const int c0 = n_t[0], c1 = n_t[1];
             const uint64_t kvd_k = smem_desc_sw128(kv_base, 16, 1024);              // K tiles, K-major
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             constexpr uint32_t kStageUnits = Cfg::kTileBytes >> 4;
             // S_t(0) = Q_t K_0^T
             if (ok) {
-                ok = mbar_wait(&st->kv_full[0], 0, wctx, 71);
+                ok = mbar_wait_warp(&st->kv_full[0], 0, wctx, 71);
                 tc_fence_after();
             }
             if (ok) {
@@ -590,11 +591,11 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                        mma_ss(tmem + t * 128, desc_add(qd, off), desc_add(kvd_k, off), idesc_s, kk > 0);
+                        mma_ss_warp(tmem + t * 128, desc_add(qd, off), desc_add(kvd_k, off), idesc_s, kk > 0);
                     }
-                    mma_commit(&st->s_full[t]);
+                    mma_commit_warp(&st->s_full[t]);
                 }
-                mma_commit(&st->kv_empty[0]);
+                mma_commit_warp(&st->kv_empty[0]);
             }
             for (int u = 0; ok && u < n_max; ++u) {
                 const int lv = 2 * u + 1, lk = 2 * u + 2;  // load indices of V_u and K_{u+1}
@@ -608,13 +609,13 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                     const int ct = t ? c1 : c0;
                     if (u >= ct) continue;
                     // P_t(u) V_u
-                    if (!mbar_wait(&st->p_full[t], u & 1, wctx, 72)) {
+                    if (!mbar_wait_warp(&st->p_full[t], u & 1, wctx, 72)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (!v_ready) {
-                        if (!mbar_wait(&st->kv_full[sv], (lv / Cfg::kStages) & 1, wctx, 74)) {
+                        if (!mbar_wait_warp(&st->kv_full[sv], (lv / Cfg::kStages) & 1, wctx, 74)) {
                             ok = false;
                             break;
                         }
@@ -623,13 +624,13 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                     }
 #pragma unroll
                     for (int kk = 0; kk < kBlockN / 16; ++kk)
-                        mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
+                        mma_ts_warp(tmem + 256 + t * D, tmem + t * 128 + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
                                (u > 0 || kk > 0) ? 1u : 0u);
-                    if (u + 1 == ct) mma_commit(&st->o_final[t]);
+                    if (u + 1 == ct) mma_commit_warp(&st->o_final[t]);
                     // S_t(u+1) = Q_t K_{u+1}^T over the S/P columns just read
                     if (u + 1 < ct) {
                         if (!k_ready) {
-                            if (!mbar_wait(&st->kv_full[sk], (lk / Cfg::kStages) & 1, wctx, 75)) {
+                            if (!mbar_wait_warp(&st->kv_full[sk], (lk / Cfg::kStages) & 1, wctx, 75)) {
                                 ok = false;
                                 break;
                             }
@@ -640,18 +641,18 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                            mma_ss(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0);
+                            mma_ss_warp(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0);
                         }
-                        mma_commit(&st->s_full[t]);
+                        mma_commit_warp(&st->s_full[t]);
                     }
                 }
                 if (!ok) break;
                 // V_u and K_{u+1} are released after their last MMA
-                mma_commit(&st->kv_empty[sv]);
-                if (need_k) mma_commit(&st->kv_empty[sk]);
+                mma_commit_warp(&st->kv_empty[sv]);
+                if (need_k) mma_commit_warp(&st->kv_empty[sk]);
             }
-            mma_commit(&st->teardown);
-            mbar_wait(&st->teardown, 0, wctx, 73);
+            mma_commit_warp(&st->teardown);
+            mbar_wait_warp(&st->teardown, 0, wctx, 73);
         }
     } else {
         // ------------------------------------------------------------ softmax
