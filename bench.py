@@ -62,6 +62,34 @@ def algorithmic_bytes(w):
     return 4 * bhnd * e + 4 * bhn, 8 * bhnd * e + 8 * bhn
 
 
+def kernel_source_hash():
+    """SHA-256 over the CUDA sources of the library (file names and bytes)."""
+    import hashlib
+    d = os.path.join(ROOT, "io_aware_exact_08_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(d)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            h.update(fn.encode())
+            h.update(open(os.path.join(d, fn), "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload, call):
+    """DRAM bytes (read + write) of one `call` ("fa_fwd" or "fa_bwd") on
+    `workload`, as ncu counted them in the capture recorded under profiles/,
+    or None when there is no record or the kernel sources have changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get("calls", {}).get(workload, {}).get(call)
+    if not ent or rec.get("source_sha256") != kernel_source_hash():
+        return None
+    return int(ent["dram_bytes"])
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -322,7 +350,8 @@ def run_fa(args, w, ws, rank, device):
                 "frac": round(hbm_frac, 4)}
     else:
         roof = {"bound": "alu", "achieved": round(tensor_ach, 3), "peak": None, "unit": "TFLOP/s", "frac": None}
-    roof.update({"kernel": dominant, "traffic": None, "peak_source": peaks["source"] + " (burst)",
+    roof.update({"kernel": dominant, "traffic": recorded_traffic(w.name, dominant),
+                 "peak_source": peaks["source"] + " (burst)",
                  "tensor_frac": round(tensor_frac, 4), "hbm_frac": round(hbm_frac, 4),
                  "algorithmic_flops": dom_f, "algorithmic_bytes": dom_b, "avg_ms": round(dom_ms, 4)})
 
