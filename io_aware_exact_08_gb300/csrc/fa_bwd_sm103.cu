@@ -232,6 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = st->tmem_base;
     const int n_active = sched.count();
+    // The next kernel (dq conversion) may start launching once every CTA is
+    // here. Q, K, V, dO and LSE were complete before the preprocess kernel
+    // ran, so the producer and MMA warps start at once; the compute and
+    // reduction warps wait for the preprocess kernel (delta, dQacc = 0).
+    pdl_trigger();
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
@@ -385,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = quarter * 32 + lane;
         bool ok = n_active > 0;
         int it = 0;
+        pdl_wait();
         for (int i = sched.next(0); ok && i < sched.nqt; i = sched.next(i + 1), ++it) {
             const int i0 = i * kTile;
             const int nvalid = min(kTile, p.N - i0);
@@ -445,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nqt = sched.nqt;
         int i_cur = sched.next(0);
         float col_val = 0.f;
+        pdl_wait();
         if (n_active > 0) {
             const int qi = i_cur * kTile + col;
             col_val = (qi < p.N) ? col_src[qi] : (stage_lse ? -INFINITY : 0.f);
@@ -622,31 +629,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
-// delta_i = sum_c dO_ic O_ic and dQacc = 0 (one warp per row, bf16 inputs).
+// delta_i = sum_c dO_ic O_ic and dQacc = 0 (bf16 inputs): D/8 threads per
+// row, 16-byte loads and stores, the row sum reduced across those threads.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_tc_kernel(const __nv_bfloat16* __restrict__ O,
                                                          const __nv_bfloat16* __restrict__ dO,
                                                          float* __restrict__ delta, float* __restrict__ dq_acc,
                                                          size_t rows) {
-    const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    constexpr int PER = D / 32;  // elements per lane (2 or 4)
+    constexpr int T = D / 8;  // threads per row (8 or 16)
+    pdl_wait();               // O comes from the forward kernel
+    pdl_trigger();
+    const size_t row = ((size_t)blockIdx.x * 256 + threadIdx.x) / T;
+    const int t = threadIdx.x % T;
+    // every lane takes part in the shuffles below; past the last row it
+    // contributes zeros and stores nothing
+    const bool valid = row < rows;
+    const uint4 zero4 = make_uint4(0, 0, 0, 0);
+    const uint4 o4 = valid ? reinterpret_cast<const uint4*>(O + row * D)[t] : zero4;
+    const uint4 g4 = valid ? reinterpret_cast<const uint4*>(dO + row * D)[t] : zero4;
+    const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w};
     float s = 0.f;
-    const __nv_bfloat16* o = O + row * D + lane * PER;
-    const __nv_bfloat16* g = dO + row * D + lane * PER;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) s = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), s);
-    s = warp_sum(s);
-    if (lane == 0) delta[row] = s;
-    float* acc = dq_acc + row * D + lane * PER;
+    for (int e = 0; e < 4; ++e) {
+        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+        s = fmaf(of.x, gf.x, s);
+        s = fmaf(of.y, gf.y, s);
+    }
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (int w = T / 2; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+    if (!valid) return;
+    if (t == 0) delta[row] = s;
+    float4* acc = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * t;
+    acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // dq = bf16(scale * dQacc), 4 elements per thread.
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
                                                          float scale, size_t n4) {
+    pdl_wait();  // the accumulator is complete only when the main kernel is
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n4) return;
     const float4 a = acc[idx];
@@ -665,11 +687,22 @@ int launch_bwd_tc_d(const Problem& pr) {
         !make_tmap_bf16(&tv, pr.v, BH, pr.N, D, kTile) || !make_tmap_bf16(&tdo, pr.dO, BH, pr.N, D, kTile))
         return FA_ERR_CUDA;
     const size_t rows = (size_t)BH * pr.N;
-    bwd_pre_tc_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, pr.stream>>>(
-        static_cast<const __nv_bfloat16*>(pr.o), static_cast<const __nv_bfloat16*>(pr.dO), pr.delta, pr.dq_acc,
-        rows);
+    // The three kernels are launched with programmatic stream serialization:
+    // each may start while the previous one drains and waits (pdl_wait) only
+    // where it reads what that one wrote.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = pr.stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3((unsigned)((rows * (D / 8) + 255) / 256));
+    if (cudaLaunchKernelEx(&cfg, bwd_pre_tc_kernel<D>, static_cast<const __nv_bfloat16*>(pr.o),
+                           static_cast<const __nv_bfloat16*>(pr.dO), pr.delta, pr.dq_acc, rows) != cudaSuccess)
+        return FA_ERR_CUDA;
     note_launches(1);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
     BwdParams p{};
     p.lse = pr.lse;
@@ -697,19 +730,23 @@ int launch_bwd_tc_d(const Problem& pr) {
             return FA_ERR_CUDA;
         attr_set = true;
     }
-    dim3 grid((pr.N + kTile - 1) / kTile, BH);
-    bwd_tc_kernel<D><<<grid, kThreads, Cfg::kSmem, pr.stream>>>(tq, tk, tv, tdo, p);
+    cfg.gridDim = dim3((pr.N + kTile - 1) / kTile, BH);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D>, tq, tk, tv, tdo, p);
     note_launches(1);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: bwd_tc launch: %s\n", cudaGetErrorString(e));
         return FA_ERR_CUDA;
     }
     const size_t n4 = rows * D / 4;
-    dq_convert_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, pr.stream>>>(
-        reinterpret_cast<const float4*>(pr.dq_acc), static_cast<uint2*>(pr.dq), pr.scale, n4);
+    cfg.gridDim = dim3((unsigned)((n4 + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, dq_convert_kernel, reinterpret_cast<const float4*>(pr.dq_acc),
+                           static_cast<uint2*>(pr.dq), pr.scale, n4);
     note_launches(1);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace

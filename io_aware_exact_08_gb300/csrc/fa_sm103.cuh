@@ -105,6 +105,18 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, c
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched with the programmatic
+// stream-serialization attribute may start before the kernel ahead of it in
+// the stream has finished; pdl_wait() blocks until that kernel has completed
+// and its writes are visible (a no-op for a normal launch). pdl_trigger()
+// lets the next such kernel start launching once every CTA of this one has
+// issued it (or exited).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
