@@ -132,6 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sKV = smem + Cfg::kQBytes;
     SharedState* st = reinterpret_cast<SharedState*>(sKV + Cfg::kStages * Cfg::kTileBytes);
 
+    // launched with programmatic stream serialization: wait for the kernel
+    // ahead (it may have written Q, K, V, kv_len or the mask), then let the
+    // next one (the backward's preprocess) start launching behind this grid
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.y;
     const int b = bh / p.H, h = bh % p.H;
@@ -488,6 +493,11 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     uint8_t* sKV = smem + 2 * Cfg::kQBytes;
     SharedPP* st = reinterpret_cast<SharedPP*>(sKV + Cfg::kStages * Cfg::kTileBytes);
 
+    // launched with programmatic stream serialization: wait for the kernel
+    // ahead (it may have written Q, K, V, kv_len or the mask), then let the
+    // next one (the backward's preprocess) start launching behind this grid
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.y;
     const int b = bh / p.H, h = bh % p.H;
@@ -894,10 +904,18 @@ int launch_fwd_tc_d(const Problem& pr) {
             return FA_ERR_CUDA;
         attr_set = true;
     }
-    dim3 grid(kPingPong ? (p.n_qtiles + 1) / 2 : p.n_qtiles, BH);
-    kernel<<<grid, kBlock, kSmem, pr.stream>>>(tq, tk, tv, p);
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kPingPong ? (p.n_qtiles + 1) / 2 : p.n_qtiles, BH);
+    cfg.blockDim = dim3(kBlock);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = pr.stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
     note_launches(1);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: fwd_tc launch: %s\n", cudaGetErrorString(e));
         return FA_ERR_CUDA;
