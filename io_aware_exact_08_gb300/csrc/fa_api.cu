@@ -65,7 +65,13 @@ int from_cuda(cudaError_t e) {
     return FA_ERR_CUDA;
 }
 
-bool use_tensor_cores(const Problem& p) { return g_kernel_path == 0 && p.dtype == FA_BF16; }
+bool use_tensor_cores(const Problem& p) {
+    if (g_kernel_path != 0 || p.dtype != FA_BF16) return false;
+    // the tile lists of a block mask must fit in the kernels' shared memory
+    const int tiles = (p.N + kMaskBlock - 1) / kMaskBlock;
+    if (p.block_mask && tiles > (p.d == 128 ? kMaskListCapBwd128 : kMaskListCap)) return false;
+    return true;
+}
 
 }  // namespace
 

@@ -62,8 +62,11 @@ struct BwdCfg {
     static constexpr int kDsBytes = kTile * kTile * 2;  // dS^T, 128 x 128 bf16
     // (no alignment slack: the dynamic shared memory window starts 1024-byte
     // aligned, which the kernel checks)
-    static constexpr int kSmem =
+    // block masks: this key tile's list of visible query tiles
+    static constexpr int kListCap = (D == 128) ? kMaskListCapBwd128 : kMaskListCap;
+    static constexpr int kSmemBase =
         2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBytes + 2 * 2 * kTile * 4 /*lse, delta x2*/ + 256;
+    static constexpr int smem(bool mask) { return kSmemBase + (mask ? kListCap * 2 : 0); }
     static constexpr uint32_t kColS = 0, kColDP = 128;
     // dQ accumulator. D = 128: dQ^T (lanes = head-dim rows, 128 query
     // columns), aliasing dP^T. D = 64: dQ (lanes = query rows, 64 columns).
@@ -129,27 +132,39 @@ struct BwdShared {
     uint64_t lse_ready[2];
     uint32_t tmem_base;
     int abort_flag;
+    int n_list;  // block mask: visible query tiles of this key tile
 };
 
-// Query tiles that see key tile j, in increasing order.
+// Query tiles that see key tile j, in increasing order: without a block
+// mask (kMask false) the suffix [first, nqt) (first = j when causal), with
+// one the list built in shared memory at the start.
+template <bool kMask>
 struct QSched {
-    int jt, nqt, L, causal, nb;
-    const uint8_t* bm;
+    int jt, nqt, L, causal;
+    const uint16_t* list;
+    int n_list;
     __device__ bool key_tile_live() const { return jt * kTile < L; }
-    __device__ bool active(int i) const {
-        if (causal && i * kTile + kTile - 1 < jt * kTile) return false;
-        if (bm && !bm[(size_t)i * nb + jt]) return false;
-        return true;
-    }
+    __device__ bool active(int i) const { return !(causal && i * kTile + kTile - 1 < jt * kTile); }
     __device__ int next(int i) const {
         while (i < nqt && !active(i)) ++i;
         return i;
     }
     __device__ int count() const {
         if (!key_tile_live()) return 0;
+        if constexpr (kMask) return n_list;
         int c = 0;
         for (int i = next(0); i < nqt; i = next(i + 1)) ++c;
         return c;
+    }
+    // the first query tile, and the one after i, the k-th (k from 0); nqt
+    // past the last
+    __device__ int first() const {
+        if constexpr (kMask) return n_list > 0 ? (int)list[0] : nqt;
+        else return next(0);
+    }
+    __device__ int after(int i, int k) const {
+        if constexpr (kMask) return k + 1 < n_list ? (int)list[k + 1] : nqt;
+        else return next(i + 1);
     }
 };
 
@@ -169,7 +184,7 @@ __device__ __forceinline__ void red_add_f32(float* dst, float a) {
 }
 
 
-template <int D>
+template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -189,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sNegLse = reinterpret_cast<float*>(sDS + Cfg::kDsBytes);
     float* sNegDelta = sNegLse + 2 * kTile;
     BwdShared* st = reinterpret_cast<BwdShared*>(sNegDelta + 2 * kTile);
+    uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.y;
@@ -196,14 +212,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int jt = blockIdx.x;
     const int j0 = jt * kTile;
 
-    QSched sched;
+    QSched<kMask> sched;
     sched.jt = jt;
     sched.nqt = (p.N + kTile - 1) / kTile;
     sched.L = p.kv_len ? min(max(p.kv_len[b], 0), p.N) : p.N;
     sched.causal = p.causal;
-    sched.nb = p.nb;
-    sched.bm = p.block_mask;
+    sched.list = sList;
+    sched.n_list = 0;
     WaitCtx wctx{&st->abort_flag, p.status};
+    // block mask: warp 0 lists the query tiles whose mask block (i, j) is set
+    // (strided loads of one mask column, 32 at a time, and a ballot)
+    if (kMask && warp == 0) {
+        const int first = p.causal ? jt : 0;
+        int cnt = 0;
+        for (int c = first; c < sched.nqt; c += 32) {
+            const int i = c + lane;
+            const bool act = i < sched.nqt && p.block_mask[(size_t)i * p.nb + jt] != 0;
+            const uint32_t bal = __ballot_sync(0xffffffffu, act);
+            if (act) sList[cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)i;
+            cnt += __popc(bal);
+        }
+        if (lane == 0) st->n_list = cnt;
+    }
 
     if (tid == 0) {
         mbar_init(&st->kv_full, 1);
@@ -231,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = st->tmem_base;
+    if constexpr (kMask) sched.n_list = st->n_list;
     const int n_active = sched.count();
     // The next kernel (dq conversion) may start launching once every CTA is
     // here. Q, K, V, dO and LSE were complete before the preprocess kernel
@@ -255,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool issued_any[Cfg::kStages];
             for (int s = 0; s < Cfg::kStages; ++s) issued_any[s] = false;
             int t = 0;
-            for (int i = sched.next(0); i < sched.nqt; i = sched.next(i + 1), ++t) {
+            for (int i = sched.first(); i < sched.nqt; i = sched.after(i, t), ++t) {
                 const int s = t % Cfg::kStages;
                 const uint32_t ph = (t / Cfg::kStages) & 1;
                 if (!mbar_wait(&st->st_empty[s], ph ^ 1, wctx, 101)) break;
@@ -391,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = n_active > 0;
         int it = 0;
         pdl_wait();
-        for (int i = sched.next(0); ok && i < sched.nqt; i = sched.next(i + 1), ++it) {
+        for (int i = sched.first(); ok && i < sched.nqt; i = sched.after(i, it), ++it) {
             const int i0 = i * kTile;
             const int nvalid = min(kTile, p.N - i0);
 #pragma unroll
@@ -449,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool stage_lse = r < 64;
         const float* col_src = (stage_lse ? p.lse : p.delta) + (size_t)bh * p.N;
         const int nqt = sched.nqt;
-        int i_cur = sched.next(0);
+        int i_cur = sched.first();
         float col_val = 0.f;
         pdl_wait();
         if (n_active > 0) {
@@ -458,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = i_cur; n_active > 0 && i < sched.nqt; ++it) {
             const int i0 = i * kTile;
-            const int i_next = sched.next(i + 1);
+            const int i_next = sched.after(i, it);
             // per-query -LSE (log2 units; -inf for masked rows so P = 0) and
             // -delta, negated so that each pair of columns takes one paired
             // fma / add
@@ -725,15 +756,18 @@ int launch_bwd_tc_d(const Problem& pr) {
     p.seed = pr.seed;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(bwd_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::smem(false)) != cudaSuccess ||
+            cudaFuncSetAttribute(bwd_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::smem(true)) != cudaSuccess)
             return FA_ERR_CUDA;
         attr_set = true;
     }
     cfg.gridDim = dim3((pr.N + kTile - 1) / kTile, BH);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg::kSmem;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D>, tq, tk, tv, tdo, p);
+    cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr);
+    cudaError_t e = pr.block_mask ? cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, true>, tq, tk, tv, tdo, p)
+                                  : cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, false>, tq, tk, tv, tdo, p);
     note_launches(1);
     if (e != cudaSuccess) {
         if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: bwd_tc launch: %s\n", cudaGetErrorString(e));

@@ -1,25 +1,16 @@
 // Forward attention on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
 //
-// One CTA computes one 128-row query tile Q_i of one (batch, head) and walks
-// the key/value tiles K_j, V_j (128 keys each) that are not masked out,
-// following the per-block update of "FlashAttention: Fast and
-// Memory-Efficient Exact Attention with IO-Awareness" (section "Metode",
-// steps 1-4): S_ij = Q_i K_j^T, running row max m and row sum l, and
-// O_i <- e^{m_old - m_new} O_i + P~_ij V_j, with the division by l deferred
-// to the end (FlashAttention-2 section of the "Flash Attention" guide).
-// Fully masked tiles are skipped (causal future, key padding, zero blocks of
-// the block-sparse mask, "Ekstensi: Block-Sparse FlashAttention").
-//
-// Roles (192 threads, warp specialised as in the FlashAttention-3 section):
-//   warps 0-3  softmax: thread r owns query row r. It reads S from TMEM,
-//              masks, updates (m, l), writes P as bf16 back into the same
-//              TMEM columns, applies dropout, and does the epilogue.
-//   warp 4     producer: TMA loads of Q once, then K_0, K_1, V_0, K_2, V_1,
-//              ... through a ring of shared-memory stages.
-//   warp 5     MMA issuer: one elected lane issues tcgen05.mma for S_j = Q K_j^T
-//              (double-buffered in TMEM so S_{j+1} overlaps the softmax of
-//              S_j) and O += P_j V_j (P read from TMEM), and owns the TMEM
-//              allocation.
+// One CTA computes two 128-row query tiles of one (batch, head) and walks the
+// key/value tiles K_j, V_j (128 keys each) that are not masked out, following
+// the per-block update of "FlashAttention: Fast and Memory-Efficient Exact
+// Attention with IO-Awareness" (section "Metode", steps 1-4): S_ij = Q_i K_j^T,
+// running row max m and row sum l, and O_i <- e^{m_old - m_new} O_i +
+// P~_ij V_j, with the division by l deferred to the end (FlashAttention-2
+// section of the "Flash Attention" guide). Fully masked tiles are skipped
+// (causal future, key padding, zero blocks of the block-sparse mask,
+// "Ekstensi: Block-Sparse FlashAttention"). Warp specialisation follows the
+// FlashAttention-3 section of the guide and the two-tile ping-pong its
+// FlashAttention-4 section.
 //
 // The running max is only raised when a row's new maximum exceeds the one
 // in use by more than 2^8 (log2 units); between raises P <= 2^8, which fp32
@@ -44,21 +35,8 @@ using namespace sm103;
 
 constexpr int kBlockM = 128;  // query rows per CTA
 constexpr int kBlockN = 128;  // keys per tile
-constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-
-template <int D>
-struct FwdCfg {
-    static constexpr int kStages = (D == 128) ? 5 : 8;
-    static constexpr int kTileBytes = kBlockN * D * 2;   // one K or V tile, bf16
-    static constexpr int kQBytes = kBlockM * D * 2;
-    static constexpr int kBoxes = D / 64;                // 64-column TMA boxes per tile
-    static constexpr int kBoxBytes = kBlockN * 128;      // 128 rows x 128 bytes
-    static constexpr int kSmem = 1024 /*alignment slack*/ + kQBytes + kStages * kTileBytes + 256;
-    static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
-};
 
 struct FwdParams {
     float* lse;
@@ -75,386 +53,18 @@ struct FwdParams {
     uint64_t seed;
 };
 
-struct SharedState {
-    uint64_t kv_full[8];
-    uint64_t kv_empty[8];
-    uint64_t q_full;
-    uint64_t s_full[2];
-    uint64_t p_full[2];
-    uint64_t pv_done;
-    uint64_t o_final;
-    uint64_t teardown;
-    uint32_t tmem_base;
-    int abort_flag;
-};
-
-// Whether key tile j is visited by query tile qt, and its element mask type.
-struct TileSched {
-    int nkt;       // key tiles in the sequence
-    int L;         // visible keys: min(kv_len[b], N)
-    int qt;
-    int causal;
-    const uint8_t* bm_row;  // block-mask row of this query tile or nullptr
-
-    __device__ bool active(int j) const {
-        const int k0 = j * kBlockN;
-        if (k0 >= L) return false;
-        if (causal && k0 > qt * kBlockM + kBlockM - 1) return false;
-        if (bm_row && !bm_row[j]) return false;
-        return true;
-    }
-    __device__ int end() const {
-        int e = (L + kBlockN - 1) / kBlockN;
-        if (causal) e = min(e, qt + 1);
-        return min(e, nkt);
-    }
-    // next active tile index >= j, or end()
-    __device__ int next(int j) const {
-        const int e = end();
-        while (j < e && !active(j)) ++j;
-        return j;
-    }
-    __device__ int count() const {
-        int c = 0;
-        for (int j = next(0); j < end(); j = next(j + 1)) ++c;
-        return c;
-    }
-};
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using Cfg = FwdCfg<D>;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sKV = smem + Cfg::kQBytes;
-    SharedState* st = reinterpret_cast<SharedState*>(sKV + Cfg::kStages * Cfg::kTileBytes);
-
-    // launched with programmatic stream serialization: wait for the kernel
-    // ahead (it may have written Q, K, V, kv_len or the mask), then let the
-    // next one (the backward's preprocess) start launching behind this grid
-    pdl_wait();
-    pdl_trigger();
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.y;
-    const int b = bh / p.H, h = bh % p.H;
-    // heaviest query tiles first (causal work grows with the tile index)
-    const int qt = p.causal ? (p.n_qtiles - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-    const int row0 = qt * kBlockM;
-
-    TileSched sched;
-    sched.nkt = (p.N + kBlockN - 1) / kBlockN;
-    sched.L = p.kv_len ? min(max(p.kv_len[b], 0), p.N) : p.N;
-    sched.qt = qt;
-    sched.causal = p.causal;
-    sched.bm_row = p.block_mask ? p.block_mask + (size_t)qt * p.nb : nullptr;
-
-    WaitCtx wctx{&st->abort_flag, p.status};
-
-    if (tid == 0) {
-        for (int s = 0; s < Cfg::kStages; ++s) {
-            mbar_init(&st->kv_full[s], 1);
-            mbar_init(&st->kv_empty[s], 1);
-        }
-        mbar_init(&st->q_full, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&st->s_full[i], 1);
-            mbar_init(&st->p_full[i], kSoftmaxThreads / 32);
-        }
-        mbar_init(&st->pv_done, 1);
-        mbar_init(&st->o_final, 1);
-        mbar_init(&st->teardown, 1);
-        st->abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == 5) {
-        tmem_alloc(&st->tmem_base, Cfg::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = st->tmem_base;
-    const int n_active = sched.count();
-
-    if (warp == 4) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0 && n_active > 0) {
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(&st->q_full, Cfg::kQBytes);
-#pragma unroll
-            for (int x = 0; x < Cfg::kBoxes; ++x)
-                tma_load_3d(sQ + x * Cfg::kBoxBytes, &tm_q, &st->q_full, x * 64, row0, bh);
-            uint32_t issued_phase[Cfg::kStages];
-            bool issued_any[Cfg::kStages];
-            for (int s = 0; s < Cfg::kStages; ++s) issued_any[s] = false;
-            int t = 0;  // load counter
-            auto load = [&](const CUtensorMap* map, int j) -> bool {
-                const int s = t % Cfg::kStages;
-                const uint32_t ph = (t / Cfg::kStages) & 1;
-                if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 1)) return false;
-                mbar_arrive_expect_tx(&st->kv_full[s], Cfg::kTileBytes);
-                uint8_t* dst = sKV + s * Cfg::kTileBytes;
-#pragma unroll
-                for (int x = 0; x < Cfg::kBoxes; ++x)
-                    tma_load_3d(dst + x * Cfg::kBoxBytes, map, &st->kv_full[s], x * 64, j * kBlockN, bh);
-                issued_phase[s] = ph;
-                issued_any[s] = true;
-                ++t;
-                return true;
-            };
-            // order: K(a0), K(a1), V(a0), K(a2), V(a1), ... (a = active tiles)
-            const int e = sched.end();
-            int ja = sched.next(0);
-            int jb = (ja < e) ? sched.next(ja + 1) : e;
-            bool ok = load(&tm_k, ja);
-            if (ok && jb < e) ok = load(&tm_k, jb);
-            int jc = (jb < e) ? sched.next(jb + 1) : e;
-            while (ok && ja < e) {
-                ok = load(&tm_v, ja);
-                if (ok && jc < e) ok = load(&tm_k, jc);
-                ja = jb;
-                jb = jc;
-                jc = (jc < e) ? sched.next(jc + 1) : e;
-            }
-            // drain: every issued copy has landed before the CTA may exit
-            for (int s = 0; s < Cfg::kStages; ++s)
-                if (issued_any[s]) mbar_wait(&st->kv_full[s], issued_phase[s], wctx, 2);
-            mbar_wait(&st->q_full, 0, wctx, 3);
-        }
-    } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
-        if (n_active > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kBlockM, D, 0, 1);
-            const uint32_t q_base = smem_u32(sQ);
-            const uint32_t kv_base = smem_u32(sKV);
-            const uint64_t qd = smem_desc_sw128(q_base, 16, 1024);
-            int t = 0;  // consume counter, same order as the producer
-            bool ok = mbar_wait_warp(&st->q_full, 0, wctx, 10);
-            tc_fence_after();
-            auto wait_tile = [&](uint32_t& addr) -> bool {
-                const int s = t % Cfg::kStages;
-                if (!mbar_wait_warp(&st->kv_full[s], (t / Cfg::kStages) & 1, wctx, 11)) return false;
-                tc_fence_after();
-                addr = kv_base + s * Cfg::kTileBytes;
-                return true;
-            };
-            auto release_tile = [&]() {
-                mma_commit_warp(&st->kv_empty[t % Cfg::kStages]);
-                ++t;
-            };
-            auto issue_s = [&](int buf) -> bool {
-                uint32_t kaddr;
-                if (!wait_tile(kaddr)) return false;
-                const uint32_t d = tmem + (buf ? Cfg::kColS1 : Cfg::kColS0);
-                const uint64_t kd = smem_desc_sw128(kaddr, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                    mma_ss_warp(d, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0);
-                }
-                mma_commit_warp(&st->s_full[buf]);
-                release_tile();
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            if (ok && n_active > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < n_active; ++j) {
-                const int buf = j & 1;
-                if (!mbar_wait_warp(&st->p_full[buf], (j >> 1) & 1, wctx, 12)) break;
-                tc_fence_after();
-                uint32_t vaddr;
-                if (!wait_tile(vaddr)) break;
-                const uint32_t a_tmem = tmem + (buf ? Cfg::kColS1 : Cfg::kColS0);
-                const uint64_t vd = smem_desc_sw128(vaddr, Cfg::kBoxBytes, 1024);
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    // P: 16 keys = 8 TMEM columns of bf16 pairs; V: 16 rows of 128 bytes
-                    mma_ts_warp(tmem + Cfg::kColO, a_tmem + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                release_tile();
-                mma_commit_warp(&st->pv_done);
-                if (j + 1 == n_active) mma_commit_warp(&st->o_final);
-                if (j + 2 < n_active) ok = issue_s(buf);
-            }
-            // every MMA this thread issued has completed before TMEM is freed
-            mma_commit_warp(&st->teardown);
-            mbar_wait_warp(&st->teardown, 0, wctx, 13);
-        }
-    } else {
-        // ------------------------------------------------------------ softmax
-        const int r = tid;  // row within the tile == TMEM lane
-        const int i = row0 + r;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        float m = -INFINITY;  // running max in use (log2 units)
-        float l = 0.f;
-        bool ok = true;
-        int j = sched.next(0);
-        for (int it = 0; it < n_active; ++it, j = sched.next(j + 1)) {
-            const int buf = it & 1;
-            const uint32_t sbase = tmem + lane_base + (buf ? Cfg::kColS1 : Cfg::kColS0);
-            if (!mbar_wait_warp(&st->s_full[buf], (it >> 1) & 1, wctx, 20)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(sbase + c * 32, sr[c]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
-            float s[kBlockN];
-#pragma unroll
-            for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sr[c / 32][c % 32]);
-            // element mask: visible keys of this tile form a prefix [0, lim)
-            const int k0 = j * kBlockN;
-            int lim = min(kBlockN, sched.L - k0);
-            if (p.causal) lim = min(lim, i - k0 + 1);
-            if (lim < kBlockN) {
-#pragma unroll
-                for (int c = 0; c < kBlockN; ++c)
-                    if (c >= lim) s[c] = -INFINITY;
-            }
-            // row max as a tree of 16 independent partial maxima (a single
-            // running max would be a 128-long dependent chain)
-            float pm[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) pm[c] = fmaxf(s[c], s[c + 16]);
-#pragma unroll
-            for (int c = 32; c < kBlockN; c += 16) {
-#pragma unroll
-                for (int x = 0; x < 16; ++x) pm[x] = fmaxf(pm[x], s[c + x]);
-            }
-#pragma unroll
-            for (int w = 8; w > 0; w >>= 1) {
-#pragma unroll
-                for (int x = 0; x < w; ++x) pm[x] = fmaxf(pm[x], pm[x + w]);
-            }
-            const float mt = pm[0] * p.scale_log2;  // scale_log2 > 0
-            const bool raise = mt > m + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, raise) && it > 0) {
-                // O must hold P_{it-1} V_{it-1} before it is rescaled. S_it
-                // was committed after P_{it-2} V_{it-2}, so pv_done has
-                // completed it-1 or it phases and the parity is unambiguous.
-                if (!mbar_wait_warp(&st->pv_done, (it - 1) & 1, wctx, 21)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const float alpha = raise ? ex2_approx(m - mt) : 1.f;
-                const uint32_t obase = tmem + lane_base + Cfg::kColO;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t orr[32];
-                    tmem_ld32(obase + c * 32, orr);
-                    tmem_ld_wait();
-                    reg_fence(orr);
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) orr[x] = __float_as_uint(__uint_as_float(orr[x]) * alpha);
-                    tmem_st32(obase + c * 32, orr);
-                }
-                if (raise) l *= alpha;
-            }
-            if (raise) m = mt;
-            const float mref = (m == -INFINITY) ? 0.f : m;
-            // exponentials and row sum, 8 independent partial sums
-            float ps[8];
-#pragma unroll
-            for (int x = 0; x < 8; ++x) ps[x] = 0.f;
-#pragma unroll
-            for (int c = 0; c < kBlockN; ++c) {
-                const float pe = ex2_approx(fmaf(s[c], p.scale_log2, -mref));
-                s[c] = pe;
-                ps[c & 7] += pe;
-            }
-#pragma unroll
-            for (int w = 4; w > 0; w >>= 1) {
-#pragma unroll
-                for (int x = 0; x < w; ++x) ps[x] += ps[x + w];
-            }
-            l += ps[0];
-            if (p.dropout) {
-#pragma unroll
-                for (int g = 0; g < kBlockN / 4; ++g) {
-                    const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, i, (k0 >> 2) + g);
-#pragma unroll
-                    for (int w = 0; w < 4; ++w)
-                        if (!((bits >> w) & 1u)) s[4 * g + w] = 0.f;
-                }
-            }
-            uint32_t pk[2][32];
-#pragma unroll
-            for (int c = 0; c < 64; ++c) pk[c / 32][c % 32] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
-            tmem_st32(sbase, pk[0]);
-            tmem_st32(sbase + 32, pk[1]);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive_warp(&st->p_full[buf]);
-        }
-        // epilogue
-        __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N) * D;
-        if (ok && n_active > 0) {
-            // pv_done may still be two phases behind here (the last S MMA
-            // was issued before the second-to-last P V), so the final O has
-            // its own single-phase barrier
-            if (mbar_wait_warp(&st->o_final, 0, wctx, 22)) {
-                tc_fence_after();
-                const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
-                const uint32_t obase = tmem + lane_base + Cfg::kColO;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t orr[32];
-                    tmem_ld32(obase + c * 32, orr);
-                    tmem_ld_wait();
-                    reg_fence(orr);
-                    if (i < p.N) {
-                        uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D + c * 32);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 w4;
-                            w4.x = pack_bf16x2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
-                            w4.y = pack_bf16x2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
-                            w4.z = pack_bf16x2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
-                            w4.w = pack_bf16x2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
-                            dst[v] = w4;
-                        }
-                    }
-                }
-                if (i < p.N) p.lse[(size_t)bh * p.N + i] = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
-            }
-        } else if (n_active == 0 && i < p.N) {
-            uint4 z = make_uint4(0, 0, 0, 0);
-            uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D);
-#pragma unroll
-            for (int v = 0; v < D / 8; ++v) dst[v] = z;
-            p.lse[(size_t)bh * p.N + i] = -INFINITY;
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, Cfg::kTmemCols);
-}
-
-
 // ---------------------------------------------------------------------------
-// Two query tiles per CTA (256 rows), one softmax warpgroup per tile, sharing
-// one K/V stream. The MMA warp issues, per key tile u,
-//     P_0(u) V_u, S_0(u+1), P_1(u) V_u, S_1(u+1)
+// Two query tiles per CTA (256 rows), one softmax warpgroup per tile. The MMA
+// warp issues, per step u,
+//     P_0(u) V, S_0(u+1), P_1(u) V, S_1(u+1)
 // so the softmax of one tile runs while the tensor core works on the other
-// (the ping-pong of the FlashAttention-4 design). Used when both tiles visit
-// the same key tiles up to their own count (no block mask): tile t visits
-// key tiles 0 .. n_t - 1.
+// (the ping-pong of the FlashAttention-4 design). Without a block mask tile t
+// visits key tiles 0 .. n_t - 1 and both tiles share one K/V stream (K_u,
+// V_u); with one (kSplit) each tile visits the tiles of its own list and the
+// producer loads them in the order of use.
 // Roles (320 threads): warps 0-3 softmax of tile 0, warps 4-7 softmax of
-// tile 1, warp 8 TMA producer, warp 9 MMA issuer.
+// tile 1, warp 8 TMA producer, warp 9 MMA issuer (all 32 lanes run its loop,
+// one elected lane issues).
 // ---------------------------------------------------------------------------
 constexpr int kThreadsPP = 320;
 
@@ -465,7 +75,8 @@ struct FwdPPCfg {
     static constexpr int kQBytes = kBlockM * D * 2;  // per query tile
     static constexpr int kBoxes = D / 64;
     static constexpr int kBoxBytes = kBlockN * 128;
-    static constexpr int kSmem = 1024 + 2 * kQBytes + kStages * kTileBytes + 256;
+    // + the two query tiles' lists of visible key tiles (block masks)
+    static constexpr int kSmem = 1024 + 2 * kQBytes + kStages * kTileBytes + 256 + 2 * kMaskListCap * 2;
     static constexpr uint32_t kTmemCols = 512;
     // S_t at columns 128 t, O_t at 256 + D t
 };
@@ -480,9 +91,10 @@ struct SharedPP {
     uint64_t teardown;
     uint32_t tmem_base;
     int abort_flag;
+    int n_list[2];  // kSplit: visible key tiles of each query tile
 };
 
-template <int D>
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreadsPP, 1)
     fwd_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -492,6 +104,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     uint8_t* sQ = smem;  // tile t at t * kQBytes
     uint8_t* sKV = smem + 2 * Cfg::kQBytes;
     SharedPP* st = reinterpret_cast<SharedPP*>(sKV + Cfg::kStages * Cfg::kTileBytes);
+    uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);  // [2][kMaskListCap]
 
     // launched with programmatic stream serialization: wait for the kernel
     // ahead (it may have written Q, K, V, kv_len or the mask), then let the
@@ -512,8 +125,29 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         const int qt = 2 * pair + t;
         n_t[t] = (qt < p.n_qtiles) ? (p.causal ? min(nkt, qt + 1) : nkt) : 0;
     }
-    const int n_max = max(n_t[0], n_t[1]);
     WaitCtx wctx{&st->abort_flag, p.status};
+    // kSplit (block mask): each query tile walks its own list of visible key
+    // tiles, built here by warp 0 from its mask row (coalesced loads and a
+    // ballot), and the K/V tiles of the two lists are loaded one after the
+    // other in the order the MMA warp uses them
+    if (kSplit && warp == 0) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int qt = 2 * pair + t;
+            int e = (qt < p.n_qtiles) ? nkt : 0;
+            if (p.causal) e = min(e, qt + 1);
+            const uint8_t* row = p.block_mask + (size_t)qt * p.nb;
+            int cnt = 0;
+            for (int c = 0; c < e; c += 32) {
+                const int j = c + lane;
+                const bool act = j < e && row[j] != 0;
+                const uint32_t bal = __ballot_sync(0xffffffffu, act);
+                if (act) sList[t * kMaskListCap + cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)j;
+                cnt += __popc(bal);
+            }
+            if (lane == 0) st->n_list[t] = cnt;
+        }
+    }
 
     if (tid == 0) {
         for (int s = 0; s < Cfg::kStages; ++s) {
@@ -538,6 +172,13 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = st->tmem_base;
+    if constexpr (kSplit) {
+        n_t[0] = st->n_list[0];
+        n_t[1] = st->n_list[1];
+    }
+    const int n_max = max(n_t[0], n_t[1]);
+    const uint16_t* list0 = sList;
+    const uint16_t* list1 = sList + kMaskListCap;
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
@@ -552,18 +193,48 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                 for (int x = 0; x < Cfg::kBoxes; ++x)
                     tma_load_3d(sQ + t * Cfg::kQBytes + x * Cfg::kBoxBytes, &tm_q, &st->q_full, x * 64,
                                 (2 * pair + t) * kBlockM, bh);
-            // load index 2u = K_u, 2u + 1 = V_u
-            int t = 0;
-            for (; t < 2 * n_max; ++t) {
-                const int s = t % Cfg::kStages;
-                const uint32_t ph = (t / Cfg::kStages) & 1;
-                if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 61)) break;
-                mbar_arrive_expect_tx(&st->kv_full[s], Cfg::kTileBytes);
-                uint8_t* dst = sKV + s * Cfg::kTileBytes;
-                const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
+            int t = 0;  // load counter
+            if constexpr (!kSplit) {
+                // load index 2u = K_u, 2u + 1 = V_u
+                for (; t < 2 * n_max; ++t) {
+                    const int s = t % Cfg::kStages;
+                    const uint32_t ph = (t / Cfg::kStages) & 1;
+                    if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 61)) break;
+                    mbar_arrive_expect_tx(&st->kv_full[s], Cfg::kTileBytes);
+                    uint8_t* dst = sKV + s * Cfg::kTileBytes;
+                    const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
 #pragma unroll
-                for (int x = 0; x < Cfg::kBoxes; ++x)
-                    tma_load_3d(dst + x * Cfg::kBoxBytes, map, &st->kv_full[s], x * 64, (t >> 1) * kBlockN, bh);
+                    for (int x = 0; x < Cfg::kBoxes; ++x)
+                        tma_load_3d(dst + x * Cfg::kBoxBytes, map, &st->kv_full[s], x * 64, (t >> 1) * kBlockN, bh);
+                }
+            } else {
+                // K of S_0(0), K of S_1(0), then per step u and tile t: V of
+                // P_t V, K of the tile's next S
+                auto load = [&](const CUtensorMap* map, int j) -> bool {
+                    const int s = t % Cfg::kStages;
+                    const uint32_t ph = (t / Cfg::kStages) & 1;
+                    if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 61)) return false;
+                    mbar_arrive_expect_tx(&st->kv_full[s], Cfg::kTileBytes);
+                    uint8_t* dst = sKV + s * Cfg::kTileBytes;
+#pragma unroll
+                    for (int x = 0; x < Cfg::kBoxes; ++x)
+                        tma_load_3d(dst + x * Cfg::kBoxBytes, map, &st->kv_full[s], x * 64, j * kBlockN, bh);
+                    ++t;
+                    return true;
+                };
+                bool okp = true;
+                if (n_t[0] > 0) okp = load(&tm_k, list0[0]);
+                if (okp && n_t[1] > 0) okp = load(&tm_k, list1[0]);
+                for (int u = 0; okp && u < n_max; ++u) {
+                    if (u < n_t[0]) {
+                        okp = load(&tm_v, list0[u]);
+                        if (okp && u + 1 < n_t[0]) okp = load(&tm_k, list0[u + 1]);
+                    }
+                    if (okp && u < n_t[1]) {
+                        okp = load(&tm_v, list1[u]);
+                        if (okp && u + 1 < n_t[1]) okp = load(&tm_k, list1[u + 1]);
+                    }
+                }
             }
             // drain: the last load issued into each stage has landed
             for (int l = max(0, t - Cfg::kStages); l < t; ++l)
@@ -588,6 +259,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             const uint64_t kvd_k = smem_desc_sw128(kv_base, 16, 1024);              // K tiles, K-major
             const uint64_t kvd_v = smem_desc_sw128(kv_base, Cfg::kBoxBytes, 1024);  // V tiles, MN-major
             constexpr uint32_t kStageUnits = Cfg::kTileBytes >> 4;
+            if constexpr (!kSplit) {
             // S_t(0) = Q_t K_0^T
             if (ok) {
                 ok = mbar_wait_warp(&st->kv_full[0], 0, wctx, 71);
@@ -661,6 +333,73 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                 mma_commit_warp(&st->kv_empty[sv]);
                 if (need_k) mma_commit_warp(&st->kv_empty[sk]);
             }
+            } else {
+            int ld = 0;  // next load to use, in the producer's order
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (!ok || (t ? c1 : c0) == 0) continue;
+                const int s = ld % Cfg::kStages;
+                ok = mbar_wait_warp(&st->kv_full[s], (ld / Cfg::kStages) & 1, wctx, 71);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t qd = t ? qd1 : qd0;
+                const uint64_t kd = kvd_k + (uint64_t)(s * kStageUnits);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                    mma_ss_warp(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0);
+                }
+                mma_commit_warp(&st->s_full[t]);
+                mma_commit_warp(&st->kv_empty[s]);
+                ++ld;
+            }
+            for (int u = 0; ok && u < n_max; ++u) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int ct = t ? c1 : c0;
+                    if (u >= ct) continue;
+                    // P_t(u) V
+                    if (!mbar_wait_warp(&st->p_full[t], u & 1, wctx, 72)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    int s = ld % Cfg::kStages;
+                    if (!mbar_wait_warp(&st->kv_full[s], (ld / Cfg::kStages) & 1, wctx, 74)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t vd = kvd_v + (uint64_t)(s * kStageUnits);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockN / 16; ++kk)
+                        mma_ts_warp(tmem + 256 + t * D, tmem + t * 128 + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
+                                    (u > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_warp(&st->kv_empty[s]);
+                    ++ld;
+                    if (u + 1 == ct) mma_commit_warp(&st->o_final[t]);
+                    if (u + 1 < ct) {
+                        // S_t of the tile's next key tile over the S/P columns just read
+                        s = ld % Cfg::kStages;
+                        if (!mbar_wait_warp(&st->kv_full[s], (ld / Cfg::kStages) & 1, wctx, 75)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t qd = t ? qd1 : qd0;
+                        const uint64_t kd = kvd_k + (uint64_t)(s * kStageUnits);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                            mma_ss_warp(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0);
+                        }
+                        mma_commit_warp(&st->s_full[t]);
+                        mma_commit_warp(&st->kv_empty[s]);
+                        ++ld;
+                    }
+                }
+            }
+            }
             mma_commit_warp(&st->teardown);
             mbar_wait_warp(&st->teardown, 0, wctx, 73);
         }
@@ -676,14 +415,17 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         float m = -INFINITY;
         float l = 0.f;
         bool ok = true;
+        // key tile of step u: u itself, or the u-th entry of this tile's list
+        const uint16_t* my_list = t ? list1 : list0;
         for (int u = 0; u < n; ++u) {
+            const int ktile = kSplit ? (int)my_list[u] : u;
             // dropout keep bits of this row's 128 keys (bit x of keep[c] is
             // key 32c + x), drawn before S arrives
             uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
             if (p.dropout) {
 #pragma unroll 1
                 for (int g = 0; g < 32; ++g) {
-                    const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, i, u * (kBlockN / 4) + g);
+                    const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, i, ktile * (kBlockN / 4) + g);
                     if (g == 0) keep[0] = keep[1] = keep[2] = keep[3] = 0;
                     const uint32_t sh = bits << (4 * (g & 7));
                     if ((g >> 3) == 0) keep[0] |= sh;
@@ -698,7 +440,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             }
             // S_t(u) was issued after P_t(u-1) V: O_t is complete here
             tc_fence_after();
-            const int k0 = u * kBlockN;
+            const int k0 = ktile * kBlockN;
             int lim = min(kBlockN, L - k0);
             if (p.causal) lim = min(lim, i - k0 + 1);
             const bool full = lim >= kBlockN;
@@ -872,10 +614,9 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int BH, int N, int d, in
     return r == CUDA_SUCCESS;
 }
 
-template <int D, bool kPingPong>
+template <int D, bool kSplit>
 int launch_fwd_tc_d(const Problem& pr) {
-    constexpr int kSmem = kPingPong ? FwdPPCfg<D>::kSmem : FwdCfg<D>::kSmem;
-    constexpr int kBlock = kPingPong ? kThreadsPP : kThreads;
+    constexpr int kSmem = FwdPPCfg<D>::kSmem;
     CUtensorMap tq, tk, tv;
     const int BH = pr.B * pr.H;
     if (!make_tmap_bf16(&tq, pr.q, BH, pr.N, D, kBlockM) || !make_tmap_bf16(&tk, pr.k, BH, pr.N, D, kBlockN) ||
@@ -897,7 +638,7 @@ int launch_fwd_tc_d(const Problem& pr) {
     p.dropout = pr.dropout_p > 0.f;
     p.causal = pr.causal;
     p.seed = pr.seed;
-    auto kernel = kPingPong ? fwd_pp_kernel<D> : fwd_tc_kernel<D>;
+    auto kernel = fwd_pp_kernel<D, kSplit>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
@@ -908,8 +649,8 @@ int launch_fwd_tc_d(const Problem& pr) {
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kPingPong ? (p.n_qtiles + 1) / 2 : p.n_qtiles, BH);
-    cfg.blockDim = dim3(kBlock);
+    cfg.gridDim = dim3((p.n_qtiles + 1) / 2, BH);
+    cfg.blockDim = dim3(kThreadsPP);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = pr.stream;
     cfg.attrs = pdl;
@@ -925,10 +666,10 @@ int launch_fwd_tc_d(const Problem& pr) {
 
 int launch_fwd_tc(const Problem& p) {
     if (!(p.scale > 0.f)) return launch_fwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
-    // the two-tile kernel needs both tiles' key lists to be prefixes of one
-    // list (no block mask); block-sparse runs one query tile per CTA
-    if (p.block_mask) return p.d == 64 ? launch_fwd_tc_d<64, false>(p) : launch_fwd_tc_d<128, false>(p);
-    return p.d == 64 ? launch_fwd_tc_d<64, true>(p) : launch_fwd_tc_d<128, true>(p);
+    // without a block mask both tiles' key lists are prefixes of one list and
+    // share its K/V loads; with one, each tile has its own list (kSplit)
+    if (p.block_mask) return p.d == 64 ? launch_fwd_tc_d<64, true>(p) : launch_fwd_tc_d<128, true>(p);
+    return p.d == 64 ? launch_fwd_tc_d<64, false>(p) : launch_fwd_tc_d<128, false>(p);
 }
 
 }  // namespace fa

@@ -39,6 +39,12 @@ struct Problem {
 };
 
 constexpr int kMaskBlock = 128;
+// With a block mask the tensor-core kernels keep each CTA's list of visible
+// tiles in shared memory: at most kMaskListCap entries (kMaskListCapBwd128
+// in the d = 128 backward, whose shared memory is otherwise full). Larger
+// masks run on the CUDA-core kernels.
+constexpr int kMaskListCap = 1024;
+constexpr int kMaskListCapBwd128 = 256;
 
 // Counts kernel launches for fa_launch_count (thread-safe).
 void note_launches(int n);
