@@ -207,9 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.y;
+    // grid (B*H, key tiles): dispatched x fastest, so under a causal mask the
+    // heaviest key tiles (lowest j) of every head go out first
+    const int bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H;
-    const int jt = blockIdx.x;
+    const int jt = blockIdx.y;
     const int j0 = jt * kTile;
 
     QSched<kMask> sched;
@@ -763,7 +765,7 @@ int launch_bwd_tc_d(const Problem& pr) {
             return FA_ERR_CUDA;
         attr_set = true;
     }
-    cfg.gridDim = dim3((pr.N + kTile - 1) / kTile, BH);
+    cfg.gridDim = dim3(BH, (pr.N + kTile - 1) / kTile);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr);
     cudaError_t e = pr.block_mask ? cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, true>, tq, tk, tv, tdo, p)

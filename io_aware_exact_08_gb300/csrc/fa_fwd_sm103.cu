@@ -112,10 +112,12 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     pdl_wait();
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.y;
+    // grid (B*H, pairs): the hardware dispatches x fastest, so every head's
+    // heaviest pair (causal) goes out before any lighter one
+    const int bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H;
     const int n_pairs = (p.n_qtiles + 1) / 2;
-    const int pair = p.causal ? (n_pairs - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    const int pair = p.causal ? (n_pairs - 1 - (int)blockIdx.y) : (int)blockIdx.y;
     const int L = p.kv_len ? min(max(p.kv_len[b], 0), p.N) : p.N;
     const int nkt = (L + kBlockN - 1) / kBlockN;  // key tiles with a visible key
     // key tiles visited by query tile t of this CTA (0 if the tile is past N)
@@ -649,7 +651,7 @@ int launch_fwd_tc_d(const Problem& pr) {
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((p.n_qtiles + 1) / 2, BH);
+    cfg.gridDim = dim3(BH, (p.n_qtiles + 1) / 2);
     cfg.blockDim = dim3(kThreadsPP);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = pr.stream;
