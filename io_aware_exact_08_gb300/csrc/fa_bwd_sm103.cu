@@ -24,9 +24,11 @@
 //      reduction warps add it into the fp32 accumulator in global memory.
 //      dK_j, dV_j stay in TMEM until the end.
 //   3. convert: dq = dtype(scale * dQacc).
-// Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer, warps
-// 10-13 dQ reduction (one per TMEM lane quarter), so that the compute warps
-// never wait for the dQ product or for the reductions to drain into L2.
+// Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer, four dQ
+// reduction warps (one per TMEM lane quarter: warps 10-13 at D = 128, 12-15
+// at D = 64, where warps 10-11 idle to complete a warpgroup), so that the
+// compute warps never wait for the dQ product or for the reductions to
+// drain into L2.
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -49,11 +51,21 @@ using namespace sm103;
 
 constexpr int kTile = 128;          // keys per CTA, queries per step
 constexpr int kComputeThreads = 256;
-constexpr int kReduceWarp0 = 10;
-constexpr int kThreads = 448;
+
+// register budgets of the D = 64 warpgroups (see BwdCfg)
+constexpr int kComputeRegs = 184, kIssueRegs = 40, kReduceRegs = 96;
 
 template <int D>
 struct BwdCfg {
+    // D = 64: 512 threads (four warpgroups: compute, compute, producer + MMA
+    // + two idle warps, dQ reduction) with setmaxnreg budgets of 184 / 40 /
+    // 96 registers (256*184 + 128*40 + 128*96 = 64512 <= 65536), which
+    // removes the compute warps' spills. D = 128: 448 threads at 128
+    // registers, where every budget split measured slower (its instances
+    // spill more).
+    static constexpr bool kRegSplit = (D == 64);
+    static constexpr int kThreads = kRegSplit ? 512 : 448;
+    static constexpr int kReduceWarp0 = kRegSplit ? 12 : 10;
     static constexpr int kStages = (D == 128) ? 2 : 3;
     static constexpr int kTileBytes = kTile * D * 2;  // one 128 x D bf16 tile
     static constexpr int kBoxBytes = kTile * 128;     // 128 rows x 64 columns
@@ -185,7 +197,7 @@ __device__ __forceinline__ void red_add_f32(float* dst, float a) {
 
 
 template <int D, bool kMask>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
@@ -273,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
+        if constexpr (Cfg::kRegSplit) regs_dec<kIssueRegs>();
         if (lane == 0 && n_active > 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
@@ -307,8 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (issued_any[s]) mbar_wait(&st->st_full[s], issued_phase[s], wctx, 102);
             mbar_wait(&st->kv_full, 0, wctx, 103);
         }
+    } else if (Cfg::kRegSplit && (warp == 10 || warp == 11)) {
+        // idle: the rest of the producer / MMA warpgroup
+        if constexpr (Cfg::kRegSplit) regs_dec<kIssueRegs>();
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
+        if constexpr (Cfg::kRegSplit) regs_dec<kIssueRegs>();
         if ((Cfg::kWarpIssue || lane == 0) && n_active > 0) {
             using I = Issue<Cfg::kWarpIssue>;
             constexpr uint32_t id_sh = idesc_bf16_f32(kTile, 64, 0, 0);      // S^T_h, dP^T_h (N = 64)
@@ -413,8 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             I::commit(&st->teardown);
             I::wait(&st->teardown, 0, wctx, 114);
         }
-    } else if (warp >= kReduceWarp0) {
+    } else if (warp >= Cfg::kReduceWarp0) {
         // ------------------------------------------------------------ dQ reduction
+        if constexpr (Cfg::kRegSplit) regs_dec<kReduceRegs>();
         // D = 128: dQ^T, lane = head-dim index, so one reduction instruction
         // covers 32 consecutive floats of one query row. D = 64: dQ, lane =
         // query row, 64 consecutive floats in 16-byte reductions.
@@ -467,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ compute
+        if constexpr (Cfg::kRegSplit) regs_inc<kComputeRegs>();
         const int quarter = warp & 3;      // TMEM lane quarter
         const int half = warp >> 2;        // query columns [64*half, 64*half + 64)
         const int r = quarter * 32 + lane;  // key row within the tile
@@ -766,7 +785,7 @@ int launch_bwd_tc_d(const Problem& pr) {
         attr_set = true;
     }
     cfg.gridDim = dim3(BH, (pr.N + kTile - 1) / kTile);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr);
     cudaError_t e = pr.block_mask ? cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, true>, tq, tk, tv, tdo, p)
                                   : cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, false>, tq, tk, tv, tdo, p);

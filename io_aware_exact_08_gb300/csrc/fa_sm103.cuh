@@ -112,6 +112,19 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, c
 // lets the next such kernel start launching once every CTA of this one has
 // issued it (or exited).
 // ---------------------------------------------------------------------------
+// Per-warpgroup register budgets (setmaxnreg): every warp of a warpgroup
+// executes the same call; the budgets of all warpgroups must add up to at
+// most the registers the CTA was launched with, or .inc would wait forever.
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
