@@ -54,6 +54,8 @@ constexpr int kComputeThreads = 256;
 
 // register budgets of the D = 64 warpgroups (see BwdCfg)
 constexpr int kComputeRegs = 184, kIssueRegs = 40, kReduceRegs = 96;
+static_assert(256 * kComputeRegs + 128 * kIssueRegs + 128 * kReduceRegs <= 512 * 128,
+              "register budgets above a 512-thread launch at 128 registers");
 
 template <int D>
 struct BwdCfg {
@@ -782,6 +784,21 @@ int launch_bwd_tc_d(const Problem& pr) {
             cudaFuncSetAttribute(bwd_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::smem(true)) != cudaSuccess)
             return FA_ERR_CUDA;
+        if constexpr (Cfg::kRegSplit) {
+            // setmaxnreg.inc takes registers from what the CTA was launched
+            // with and waits (without bound) until they are free: refuse to
+            // launch unless the budgets fit in that allocation
+            constexpr int need = 256 * kComputeRegs + 128 * kIssueRegs + 128 * kReduceRegs;
+            cudaFuncAttributes a0{}, a1{};
+            if (cudaFuncGetAttributes(&a0, bwd_tc_kernel<D, false>) != cudaSuccess ||
+                cudaFuncGetAttributes(&a1, bwd_tc_kernel<D, true>) != cudaSuccess ||
+                a0.numRegs * Cfg::kThreads < need || a1.numRegs * Cfg::kThreads < need) {
+                if (std::getenv("FA_DEBUG"))
+                    std::fprintf(stderr, "fa: bwd register budget %d exceeds the launch allocation (%d, %d regs)\n",
+                                 need, a0.numRegs, a1.numRegs);
+                return FA_ERR_CUDA;
+            }
+        }
         attr_set = true;
     }
     cfg.gridDim = dim3(BH, (pr.N + kTile - 1) / kTile);

@@ -62,11 +62,18 @@ struct FwdParams {
 // visits key tiles 0 .. n_t - 1 and both tiles share one K/V stream (K_u,
 // V_u); with one (kSplit) each tile visits the tiles of its own list and the
 // producer loads them in the order of use.
-// Roles (320 threads): warps 0-3 softmax of tile 0, warps 4-7 softmax of
-// tile 1, warp 8 TMA producer, warp 9 MMA issuer (all 32 lanes run its loop,
-// one elected lane issues).
+// Roles (384 threads, three warpgroups): warps 0-3 softmax of tile 0, warps
+// 4-7 softmax of tile 1, warp 8 TMA producer, warp 9 MMA issuer (all 32 lanes
+// run its loop, one elected lane issues), warps 10-11 idle. setmaxnreg moves
+// registers from the third warpgroup to the softmax warpgroups (208 each
+// thread against 80; launched at 168), which removes the softmax spills.
 // ---------------------------------------------------------------------------
-constexpr int kThreadsPP = 320;
+constexpr int kThreadsPP = 384;
+constexpr int kSoftmaxRegs = 208, kIssueRegs = 80;
+// setmaxnreg.inc takes registers from the CTA's launch allocation (384
+// threads at 168, the most a 384-thread launch gets) and waits until they
+// are free, so the budgets must fit in it
+static_assert(256 * kSoftmaxRegs + 128 * kIssueRegs <= kThreadsPP * 168, "register budgets above the launch");
 
 template <int D>
 struct FwdPPCfg {
@@ -184,6 +191,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
+        regs_dec<kIssueRegs>();
         if (lane == 0 && n_max > 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
@@ -243,8 +251,11 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                 mbar_wait(&st->kv_full[l % Cfg::kStages], (l / Cfg::kStages) & 1, wctx, 62);
             mbar_wait(&st->q_full, 0, wctx, 63);
         }
+    } else if (warp == 10 || warp == 11) {
+        regs_dec<kIssueRegs>();  // idle: the rest of the producer / MMA warpgroup
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
+        regs_dec<kIssueRegs>();
         if (n_max > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBlockM, D, 0, 1);
@@ -407,6 +418,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax
+        regs_inc<kSoftmaxRegs>();
         const int t = warp >> 2;  // query tile of this warpgroup
         const int r = tid & 127;
         const int i = (2 * pair + t) * kBlockM + r;
@@ -645,6 +657,15 @@ int launch_fwd_tc_d(const Problem& pr) {
     if (!attr_set) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
             return FA_ERR_CUDA;
+        // the setmaxnreg budgets must fit in the registers the kernel is
+        // actually launched with, or the softmax warps would wait forever
+        cudaFuncAttributes a{};
+        if (cudaFuncGetAttributes(&a, kernel) != cudaSuccess ||
+            a.numRegs * kThreadsPP < 256 * kSoftmaxRegs + 128 * kIssueRegs) {
+            if (std::getenv("FA_DEBUG"))
+                std::fprintf(stderr, "fa: fwd register budget exceeds the launch allocation (%d regs)\n", a.numRegs);
+            return FA_ERR_CUDA;
+        }
         attr_set = true;
     }
     cudaLaunchAttribute pdl[1];
