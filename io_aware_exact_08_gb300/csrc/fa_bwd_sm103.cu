@@ -24,11 +24,11 @@
 //      reduction warps add it into the fp32 accumulator in global memory.
 //      dK_j, dV_j stay in TMEM until the end.
 //   3. convert: dq = dtype(scale * dQacc).
-// Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer, four dQ
-// reduction warps (one per TMEM lane quarter: warps 10-13 at D = 128, 12-15
-// at D = 64, where warps 10-11 idle to complete a warpgroup), so that the
-// compute warps never wait for the dQ product or for the reductions to
-// drain into L2.
+// Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer (all 32
+// lanes run its loop, one elected lane issues), warps 10-11 idle (they
+// complete the third warpgroup), warps 12-15 dQ reduction (one per TMEM lane
+// quarter), so that the compute warps never wait for the dQ product or for
+// the reductions to drain into L2.
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -52,22 +52,19 @@ using namespace sm103;
 constexpr int kTile = 128;          // keys per CTA, queries per step
 constexpr int kComputeThreads = 256;
 
-// register budgets of the D = 64 warpgroups (see BwdCfg)
-constexpr int kComputeRegs = 184, kIssueRegs = 40, kReduceRegs = 96;
-static_assert(256 * kComputeRegs + 128 * kIssueRegs + 128 * kReduceRegs <= 512 * 128,
-              "register budgets above a 512-thread launch at 128 registers");
-
 template <int D>
 struct BwdCfg {
-    // D = 64: 512 threads (four warpgroups: compute, compute, producer + MMA
-    // + two idle warps, dQ reduction) with setmaxnreg budgets of 184 / 40 /
-    // 96 registers (256*184 + 128*40 + 128*96 = 64512 <= 65536), which
-    // removes the compute warps' spills. D = 128: 448 threads at 128
-    // registers, where every budget split measured slower (its instances
-    // spill more).
-    static constexpr bool kRegSplit = (D == 64);
-    static constexpr int kThreads = kRegSplit ? 512 : 448;
-    static constexpr int kReduceWarp0 = kRegSplit ? 12 : 10;
+    // 512 threads in four warpgroups (compute, compute, producer + MMA + two
+    // idle warps, dQ reduction), launched at 128 registers a thread; the
+    // setmaxnreg budgets below move registers to the compute warps. They must
+    // fit in the launch allocation (512 * 128), or .inc would wait forever.
+    static constexpr int kThreads = 512;
+    static constexpr int kReduceWarp0 = 12;
+    static constexpr int kComputeRegs = (D == 64) ? 184 : 168;
+    static constexpr int kIssueRegs = (D == 64) ? 40 : 72;
+    static constexpr int kReduceRegs = 96;
+    static constexpr int kRegBudget = 256 * kComputeRegs + 128 * kIssueRegs + 128 * kReduceRegs;
+    static_assert(kRegBudget <= kThreads * 128, "register budgets above the launch allocation");
     static constexpr int kStages = (D == 128) ? 2 : 3;
     static constexpr int kTileBytes = kTile * D * 2;  // one 128 x D bf16 tile
     static constexpr int kBoxBytes = kTile * 128;     // 128 rows x 64 columns
@@ -88,31 +85,8 @@ struct BwdCfg {
     static constexpr uint32_t kColDQ = (D == 128) ? 128 : 256;
     static constexpr uint32_t kColDV = (D == 128) ? 256 : 320;
     static constexpr uint32_t kColDK = 384;
-    // MMA issue by the whole warp with one elected lane (measured faster at
-    // D = 64) or by lane 0 alone (measured faster at D = 128)
-    static constexpr bool kWarpIssue = (D == 64);
 };
 
-// The MMA issuer's calls in either form (see kWarpIssue).
-template <bool kWarp>
-struct Issue {
-    static __device__ __forceinline__ void ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-        if constexpr (kWarp) mma_ss_warp(d, a, b, id, acc);
-        else mma_ss(d, a, b, id, acc);
-    }
-    static __device__ __forceinline__ void ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
-        if constexpr (kWarp) mma_ts_warp(d, a, b, id, acc);
-        else mma_ts(d, a, b, id, acc);
-    }
-    static __device__ __forceinline__ void commit(uint64_t* bar) {
-        if constexpr (kWarp) mma_commit_warp(bar);
-        else mma_commit(bar);
-    }
-    static __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, const WaitCtx& w, int site) {
-        if constexpr (kWarp) return mbar_wait_warp(bar, parity, w, site);
-        else return mbar_wait(bar, parity, w, site);
-    }
-};
 
 struct BwdParams {
     const float* lse;
@@ -287,7 +261,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
-        if constexpr (Cfg::kRegSplit) regs_dec<kIssueRegs>();
+        regs_dec<Cfg::kIssueRegs>();
         if (lane == 0 && n_active > 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
@@ -322,14 +296,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 if (issued_any[s]) mbar_wait(&st->st_full[s], issued_phase[s], wctx, 102);
             mbar_wait(&st->kv_full, 0, wctx, 103);
         }
-    } else if (Cfg::kRegSplit && (warp == 10 || warp == 11)) {
+    } else if (warp == 10 || warp == 11) {
         // idle: the rest of the producer / MMA warpgroup
-        if constexpr (Cfg::kRegSplit) regs_dec<kIssueRegs>();
+        regs_dec<Cfg::kIssueRegs>();
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if constexpr (Cfg::kRegSplit) regs_dec<kIssueRegs>();
-        if ((Cfg::kWarpIssue || lane == 0) && n_active > 0) {
-            using I = Issue<Cfg::kWarpIssue>;
+        regs_dec<Cfg::kIssueRegs>();
+        // the whole warp runs the issue loop; one elected lane issues
+        if (n_active > 0) {
             constexpr uint32_t id_sh = idesc_bf16_f32(kTile, 64, 0, 0);      // S^T_h, dP^T_h (N = 64)
             constexpr uint32_t id_dv = idesc_bf16_f32(kTile, D, 0, 1);      // dV (A tmem), dK (A K-major)
             constexpr uint32_t id_dqt_h = idesc_bf16_f32(kTile, 64, 1, 1);   // dQ^T_h (A, B MN-major, N = 64)
@@ -342,11 +316,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const uint64_t dsd_mn = smem_desc_sw128(ds_base, kTile * 128, 1024);  // dS^T, MN-major
             const uint64_t kd_mn = smem_desc_sw128(k_base, Cfg::kBoxBytes, 1024);  // K, MN-major (N = d)
             const uint64_t kd_mn2 = smem_desc_sw128(k_base, kTile * 128, 1024);    // K, MN-major (M = d)
-            bool ok = I::wait(&st->kv_full, 0, wctx, 110);
+            bool ok = mbar_wait_warp(&st->kv_full, 0, wctx, 110);
             tc_fence_after();
             for (int it = 0; ok && it < n_active; ++it) {
                 const int s = it % Cfg::kStages;
-                if (!I::wait(&st->st_full[s], (it / Cfg::kStages) & 1, wctx, 111)) break;
+                if (!mbar_wait_warp(&st->st_full[s], (it / Cfg::kStages) & 1, wctx, 111)) break;
                 tc_fence_after();
                 const uint32_t q_base = smem_u32(sStages + s * Cfg::kStageBytes);
                 const uint32_t do_base = q_base + Cfg::kTileBytes;
@@ -363,12 +337,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                        I::ss(tmem + Cfg::kColS + 64 * h, desc_add(kd_k, off), desc_add(qd_k, off + 8192 * h), id_sh,
+                        mma_ss_warp(tmem + Cfg::kColS + 64 * h, desc_add(kd_k, off), desc_add(qd_k, off + 8192 * h), id_sh,
                                kk > 0);
                     }
                     // at D = 128, dP^T_h overwrites the previous tile's dQ^T_h
                     if (D == 128 && it > 0) {
-                        if (!I::wait(&st->dq_free[h], (it - 1) & 1, wctx, 112)) {
+                        if (!mbar_wait_warp(&st->dq_free[h], (it - 1) & 1, wctx, 112)) {
                             ok = false;
                             break;
                         }
@@ -377,15 +351,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-                        I::ss(tmem + Cfg::kColDP + 64 * h, desc_add(vd_k, off), desc_add(dod_k, off + 8192 * h), id_sh,
+                        mma_ss_warp(tmem + Cfg::kColDP + 64 * h, desc_add(vd_k, off), desc_add(dod_k, off + 8192 * h), id_sh,
                                kk > 0);
                     }
-                    I::commit(&st->s_full[h]);
+                    mma_commit_warp(&st->s_full[h]);
                 }
                 if (!ok) break;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    if (!I::wait(&st->p_ready[h], it & 1, wctx, 113)) {
+                    if (!mbar_wait_warp(&st->p_ready[h], it & 1, wctx, 113)) {
                         ok = false;
                         break;
                     }
@@ -393,28 +367,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     // dV += P^T_h dO_h: P^T_h (bf16) in TMEM columns 64h..64h+31
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        I::ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
+                        mma_ts_warp(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
                                desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
                     // dK += dS^T_h Q_h (dS^T half h is shared-memory box h)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        I::ss(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
+                        mma_ss_warp(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
                                desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                    if (h == 1) I::commit(&st->st_empty[s]);
+                    if (h == 1) mma_commit_warp(&st->st_empty[s]);
                     if (Cfg::kDqTransposed) {
                         // dQ^T_h = K_j^T dS^T_h (M = head dim, N = 64 queries):
                         // lane = head-dim index, so one reduction instruction
                         // covers 32 consecutive floats of a dQ row
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            I::ss(tmem + Cfg::kColDQ + 64 * h, desc_add(kd_mn2, kk * 2048),
+                            mma_ss_warp(tmem + Cfg::kColDQ + 64 * h, desc_add(kd_mn2, kk * 2048),
                                    desc_add(dsd_mn, h * (kTile * 128) + kk * 2048), id_dqt_h, kk > 0);
-                        I::commit(&st->dq_full[h]);
+                        mma_commit_warp(&st->dq_full[h]);
                     } else if (h == 1) {
                         // dQ = dS K_j over the whole tile (M = 128 queries, lane = query),
                         // over the previous tile's dQ once it has been read out
                         if (it > 0) {
-                            if (!I::wait(&st->dq_free[0], (it - 1) & 1, wctx, 115)) {
+                            if (!mbar_wait_warp(&st->dq_free[0], (it - 1) & 1, wctx, 115)) {
                                 ok = false;
                                 break;
                             }
@@ -422,19 +396,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         }
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            I::ss(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048), id_dq,
+                            mma_ss_warp(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048), id_dq,
                                    kk > 0);
-                        I::commit(&st->dq_full[0]);
+                        mma_commit_warp(&st->dq_full[0]);
                     }
                 }
             }
-            I::commit(&st->acc_done);
-            I::commit(&st->teardown);
-            I::wait(&st->teardown, 0, wctx, 114);
+            mma_commit_warp(&st->acc_done);
+            mma_commit_warp(&st->teardown);
+            mbar_wait_warp(&st->teardown, 0, wctx, 114);
         }
     } else if (warp >= Cfg::kReduceWarp0) {
         // ------------------------------------------------------------ dQ reduction
-        if constexpr (Cfg::kRegSplit) regs_dec<kReduceRegs>();
+        regs_dec<Cfg::kReduceRegs>();
         // D = 128: dQ^T, lane = head-dim index, so one reduction instruction
         // covers 32 consecutive floats of one query row. D = 64: dQ, lane =
         // query row, 64 consecutive floats in 16-byte reductions.
@@ -487,7 +461,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ compute
-        if constexpr (Cfg::kRegSplit) regs_inc<kComputeRegs>();
+        regs_inc<Cfg::kComputeRegs>();
         const int quarter = warp & 3;      // TMEM lane quarter
         const int half = warp >> 2;        // query columns [64*half, 64*half + 64)
         const int r = quarter * 32 + lane;  // key row within the tile
@@ -784,20 +758,17 @@ int launch_bwd_tc_d(const Problem& pr) {
             cudaFuncSetAttribute(bwd_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::smem(true)) != cudaSuccess)
             return FA_ERR_CUDA;
-        if constexpr (Cfg::kRegSplit) {
-            // setmaxnreg.inc takes registers from what the CTA was launched
-            // with and waits (without bound) until they are free: refuse to
-            // launch unless the budgets fit in that allocation
-            constexpr int need = 256 * kComputeRegs + 128 * kIssueRegs + 128 * kReduceRegs;
-            cudaFuncAttributes a0{}, a1{};
-            if (cudaFuncGetAttributes(&a0, bwd_tc_kernel<D, false>) != cudaSuccess ||
-                cudaFuncGetAttributes(&a1, bwd_tc_kernel<D, true>) != cudaSuccess ||
-                a0.numRegs * Cfg::kThreads < need || a1.numRegs * Cfg::kThreads < need) {
-                if (std::getenv("FA_DEBUG"))
-                    std::fprintf(stderr, "fa: bwd register budget %d exceeds the launch allocation (%d, %d regs)\n",
-                                 need, a0.numRegs, a1.numRegs);
-                return FA_ERR_CUDA;
-            }
+        // setmaxnreg.inc takes registers from what the CTA was launched with
+        // and waits (without bound) until they are free: refuse to launch
+        // unless the budgets fit in that allocation
+        cudaFuncAttributes a0{}, a1{};
+        if (cudaFuncGetAttributes(&a0, bwd_tc_kernel<D, false>) != cudaSuccess ||
+            cudaFuncGetAttributes(&a1, bwd_tc_kernel<D, true>) != cudaSuccess ||
+            a0.numRegs * Cfg::kThreads < Cfg::kRegBudget || a1.numRegs * Cfg::kThreads < Cfg::kRegBudget) {
+            if (std::getenv("FA_DEBUG"))
+                std::fprintf(stderr, "fa: bwd register budget %d exceeds the launch allocation (%d, %d regs)\n",
+                             Cfg::kRegBudget, a0.numRegs, a1.numRegs);
+            return FA_ERR_CUDA;
         }
         attr_set = true;
     }
