@@ -364,42 +364,61 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    // dV += P^T_h dO_h: P^T_h (bf16) in TMEM columns 64h..64h+31
+                    // dV += P^T_h dO_h (P^T_h, bf16, in TMEM columns 64h..64h+31) and
+                    // dK += dS^T_h Q_h (dS^T half h is shared-memory box h),
+                    // at D = 128 interleaved with dQ so that consecutive MMAs
+                    // go to different accumulators:
+                    //   D = 128: dQ^T_h = K_j^T dS^T_h (M = head dim, N = 64
+                    //     queries: lane = head-dim index, so one reduction
+                    //     instruction covers 32 consecutive floats of a row);
+                    //   D = 64, with half 1: dQ = dS K_j over the whole tile
+                    //     (M = 128 queries, lane = query), over the previous
+                    //     tile's dQ once it has been read out.
+                    const uint32_t acc = (it > 0 || h > 0) ? 1u : 0u;
+                    const bool with_dq = Cfg::kDqTransposed || h == 1;
+                    if constexpr (Cfg::kDqTransposed) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ts_warp(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
-                               desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                    // dK += dS^T_h Q_h (dS^T half h is shared-memory box h)
+                        for (int kk = 0; kk < 4; ++kk) {
+                            mma_ts_warp(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
+                                        desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss_warp(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
-                               desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                    if (h == 1) mma_commit_warp(&st->st_empty[s]);
-                    if (Cfg::kDqTransposed) {
-                        // dQ^T_h = K_j^T dS^T_h (M = head dim, N = 64 queries):
-                        // lane = head-dim index, so one reduction instruction
-                        // covers 32 consecutive floats of a dQ row
-#pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ss_warp(tmem + Cfg::kColDQ + 64 * h, desc_add(kd_mn2, kk * 2048),
-                                   desc_add(dsd_mn, h * (kTile * 128) + kk * 2048), id_dqt_h, kk > 0);
-                        mma_commit_warp(&st->dq_full[h]);
-                    } else if (h == 1) {
-                        // dQ = dS K_j over the whole tile (M = 128 queries, lane = query),
-                        // over the previous tile's dQ once it has been read out
-                        if (it > 0) {
-                            if (!mbar_wait_warp(&st->dq_free[0], (it - 1) & 1, wctx, 115)) {
-                                ok = false;
-                                break;
+                            for (int e = 0; e < 2; ++e) {
+                                const int k2 = 2 * kk + e;
+                                mma_ss_warp(tmem + Cfg::kColDQ + 64 * h, desc_add(kd_mn2, k2 * 2048),
+                                            desc_add(dsd_mn, h * (kTile * 128) + k2 * 2048), id_dqt_h, k2 > 0);
+                                if (e == 0)
+                                    mma_ss_warp(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
+                                                desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
                             }
-                            tc_fence_after();
                         }
+                    } else {
+                        // (at D = 64 the products go one after the other, which
+                        // measured faster there)
 #pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ss_warp(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048), id_dq,
-                                   kk > 0);
-                        mma_commit_warp(&st->dq_full[0]);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ts_warp(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
+                                        desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss_warp(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
+                                        desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
+                        if (h == 1) mma_commit_warp(&st->st_empty[s]);  // Q_i, dO_i read
+                        if (with_dq) {
+                            if (it > 0) {
+                                if (!mbar_wait_warp(&st->dq_free[0], (it - 1) & 1, wctx, 115)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                            }
+#pragma unroll
+                            for (int kk = 0; kk < kTile / 16; ++kk)
+                                mma_ss_warp(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048),
+                                            id_dq, kk > 0);
+                        }
                     }
+                    if (Cfg::kDqTransposed && h == 1) mma_commit_warp(&st->st_empty[s]);
+                    if (with_dq) mma_commit_warp(&st->dq_full[Cfg::kDqTransposed ? h : 0]);
                 }
             }
             mma_commit_warp(&st->acc_done);
