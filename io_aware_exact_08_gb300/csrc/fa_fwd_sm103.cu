@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             // key 32c + x), drawn before S arrives
             uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
             if (p.dropout) {
-#pragma unroll 1
+#pragma unroll 8
                 for (int g = 0; g < 32; ++g) {
                     const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, i, ktile * (kBlockN / 4) + g);
                     if (g == 0) keep[0] = keep[1] = keep[2] = keep[3] = 0;

@@ -1,0 +1,34 @@
+"""Host-side helpers of bench.py: the FLOP/byte models and the recorded DRAM
+traffic, which is reported only for the kernel sources it was measured on."""
+import json
+
+import bench
+from workloads import WORKLOADS
+
+
+def test_flop_model_matches_formula():
+    w = WORKLOADS["long_causal"]
+    fwd, bwd = bench.flops(w)
+    assert fwd == 4 * w.B * w.H * w.N * w.N * w.d / 2
+    assert bwd == 2.5 * fwd
+
+
+def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
+    rec = {"source_sha256": bench.kernel_source_hash(),
+           "calls": {"gpt2_causal": {"fa_bwd": {"dram_bytes": 1234}}}}
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "dram_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # the hash is taken from the package sources under ROOT: point it back
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["source_sha256"])
+    assert bench.recorded_traffic("gpt2_causal", "fa_bwd") == 1234
+    assert bench.recorded_traffic("gpt2_causal", "fa_fwd") is None
+    assert bench.recorded_traffic("long_causal", "fa_bwd") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 64)
+    assert bench.recorded_traffic("gpt2_causal", "fa_bwd") is None
+
+
+def test_source_hash_tracks_kernel_files():
+    h1 = bench.kernel_source_hash()
+    assert len(h1) == 64 and h1 == bench.kernel_source_hash()
