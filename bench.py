@@ -259,9 +259,19 @@ def run_fa(args, w, ws, rank, device):
     ptr = lambda t: None if t is None else t.data_ptr()
     scale, causal, p, seed = w.softmax_scale, int(w.causal), float(w.dropout_p), int(inp["seed"])
 
+    splits = max(1, int(getattr(args, "splits", 1)))
+    kv_ws = None
+    if splits > 1:
+        kv_wsb = fa.fa_fwd_splitkv_workspace_size(B, H, N, d, splits)
+        kv_ws = torch.empty(kv_wsb, dtype=torch.uint8, device=device)
+
     def fwd():
-        rc = fa.fa_fwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, N, d, scale, causal, ptr(bm), p, seed,
-                       dtype, ptr(kl), sh)
+        if kv_ws is not None:
+            rc = fa.fa_fwd_splitkv(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, N, d, scale, causal, ptr(bm), p,
+                                   seed, dtype, ptr(kl), splits, kv_ws.data_ptr(), kv_ws.numel(), sh)
+        else:
+            rc = fa.fa_fwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, N, d, scale, causal, ptr(bm), p, seed,
+                           dtype, ptr(kl), sh)
         assert rc == 0, fa.fa_status_string(rc)
 
     def bwd():
@@ -361,7 +371,8 @@ def run_fa(args, w, ws, rank, device):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
                    "dropout_p": w.dropout_p, "kv_len_range": w.kv_len_range, "block_density": round(dens, 5),
-                   "scale": scale, "step": "fa_fwd + fa_bwd", "l2": "flushed before every timed step",
+                   "scale": scale, "step": "fa_fwd + fa_bwd" if splits == 1 else f"fa_fwd_splitkv ({splits} splits) + fa_bwd",
+                   "l2": "flushed before every timed step",
                    "parallelism": f"replicas x{ws}"},
         "fwd_tflops": round(fwd_tflops, 3), "bwd_tflops": round(bwd_tflops, 3),
         "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
@@ -416,13 +427,16 @@ def main(argv=None):
     ap.add_argument("--impl", default="fa", choices=["fa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--splits", type=int, default=1,
+                    help="forward through fa_fwd_splitkv with this many key-tile ranges per query-tile pair")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    from workloads import WORKLOADS, sweep_workloads
+    from workloads import WORKLOADS, splitkv_workloads, sweep_workloads
     table = dict(WORKLOADS)
     table.update({w.name: w for w in sweep_workloads()})
+    table.update({w.name: w for w in splitkv_workloads()})
     w = table[args.workload]
     ws, rank, local = dist_env()
 

@@ -114,6 +114,34 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    fa_dtype dtype, const int32_t* kv_len, void* stream);
 
 /*
+ * Split-KV forward: the same result as fa_fwd (O and LSE up to rounding),
+ * computed with the key tiles of every pair of 128-row query tiles cut into
+ * n_splits ranges, one CTA each, for problems whose B*H*ceil(N/256) work items
+ * would not fill the GPU (sequence parallelism across the key dimension,
+ * "Flash Attention" guide, section "Flash Attention 2 / Paralelisme sepanjang
+ * panjang sekuens"). Each CTA writes its range's O (normalised over the range)
+ * and LSE to the workspace; a second kernel merges them with the
+ * incremental-softmax combination of the paper summary (section "Pelacakan
+ * Softmax Inkremental"): M = max_s LSE_s, w_s = e^{LSE_s - M},
+ * O = sum_s w_s O_s / sum_s w_s, LSE = M + log sum_s w_s.
+ *   n_splits   1 .. 64 (1 runs fa_fwd); arguments otherwise as fa_fwd.
+ *   workspace  caller-owned device memory, >= fa_fwd_splitkv_workspace_size
+ *              bytes, 256-byte aligned; contents undefined on return.
+ * Returns as fa_fwd, plus FA_ERR_INVALID_ARG for n_splits outside 1..64 and
+ * FA_ERR_WORKSPACE for a missing, small or misaligned workspace. With the
+ * CUDA-core kernels (fp32, or fa_set_kernel_path(1)) it runs fa_fwd.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, float scale, int causal,
+                   const uint8_t* block_mask, float dropout_p, uint64_t seed,
+                   fa_dtype dtype, const int32_t* kv_len, int n_splits,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of split-KV workspace: n_splits * B*H*N*(d + 1) floats (partial O,
+ * then partial LSE), each part rounded up to 256 bytes; 0 for invalid sizes. */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int n_splits);
+
+/*
  * Bytes of backward workspace: rowsum(dO o O) (fp32 [B,H,N]) plus the fp32
  * dQ accumulator ([B,H,N,d]), each rounded up to 256 bytes. O(B*H*N*d): the
  * backward keeps no N x N state. Returns 0 for invalid sizes.

@@ -36,7 +36,7 @@ _lock = threading.Lock()
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
             "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
-            "fa_bwd_noalloc", "fa_test_wait_timeout")
+            "fa_bwd_noalloc", "fa_test_wait_timeout", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size")
 
 # Size of the fixed device array fa_bwd_noalloc takes its workspace from.
 FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -67,6 +67,10 @@ def load_library(build_if_missing: bool = True):
         P, I, F, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
         lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, P]
         lib.fa_fwd.restype = I
+        lib.fa_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, I, P, SZ, P]
+        lib.fa_fwd_splitkv.restype = I
+        lib.fa_fwd_splitkv_workspace_size.argtypes = [I, I, I, I, I]
+        lib.fa_fwd_splitkv_workspace_size.restype = SZ
         lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, P, SZ, P]
         lib.fa_bwd.restype = I
         lib.fa_bwd_workspace_size.argtypes = [I, I, I, I]
@@ -96,6 +100,17 @@ def load_library(build_if_missing: bool = True):
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, block_mask, dropout_p, seed, dtype, kv_len, stream):
     return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, int(causal), block_mask, dropout_p,
                                  seed & 0xFFFFFFFFFFFFFFFF, dtype, kv_len, stream)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, block_mask, dropout_p, seed, dtype, kv_len,
+                   n_splits, workspace, workspace_bytes, stream):
+    return load_library().fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, int(causal), block_mask, dropout_p,
+                                         seed & 0xFFFFFFFFFFFFFFFF, dtype, kv_len, n_splits, workspace,
+                                         workspace_bytes, stream)
+
+
+def fa_fwd_splitkv_workspace_size(B, H, N, d, n_splits):
+    return load_library().fa_fwd_splitkv_workspace_size(B, H, N, d, n_splits)
 
 
 def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, block_mask, dropout_p, seed, dtype,
@@ -187,8 +202,11 @@ def _stream(stream):
 
 
 def attention_fwd(q, k, v, scale=None, causal=False, block_mask=None, dropout_p=0.0, seed=0, kv_len=None,
-                  out=None, lse=None, stream=None):
-    """O, LSE = attention(q, k, v) for [B,H,N,d] CUDA tensors (bf16 or fp32)."""
+                  out=None, lse=None, stream=None, num_splits=1):
+    """O, LSE = attention(q, k, v) for [B,H,N,d] CUDA tensors (bf16 or fp32).
+
+    num_splits > 1 runs the split-KV forward (fa_fwd_splitkv) with a
+    workspace allocated here."""
     torch = _torch()
     _check(q, "q")
     _check(k, "k", q)
@@ -197,6 +215,17 @@ def attention_fwd(q, k, v, scale=None, causal=False, block_mask=None, dropout_p=
     scale = (1.0 / d ** 0.5) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if num_splits > 1:
+        wsb = fa_fwd_splitkv_workspace_size(B, H, N, d, int(num_splits))
+        if wsb == 0 and N > 0:
+            raise FaError(-1, "fa_fwd_splitkv_workspace_size")
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=q.device)
+        rc = fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, scale, causal,
+                            _ptr(block_mask), float(dropout_p), int(seed), _dtype_code(q), _ptr(kv_len),
+                            int(num_splits), ws.data_ptr(), wsb, _stream(stream))
+        if rc != 0:
+            raise FaError(rc, "fa_fwd_splitkv")
+        return o, l
     rc = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, scale, causal, _ptr(block_mask),
                 float(dropout_p), int(seed), _dtype_code(q), _ptr(kv_len), _stream(stream))
     if rc != 0:

@@ -121,6 +121,46 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return from_cuda(launch_fwd_simt(p));
 }
 
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int n_splits) {
+    if (B < 1 || H < 1 || N < 0 || (d != 64 && d != 128) || n_splits < 1 || n_splits > kMaxSplits) return 0;
+    const size_t rows = (size_t)B * H * N;
+    return round256((size_t)n_splits * rows * d * sizeof(float)) + round256((size_t)n_splits * rows * sizeof(float));
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   float scale, int causal, const uint8_t* block_mask, float dropout_p, uint64_t seed, fa_dtype dtype,
+                   const int32_t* kv_len, int n_splits, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_common(B, H, N, d, scale, dropout_p, dtype);
+    if (rc != FA_OK) return rc;
+    if (n_splits < 1 || n_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+    if (N == 0) return FA_OK;
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+        return FA_ERR_INVALID_ARG;
+    const size_t need = fa_fwd_splitkv_workspace_size(B, H, N, d, n_splits);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return FA_ERR_WORKSPACE;
+    Problem p{};
+    fill_common(p, B, H, N, d, scale, causal, block_mask, dropout_p, seed, dtype, kv_len, stream);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    rc = status_address(&p.status);
+    if (rc != FA_OK) return rc;
+    // one split, the CUDA-core kernels or a non-positive scale: the plain
+    // forward computes the same result
+    if (n_splits == 1 || !use_tensor_cores(p) || !(scale > 0.f)) {
+        if (use_tensor_cores(p)) return launch_fwd_tc(p);
+        return from_cuda(launch_fwd_simt(p));
+    }
+    const size_t rows = (size_t)B * H * N;
+    p.n_splits = n_splits;
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256((size_t)n_splits * rows * d * sizeof(float)));
+    return launch_fwd_tc(p);
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 0 || (d != 64 && d != 128)) return 0;
     const size_t rows = (size_t)B * H * N;

@@ -45,6 +45,14 @@ struct FwdParams {
     const int32_t* kv_len;
     int* status;
     int H, N, nb, n_qtiles;
+    // split-KV: the key tiles of each pair of query tiles are cut into
+    // n_splits ranges, one CTA each, which write the partial O (fp32,
+    // normalised over their range) and LSE to o_part / lse_part
+    // ([n_splits][B*H][N][D] and [n_splits][B*H][N]); 1 and null otherwise
+    int n_splits;
+    float* o_part;
+    float* lse_part;
+    int BH;
     float scale_log2;
     float out_scale;  // 1/(1-p)
     uint32_t drop_thr;
@@ -101,7 +109,7 @@ struct SharedPP {
     int n_list[2];  // kSplit: visible key tiles of each query tile
 };
 
-template <int D, bool kSplit>
+template <int D, bool kSplit, bool kPartial>
 __global__ void __launch_bounds__(kThreadsPP, 1)
     fwd_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -119,12 +127,15 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     pdl_wait();
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // grid (B*H, pairs): the hardware dispatches x fastest, so every head's
-    // heaviest pair (causal) goes out before any lighter one
+    // grid (B*H, pairs x splits): the hardware dispatches x fastest, so every
+    // head's heaviest pair (causal) goes out before any lighter one
     const int bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H;
     const int n_pairs = (p.n_qtiles + 1) / 2;
-    const int pair = p.causal ? (n_pairs - 1 - (int)blockIdx.y) : (int)blockIdx.y;
+    // kPartial (split-KV): blockIdx.y = rank * n_splits + split
+    const int rank = kPartial ? (int)blockIdx.y / p.n_splits : (int)blockIdx.y;
+    const int split = kPartial ? (int)blockIdx.y % p.n_splits : 0;
+    const int pair = p.causal ? (n_pairs - 1 - rank) : rank;
     const int L = p.kv_len ? min(max(p.kv_len[b], 0), p.N) : p.N;
     const int nkt = (L + kBlockN - 1) / kBlockN;  // key tiles with a visible key
     // key tiles visited by query tile t of this CTA (0 if the tile is past N)
@@ -133,6 +144,16 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
     for (int t = 0; t < 2; ++t) {
         const int qt = 2 * pair + t;
         n_t[t] = (qt < p.n_qtiles) ? (p.causal ? min(nkt, qt + 1) : nkt) : 0;
+    }
+    // this CTA's range [kb, ke) of the pair's key tiles (all of them unless
+    // split-KV); tile t visits key tiles kb .. kb + n_t - 1
+    int kb = 0, ke = 1 << 30;
+    if constexpr (kPartial) {
+        const int chunk = (max(n_t[0], n_t[1]) + p.n_splits - 1) / p.n_splits;
+        kb = split * chunk;
+        ke = kb + chunk;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) n_t[t] = max(0, min(n_t[t], ke) - kb);
     }
     WaitCtx wctx{&st->abort_flag, p.status};
     // kSplit (block mask): each query tile walks its own list of visible key
@@ -145,11 +166,12 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             const int qt = 2 * pair + t;
             int e = (qt < p.n_qtiles) ? nkt : 0;
             if (p.causal) e = min(e, qt + 1);
+            e = min(e, ke);
             const uint8_t* row = p.block_mask + (size_t)qt * p.nb;
             int cnt = 0;
-            for (int c = 0; c < e; c += 32) {
+            for (int c = kb & ~31; c < e; c += 32) {
                 const int j = c + lane;
-                const bool act = j < e && row[j] != 0;
+                const bool act = j >= kb && j < e && row[j] != 0;
                 const uint32_t bal = __ballot_sync(0xffffffffu, act);
                 if (act) sList[t * kMaskListCap + cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)j;
                 cnt += __popc(bal);
@@ -215,7 +237,8 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                     const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
 #pragma unroll
                     for (int x = 0; x < Cfg::kBoxes; ++x)
-                        tma_load_3d(dst + x * Cfg::kBoxBytes, map, &st->kv_full[s], x * 64, (t >> 1) * kBlockN, bh);
+                        tma_load_3d(dst + x * Cfg::kBoxBytes, map, &st->kv_full[s], x * 64, (kb + (t >> 1)) * kBlockN,
+                                    bh);
                 }
             } else {
                 // K of S_0(0), K of S_1(0), then per step u and tile t: V of
@@ -432,7 +455,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         // key tile of step u: u itself, or the u-th entry of this tile's list
         const uint16_t* my_list = t ? list1 : list0;
         for (int u = 0; u < n; ++u) {
-            const int ktile = kSplit ? (int)my_list[u] : u;
+            const int ktile = kSplit ? (int)my_list[u] : kb + u;
             // dropout keep bits of this row's 128 keys (bit x of keep[c] is
             // key 32c + x), drawn before S arrives
             uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
@@ -551,6 +574,8 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             mbar_arrive_warp(&st->p_full[t]);
         }
         __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N) * D;
+        // split-KV partials of this split and head
+        const size_t prow = ((size_t)split * p.BH + bh) * p.N;
         if (ok && n > 0) {
             if (mbar_wait_warp(&st->o_final[t], 0, wctx, 81)) {
                 tc_fence_after();
@@ -561,7 +586,14 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                     tmem_ld32(obase + c * 32, orr);
                     tmem_ld_wait();
                     reg_fence(orr);
-                    if (i < p.N) {
+                    if (kPartial && i < p.N) {
+                        float4* dst = reinterpret_cast<float4*>(p.o_part + (prow + i) * D + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(__uint_as_float(orr[4 * v]) * inv, __uint_as_float(orr[4 * v + 1]) * inv,
+                                                 __uint_as_float(orr[4 * v + 2]) * inv,
+                                                 __uint_as_float(orr[4 * v + 3]) * inv);
+                    } else if (i < p.N) {
                         uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D + c * 32);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
@@ -574,14 +606,25 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                         }
                     }
                 }
-                if (i < p.N) p.lse[(size_t)bh * p.N + i] = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+                if (i < p.N) {
+                    const float lse_i = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+                    if (kPartial) p.lse_part[prow + i] = lse_i;
+                    else p.lse[(size_t)bh * p.N + i] = lse_i;
+                }
             }
         } else if (n == 0 && i < p.N) {
-            uint4 z = make_uint4(0, 0, 0, 0);
-            uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D);
+            if (kPartial) {
+                float4* dst = reinterpret_cast<float4*>(p.o_part + (prow + i) * D);
 #pragma unroll
-            for (int v = 0; v < D / 8; ++v) dst[v] = z;
-            p.lse[(size_t)bh * p.N + i] = -INFINITY;
+                for (int v = 0; v < D / 4; ++v) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                p.lse_part[prow + i] = -INFINITY;
+            } else {
+                uint4 z = make_uint4(0, 0, 0, 0);
+                uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D);
+#pragma unroll
+                for (int v = 0; v < D / 8; ++v) dst[v] = z;
+                p.lse[(size_t)bh * p.N + i] = -INFINITY;
+            }
         }
     }
 
@@ -628,7 +671,47 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int BH, int N, int d, in
     return r == CUDA_SUCCESS;
 }
 
-template <int D, bool kSplit>
+// Merges the n_splits partial results of split-KV: with w_s = e^{LSE_s - M},
+// O = sum_s w_s O_s / sum_s w_s and LSE = M + log sum_s w_s (M = max_s LSE_s),
+// the combination of softmax partials over disjoint key blocks of the
+// "FlashAttention" blog post (section "Tiling") and of the paper summary's
+// incremental softmax (section "Pelacakan Softmax Inkremental"). One warp per
+// row; rows without a visible key (every LSE_s = -inf) get O = 0, LSE = -inf.
+template <int D>
+__global__ void __launch_bounds__(256) splitkv_merge_kernel(const float* __restrict__ o_part,
+                                                            const float* __restrict__ lse_part,
+                                                            __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                                            int n_splits, size_t rows) {
+    pdl_wait();  // the partials come from the forward kernel
+    const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    constexpr int PER = D / 32;  // 2 or 4 floats per lane
+    float mx = -INFINITY;
+    for (int s = 0; s < n_splits; ++s) mx = fmaxf(mx, lse_part[(size_t)s * rows + row]);
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+        for (int s = 0; s < n_splits; ++s) {
+            const float ls = lse_part[(size_t)s * rows + row];
+            const float w = (ls == -INFINITY) ? 0.f : expf(ls - mx);
+            wsum += w;
+            const float* src = o_part + ((size_t)s * rows + row) * D + lane * PER;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+        }
+    }
+    const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
+    __nv_bfloat16* dst = o + row * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2)
+        *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    if (lane == 0) lse[row] = (wsum > 0.f) ? mx + logf(wsum) : -INFINITY;
+}
+
+template <int D, bool kSplit, bool kPartial>
 int launch_fwd_tc_d(const Problem& pr) {
     constexpr int kSmem = FwdPPCfg<D>::kSmem;
     CUtensorMap tq, tk, tv;
@@ -646,13 +729,17 @@ int launch_fwd_tc_d(const Problem& pr) {
     p.N = pr.N;
     p.nb = pr.nb;
     p.n_qtiles = (pr.N + kBlockM - 1) / kBlockM;
+    p.BH = BH;
+    p.n_splits = pr.o_part ? pr.n_splits : 1;
+    p.o_part = pr.o_part;
+    p.lse_part = pr.lse_part;
     p.scale_log2 = pr.scale * kLog2e;
     p.out_scale = 1.0f / (1.0f - pr.dropout_p);
     p.drop_thr = pr.drop_threshold;
     p.dropout = pr.dropout_p > 0.f;
     p.causal = pr.causal;
     p.seed = pr.seed;
-    auto kernel = fwd_pp_kernel<D, kSplit>;
+    auto kernel = fwd_pp_kernel<D, kSplit, kPartial>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
@@ -672,7 +759,9 @@ int launch_fwd_tc_d(const Problem& pr) {
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(BH, (p.n_qtiles + 1) / 2);
+    const long long grid_y = (long long)((p.n_qtiles + 1) / 2) * p.n_splits;
+    if (grid_y > 65535) return FA_ERR_UNSUPPORTED;
+    cfg.gridDim = dim3(BH, (unsigned)grid_y);
     cfg.blockDim = dim3(kThreadsPP);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = pr.stream;
@@ -684,6 +773,17 @@ int launch_fwd_tc_d(const Problem& pr) {
         if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: fwd_tc launch: %s\n", cudaGetErrorString(e));
         return FA_ERR_CUDA;
     }
+    if (p.o_part) {
+        // split-KV: merge the partial results into O and LSE
+        const size_t rows = (size_t)BH * pr.N;
+        cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, splitkv_merge_kernel<D>, (const float*)p.o_part, (const float*)p.lse_part,
+                               static_cast<__nv_bfloat16*>(pr.o), pr.lse, p.n_splits, rows);
+        note_launches(1);
+        if (e != cudaSuccess) return FA_ERR_CUDA;
+    }
     return FA_OK;
 }
 
@@ -691,8 +791,12 @@ int launch_fwd_tc(const Problem& p) {
     if (!(p.scale > 0.f)) return launch_fwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
     // without a block mask both tiles' key lists are prefixes of one list and
     // share its K/V loads; with one, each tile has its own list (kSplit)
-    if (p.block_mask) return p.d == 64 ? launch_fwd_tc_d<64, true>(p) : launch_fwd_tc_d<128, true>(p);
-    return p.d == 64 ? launch_fwd_tc_d<64, false>(p) : launch_fwd_tc_d<128, false>(p);
+    if (p.o_part) {  // split-KV
+        if (p.block_mask) return p.d == 64 ? launch_fwd_tc_d<64, true, true>(p) : launch_fwd_tc_d<128, true, true>(p);
+        return p.d == 64 ? launch_fwd_tc_d<64, false, true>(p) : launch_fwd_tc_d<128, false, true>(p);
+    }
+    if (p.block_mask) return p.d == 64 ? launch_fwd_tc_d<64, true, false>(p) : launch_fwd_tc_d<128, true, false>(p);
+    return p.d == 64 ? launch_fwd_tc_d<64, false, false>(p) : launch_fwd_tc_d<128, false, false>(p);
 }
 
 }  // namespace fa

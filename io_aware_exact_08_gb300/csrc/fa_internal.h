@@ -36,7 +36,14 @@ struct Problem {
     float* dq_acc;              // workspace: fp32 [B,H,N,d]
     int* status;                // device status word (timeouts)
     cudaStream_t stream;
+    // split-KV forward: n_splits key-tile ranges per pair of query tiles,
+    // partial O / LSE in the caller's workspace, merged after (1 = off)
+    int n_splits = 1;
+    float* o_part = nullptr;    // [n_splits][B*H][N][d] fp32
+    float* lse_part = nullptr;  // [n_splits][B*H][N] fp32
 };
+
+constexpr int kMaxSplits = 64;
 
 constexpr int kMaskBlock = 128;
 // With a block mask the tensor-core kernels keep each CTA's list of visible

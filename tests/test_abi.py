@@ -97,3 +97,26 @@ def test_status_strings():
 def test_kernel_path_switch_roundtrips():
     old = fa.fa_set_kernel_path(1)
     assert fa.fa_set_kernel_path(old) == 1
+
+
+def test_splitkv_workspace_size():
+    # n_splits partial O (fp32, d per row) then partial LSE, each rounded to 256 bytes
+    r256 = lambda x: (x + 255) // 256 * 256
+    for B, H, N, d, s in [(1, 4, 16384, 128, 4), (2, 3, 300, 64, 3), (1, 1, 1, 64, 1)]:
+        rows = B * H * N
+        assert fa.fa_fwd_splitkv_workspace_size(B, H, N, d, s) == r256(4 * s * rows * d) + r256(4 * s * rows)
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 128, 64, 0) == 0
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 128, 64, 65) == 0
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 128, 96, 2) == 0
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(n_splits=0), -1), (dict(n_splits=65), -1), (dict(workspace=None), -4), (dict(workspace_bytes=16), -4),
+    (dict(workspace=FAKE + 16), -4), (dict(d=96), -2), (dict(o=None), -1),
+])
+def test_splitkv_argument_errors(kw, expect):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=16, d=64, scale=0.125, causal=0,
+                block_mask=None, dropout_p=0.0, seed=0, dtype=fa.FA_BF16, kv_len=None, n_splits=2,
+                workspace=FAKE, workspace_bytes=1 << 20, stream=None)
+    args.update(kw)
+    assert fa.fa_fwd_splitkv(**args) == expect

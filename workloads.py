@@ -92,6 +92,15 @@ def sweep_workloads():
     return out
 
 
+def splitkv_workloads():
+    """Long sequences with few heads, where the two-tile forward grid
+    (B*H*ceil(N/256) CTAs) would not fill the GPU: the case split-KV serves."""
+    return [Workload("longctx_b1h4", 20, B=1, H=4, N=16384, d=128, dtype="bf16", causal=True,
+                     note="few heads, long context"),
+            Workload("longctx_b1h2_d64", 21, B=1, H=2, N=8192, d=64, dtype="bf16", causal=False,
+                     note="few heads, long context")]
+
+
 def band_butterfly_block_mask(nb: int, band: int = 2) -> torch.Tensor:
     """Block mask M[i][j] (uint8, nb x nb): |i-j| <= band, or j == i XOR 2^k.
 
