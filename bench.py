@@ -360,7 +360,8 @@ def run_fa(args, w, ws, rank, device):
                 "frac": round(hbm_frac, 4)}
     else:
         roof = {"bound": "alu", "achieved": round(tensor_ach, 3), "peak": None, "unit": "TFLOP/s", "frac": None}
-    roof.update({"kernel": dominant, "traffic": recorded_traffic(w.name, dominant),
+    roof.update({"kernel": dominant,
+                 "traffic": recorded_traffic(w.name if splits == 1 else f"{w.name}/splits={splits}", dominant),
                  "peak_source": peaks["source"] + " (burst)",
                  "tensor_frac": round(tensor_frac, 4), "hbm_frac": round(hbm_frac, 4),
                  "algorithmic_flops": dom_f, "algorithmic_bytes": dom_b, "avg_ms": round(dom_ms, 4)})
