@@ -56,7 +56,7 @@ def flops(w, density=1.0):
 def algorithmic_bytes(w):
     """Forward: read Q, K, V, write O (elements) + write LSE (fp32).
     Backward: read Q, K, V, O, dO, LSE; write dQ, dK, dV."""
-    e = 2 if w.dtype == "bf16" else 4
+    e = 2 if w.dtype in ("bf16", "fp16") else 4
     bhnd = w.B * w.H * w.N * w.d
     bhn = w.B * w.H * w.N
     return 4 * bhnd * e + 4 * bhn, 8 * bhnd * e + 8 * bhn
@@ -88,6 +88,18 @@ def recorded_traffic(workload, call):
     if not ent or rec.get("source_sha256") != kernel_source_hash():
         return None
     return int(ent["dram_bytes"])
+
+
+def traffic_key(w, splits=1):
+    """Key of a (workload, dtype, split count) in the DRAM traffic record."""
+    from workloads import WORKLOADS, splitkv_workloads, sweep_workloads
+    base = {x.name: x for x in list(WORKLOADS.values()) + sweep_workloads() + splitkv_workloads()}.get(w.name)
+    key = w.name
+    if base is not None and base.dtype != w.dtype:
+        key += f"/{w.dtype}"
+    if splits > 1:
+        key += f"/splits={splits}"
+    return key
 
 
 def load_peaks():
@@ -247,7 +259,7 @@ def run_fa(args, w, ws, rank, device):
     q, k, v, do = (dev(inp[n]) for n in ("q", "k", "v", "do"))
     bm, kl = dev(inp["block_mask"]), dev(inp["kv_len"])
     B, H, N, d = w.B, w.H, w.N, w.d
-    dtype = fa.FA_BF16 if w.dtype == "bf16" else fa.FA_FP32
+    dtype = {"bf16": fa.FA_BF16, "fp16": fa.FA_FP16, "fp32": fa.FA_FP32}[w.dtype]
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
@@ -350,19 +362,22 @@ def run_fa(args, w, ws, rank, device):
     dom_b = bwd_b if dominant == "fa_bwd" else fwd_b
     tensor_ach = dom_f / (dom_ms * 1e-3) / 1e12
     hbm_ach = dom_b / (dom_ms * 1e-3) / 1e9
+    # fp16 and bf16 share the dense tensor rate (2.25 PFLOP/s nominal each), so
+    # an fp16 contraction takes the measured bf16 peak times 1
+    sixteen = w.dtype in ("bf16", "fp16")
     tensor_frac = tensor_ach / peaks["bf16"]
     hbm_frac = hbm_ach / peaks["hbm"]
-    if w.dtype == "bf16" and tensor_frac >= hbm_frac:
+    if sixteen and tensor_frac >= hbm_frac:
         roof = {"bound": "tensor", "achieved": round(tensor_ach, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
                 "frac": round(tensor_frac, 4)}
-    elif w.dtype == "bf16":
+    elif sixteen:
         roof = {"bound": "hbm", "achieved": round(hbm_ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": round(hbm_frac, 4)}
     else:
         roof = {"bound": "alu", "achieved": round(tensor_ach, 3), "peak": None, "unit": "TFLOP/s", "frac": None}
     roof.update({"kernel": dominant,
-                 "traffic": recorded_traffic(w.name if splits == 1 else f"{w.name}/splits={splits}", dominant),
-                 "peak_source": peaks["source"] + " (burst)",
+                 "traffic": recorded_traffic(traffic_key(w, splits), dominant),
+                 "peak_source": peaks["source"] + " (burst)" + (", bf16 peak x 1 for fp16" if w.dtype == "fp16" else ""),
                  "tensor_frac": round(tensor_frac, 4), "hbm_frac": round(hbm_frac, 4),
                  "algorithmic_flops": dom_f, "algorithmic_bytes": dom_b, "avg_ms": round(dom_ms, 4)})
 
@@ -377,8 +392,8 @@ def run_fa(args, w, ws, rank, device):
                    "parallelism": f"replicas x{ws}"},
         "fwd_tflops": round(fwd_tflops, 3), "bwd_tflops": round(bwd_tflops, 3),
         "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
-        "frac_of_bf16_peak": round(value / ws / peaks["bf16"], 4) if w.dtype == "bf16" else None,
-        "fwd_frac_of_bf16_peak": round(fwd_tflops / ws / peaks["bf16"], 4) if w.dtype == "bf16" else None,
+        "frac_of_bf16_peak": round(value / ws / peaks["bf16"], 4) if sixteen else None,
+        "fwd_frac_of_bf16_peak": round(fwd_tflops / ws / peaks["bf16"], 4) if sixteen else None,
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
@@ -428,6 +443,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="fa", choices=["fa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
+                    help="run a 16-bit workload with this input type instead of its own")
     ap.add_argument("--splits", type=int, default=1,
                     help="forward through fa_fwd_splitkv with this many key-tile ranges per query-tile pair")
     args = ap.parse_args(argv)
@@ -439,6 +456,10 @@ def main(argv=None):
     table.update({w.name: w for w in sweep_workloads()})
     table.update({w.name: w for w in splitkv_workloads()})
     w = table[args.workload]
+    if args.dtype is not None:
+        if w.dtype not in ("bf16", "fp16"):
+            ap.error("--dtype applies to the 16-bit workloads only")
+        w = w.with_(dtype=args.dtype)
     ws, rank, local = dist_env()
 
     if args.impl == "reference":

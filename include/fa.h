@@ -50,7 +50,10 @@
 extern "C" {
 #endif
 
-typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
+/* Element type of q, k, v, o, dO, dq, dk, dv. The 16-bit types run on the
+ * tcgen05 tensor-core kernels (fp32 accumulation); fp32 runs on fp32
+ * CUDA-core kernels. */
+typedef enum { FA_BF16 = 0, FA_FP32 = 1, FA_FP16 = 2 } fa_dtype;
 
 typedef enum {
     FA_OK = 0,
@@ -65,8 +68,8 @@ typedef enum {
  * Forward: o = softmax(scale * q k^T + mask) v with optional dropout, and
  * lse[b,h,i] = log-sum-exp of row i's (masked, scaled) scores.
  * Inputs q, k, v; outputs o (dtype) and lse (fp32). All device pointers,
- * owned by the caller. bf16 runs on the tcgen05 tensor-core kernel; fp32 on
- * an fp32 CUDA-core kernel.
+ * owned by the caller. bf16 and fp16 run on the tcgen05 tensor-core kernel;
+ * fp32 on an fp32 CUDA-core kernel.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal,
@@ -165,7 +168,7 @@ int fa_check_device_status(void* stream, int* site);
 const char* fa_status_string(int status);
 
 /*
- * Diagnostic: 0 = default kernels (tcgen05 for bf16), 1 = force the
+ * Diagnostic: 0 = default kernels (tcgen05 for bf16 and fp16), 1 = force the
  * CUDA-core kernels for every dtype. Process-wide; returns the old value.
  */
 int fa_set_kernel_path(int path);

@@ -28,6 +28,7 @@ __all__ = [
 
 FA_BF16 = 0
 FA_FP32 = 1
+FA_FP16 = 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libfa_gb300.so")
@@ -178,7 +179,9 @@ def _dtype_code(t):
         return FA_BF16
     if t.dtype == torch.float32:
         return FA_FP32
-    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+    if t.dtype == torch.float16:
+        return FA_FP16
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16, float16 or float32")
 
 
 def _ptr(t):
@@ -203,7 +206,7 @@ def _stream(stream):
 
 def attention_fwd(q, k, v, scale=None, causal=False, block_mask=None, dropout_p=0.0, seed=0, kv_len=None,
                   out=None, lse=None, stream=None, num_splits=1):
-    """O, LSE = attention(q, k, v) for [B,H,N,d] CUDA tensors (bf16 or fp32).
+    """O, LSE = attention(q, k, v) for [B,H,N,d] CUDA tensors (bf16, fp16 or fp32).
 
     num_splits > 1 runs the split-KV forward (fa_fwd_splitkv) with a
     workspace allocated here."""

@@ -34,7 +34,7 @@ int check_common(int B, int H, int N, int d, float scale, float dropout_p, fa_dt
     if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (!(dropout_p >= 0.f && dropout_p < 1.f)) return FA_ERR_INVALID_ARG;
-    if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_UNSUPPORTED;
+    if (dtype != FA_BF16 && dtype != FA_FP32 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if ((long long)B * H > 65535) return FA_ERR_UNSUPPORTED;
     if (N > (1 << 24)) return FA_ERR_UNSUPPORTED;
@@ -66,7 +66,7 @@ int from_cuda(cudaError_t e) {
 }
 
 bool use_tensor_cores(const Problem& p) {
-    if (g_kernel_path != 0 || p.dtype != FA_BF16) return false;
+    if (g_kernel_path != 0 || (p.dtype != FA_BF16 && p.dtype != FA_FP16)) return false;
     // the tile lists of a block mask must fit in the kernels' shared memory
     const int tiles = (p.N + kMaskBlock - 1) / kMaskBlock;
     if (p.block_mask && tiles > (p.d == 128 ? kMaskListCapBwd128 : kMaskListCap)) return false;

@@ -15,8 +15,8 @@
 //        S^T = K_j Q_i^T,  dP^T = V_j dO_i^T          (TMEM, fp32)
 //      eight compute warps (thread = key row, half of the 128 query columns
 //      each) rebuild P^T = exp(S^T - LSE), apply masks and dropout, and form
-//      dS^T = P^T o (dP^T - delta); P^T (bf16) goes back into TMEM and dS^T
-//      (bf16) into a swizzled shared-memory tile, then
+//      dS^T = P^T o (dP^T - delta); P^T (16-bit) goes back into TMEM and dS^T
+//      (16-bit) into a swizzled shared-memory tile, then
 //        dV_j += P^T dO_i  (A from TMEM),  dK_j += dS^T Q_i,
 //        dQ_i^T = K_j^T dS^T (both operands read MN-major)
 //      (at D = 128 computed transposed, dQ_i^T = K_j^T dS^T, so that a
@@ -43,7 +43,7 @@
 
 namespace fa {
 
-bool make_tmap_bf16(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
+bool make_tmap16(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows, CUtensorMapDataType type);
 
 namespace {
 
@@ -66,11 +66,11 @@ struct BwdCfg {
     static constexpr int kRegBudget = 256 * kComputeRegs + 128 * kIssueRegs + 128 * kReduceRegs;
     static_assert(kRegBudget <= kThreads * 128, "register budgets above the launch allocation");
     static constexpr int kStages = (D == 128) ? 2 : 3;
-    static constexpr int kTileBytes = kTile * D * 2;  // one 128 x D bf16 tile
+    static constexpr int kTileBytes = kTile * D * 2;  // one 128 x D 16-bit tile
     static constexpr int kBoxBytes = kTile * 128;     // 128 rows x 64 columns
     static constexpr int kBoxes = D / 64;
     static constexpr int kStageBytes = 2 * kTileBytes;  // Q_i and dO_i
-    static constexpr int kDsBytes = kTile * kTile * 2;  // dS^T, 128 x 128 bf16
+    static constexpr int kDsBytes = kTile * kTile * 2;  // dS^T, 128 x 128, 16-bit
     // (no alignment slack: the dynamic shared memory window starts 1024-byte
     // aligned, which the kernel checks)
     // block masks: this key tile's list of visible query tiles
@@ -172,7 +172,7 @@ __device__ __forceinline__ void red_add_f32(float* dst, float a) {
 }
 
 
-template <int D, bool kMask>
+template <typename T, int D, bool kMask>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -304,10 +304,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         regs_dec<Cfg::kIssueRegs>();
         // the whole warp runs the issue loop; one elected lane issues
         if (n_active > 0) {
-            constexpr uint32_t id_sh = idesc_bf16_f32(kTile, 64, 0, 0);      // S^T_h, dP^T_h (N = 64)
-            constexpr uint32_t id_dv = idesc_bf16_f32(kTile, D, 0, 1);      // dV (A tmem), dK (A K-major)
-            constexpr uint32_t id_dqt_h = idesc_bf16_f32(kTile, 64, 1, 1);   // dQ^T_h (A, B MN-major, N = 64)
-            constexpr uint32_t id_dq = idesc_bf16_f32(kTile, D, 1, 1);       // dQ (A, B MN-major)
+            constexpr uint32_t id_sh = idesc_f32acc(Elem16<T>::kFmt, kTile, 64, 0, 0);      // S^T_h, dP^T_h (N = 64)
+            constexpr uint32_t id_dv = idesc_f32acc(Elem16<T>::kFmt, kTile, D, 0, 1);      // dV (A tmem), dK (A K-major)
+            constexpr uint32_t id_dqt_h = idesc_f32acc(Elem16<T>::kFmt, kTile, 64, 1, 1);   // dQ^T_h (A, B MN-major, N = 64)
+            constexpr uint32_t id_dq = idesc_f32acc(Elem16<T>::kFmt, kTile, D, 1, 1);       // dQ (A, B MN-major)
             const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
             // descriptors built once, advanced by constants per MMA
             const uint64_t kd_k = smem_desc_sw128(k_base, 16, 1024);         // K, K-major
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    // dV += P^T_h dO_h (P^T_h, bf16, in TMEM columns 64h..64h+31) and
+                    // dV += P^T_h dO_h (P^T_h, 16-bit, in TMEM columns 64h..64h+31) and
                     // dK += dS^T_h Q_h (dS^T half h is shared-memory box h),
                     // at D = 128 interleaved with dQ so that consecutive MMAs
                     // go to different accumulators:
@@ -585,10 +585,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         fadd2(t[2], t[3], __uint_as_float(dr[x + 2]), __uint_as_float(dr[x + 3]), d4.z, d4.w);
                         fmul2(g[0], g[1], e[0], e[1], t[0], t[1]);
                         fmul2(g[2], g[3], e[2], e[3], t[2], t[3]);
-                        pk[x / 2] = pack_bf16x2(e[0], e[1]);
-                        pk[x / 2 + 1] = pack_bf16x2(e[2], e[3]);
-                        dsk[x / 2] = pack_bf16x2(g[0], g[1]);
-                        dsk[x / 2 + 1] = pack_bf16x2(g[2], g[3]);
+                        pk[x / 2] = Elem16<T>::pack2(e[0], e[1]);
+                        pk[x / 2 + 1] = Elem16<T>::pack2(e[2], e[3]);
+                        dsk[x / 2] = Elem16<T>::pack2(g[0], g[1]);
+                        dsk[x / 2 + 1] = Elem16<T>::pack2(g[2], g[3]);
                     }
                 } else {
 #pragma unroll
@@ -610,10 +610,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         ffma2(t[2], t[3], __uint_as_float(dr[x + 2]), __uint_as_float(dr[x + 3]), z[2], z[3], d4.z, d4.w);
                         fmul2(g[0], g[1], e[0], e[1], t[0], t[1]);
                         fmul2(g[2], g[3], e[2], e[3], t[2], t[3]);
-                        pk[x / 2] = pack_bf16x2(pv[0], pv[1]);
-                        pk[x / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-                        dsk[x / 2] = pack_bf16x2(g[0], g[1]);
-                        dsk[x / 2 + 1] = pack_bf16x2(g[2], g[3]);
+                        pk[x / 2] = Elem16<T>::pack2(pv[0], pv[1]);
+                        pk[x / 2 + 1] = Elem16<T>::pack2(pv[2], pv[3]);
+                        dsk[x / 2] = Elem16<T>::pack2(g[0], g[1]);
+                        dsk[x / 2 + 1] = Elem16<T>::pack2(g[2], g[3]);
                     }
                 }
                 // P^T into TMEM columns this warp has already read
@@ -634,13 +634,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             i = i_next;
         }
         // epilogue: dK = scale * acc, dV = acc, rows of this key tile
-        __nv_bfloat16* dK = static_cast<__nv_bfloat16*>(p.dk) + ((size_t)bh * p.N) * D;
-        __nv_bfloat16* dV = static_cast<__nv_bfloat16*>(p.dv) + ((size_t)bh * p.N) * D;
+        T* dK = static_cast<T*>(p.dk) + ((size_t)bh * p.N) * D;
+        T* dV = static_cast<T*>(p.dv) + ((size_t)bh * p.N) * D;
         const bool have = ok && n_active > 0 && mbar_wait_warp(&st->acc_done, 0, wctx, 122);
         if (have) tc_fence_after();
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
-            __nv_bfloat16* out = which ? dV : dK;
+            T* out = which ? dV : dK;
             const float mul = which ? 1.f : p.scale;
             const uint32_t col0 = (which ? Cfg::kColDV : Cfg::kColDK) + half * (D / 2);
 #pragma unroll
@@ -659,10 +659,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         uint4 w4;
-                        w4.x = pack_bf16x2(__uint_as_float(ar[8 * v + 0]) * mul, __uint_as_float(ar[8 * v + 1]) * mul);
-                        w4.y = pack_bf16x2(__uint_as_float(ar[8 * v + 2]) * mul, __uint_as_float(ar[8 * v + 3]) * mul);
-                        w4.z = pack_bf16x2(__uint_as_float(ar[8 * v + 4]) * mul, __uint_as_float(ar[8 * v + 5]) * mul);
-                        w4.w = pack_bf16x2(__uint_as_float(ar[8 * v + 6]) * mul, __uint_as_float(ar[8 * v + 7]) * mul);
+                        w4.x = Elem16<T>::pack2(__uint_as_float(ar[8 * v + 0]) * mul, __uint_as_float(ar[8 * v + 1]) * mul);
+                        w4.y = Elem16<T>::pack2(__uint_as_float(ar[8 * v + 2]) * mul, __uint_as_float(ar[8 * v + 3]) * mul);
+                        w4.z = Elem16<T>::pack2(__uint_as_float(ar[8 * v + 4]) * mul, __uint_as_float(ar[8 * v + 5]) * mul);
+                        w4.w = Elem16<T>::pack2(__uint_as_float(ar[8 * v + 6]) * mul, __uint_as_float(ar[8 * v + 7]) * mul);
                         dst[v] = w4;
                     }
                 }
@@ -676,18 +676,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
-// delta_i = sum_c dO_ic O_ic and dQacc = 0 (bf16 inputs): D/8 threads per
+// delta_i = sum_c dO_ic O_ic and dQacc = 0 (16-bit inputs): D/8 threads per
 // row, 16-byte loads and stores, the row sum reduced across those threads.
-template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_tc_kernel(const __nv_bfloat16* __restrict__ O,
-                                                         const __nv_bfloat16* __restrict__ dO,
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_pre_tc_kernel(const T* __restrict__ O, const T* __restrict__ dO,
                                                          float* __restrict__ delta, float* __restrict__ dq_acc,
                                                          size_t rows) {
-    constexpr int T = D / 8;  // threads per row (8 or 16)
+    constexpr int TPR = D / 8;  // threads per row (8 or 16)
     pdl_wait();               // O comes from the forward kernel
     pdl_trigger();
-    const size_t row = ((size_t)blockIdx.x * 256 + threadIdx.x) / T;
-    const int t = threadIdx.x % T;
+    const size_t row = ((size_t)blockIdx.x * 256 + threadIdx.x) / TPR;
+    const int t = threadIdx.x % TPR;
     // every lane takes part in the shuffles below; past the last row it
     // contributes zeros and stores nothing
     const bool valid = row < rows;
@@ -698,13 +697,13 @@ __global__ void __launch_bounds__(256) bwd_pre_tc_kernel(const __nv_bfloat16* __
     float s = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
-        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+        const float2 of = Elem16<T>::unpack2(ow[e]);
+        const float2 gf = Elem16<T>::unpack2(gw[e]);
         s = fmaf(of.x, gf.x, s);
         s = fmaf(of.y, gf.y, s);
     }
 #pragma unroll
-    for (int w = T / 2; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+    for (int w = TPR / 2; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
     if (!valid) return;
     if (t == 0) delta[row] = s;
     float4* acc = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * t;
@@ -712,7 +711,8 @@ __global__ void __launch_bounds__(256) bwd_pre_tc_kernel(const __nv_bfloat16* __
     acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// dq = bf16(scale * dQacc), 4 elements per thread.
+// dq = T(scale * dQacc), 4 elements per thread.
+template <typename T>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
                                                          float scale, size_t n4) {
     pdl_wait();  // the accumulator is complete only when the main kernel is
@@ -720,18 +720,19 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restric
     if (idx >= n4) return;
     const float4 a = acc[idx];
     uint2 w;
-    w.x = pack_bf16x2(a.x * scale, a.y * scale);
-    w.y = pack_bf16x2(a.z * scale, a.w * scale);
+    w.x = Elem16<T>::pack2(a.x * scale, a.y * scale);
+    w.y = Elem16<T>::pack2(a.z * scale, a.w * scale);
     dq[idx] = w;
 }
 
-template <int D>
+template <typename T, int D>
 int launch_bwd_tc_d(const Problem& pr) {
     using Cfg = BwdCfg<D>;
+    constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
     const int BH = pr.B * pr.H;
     CUtensorMap tq, tk, tv, tdo;
-    if (!make_tmap_bf16(&tq, pr.q, BH, pr.N, D, kTile) || !make_tmap_bf16(&tk, pr.k, BH, pr.N, D, kTile) ||
-        !make_tmap_bf16(&tv, pr.v, BH, pr.N, D, kTile) || !make_tmap_bf16(&tdo, pr.dO, BH, pr.N, D, kTile))
+    if (!make_tmap16(&tq, pr.q, BH, pr.N, D, kTile, tt) || !make_tmap16(&tk, pr.k, BH, pr.N, D, kTile, tt) ||
+        !make_tmap16(&tv, pr.v, BH, pr.N, D, kTile, tt) || !make_tmap16(&tdo, pr.dO, BH, pr.N, D, kTile, tt))
         return FA_ERR_CUDA;
     const size_t rows = (size_t)BH * pr.N;
     // The three kernels are launched with programmatic stream serialization:
@@ -746,8 +747,8 @@ int launch_bwd_tc_d(const Problem& pr) {
     cfg.numAttrs = 1;
     cfg.blockDim = dim3(256);
     cfg.gridDim = dim3((unsigned)((rows * (D / 8) + 255) / 256));
-    if (cudaLaunchKernelEx(&cfg, bwd_pre_tc_kernel<D>, static_cast<const __nv_bfloat16*>(pr.o),
-                           static_cast<const __nv_bfloat16*>(pr.dO), pr.delta, pr.dq_acc, rows) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, bwd_pre_tc_kernel<T, D>, static_cast<const T*>(pr.o), static_cast<const T*>(pr.dO),
+                           pr.delta, pr.dq_acc, rows) != cudaSuccess)
         return FA_ERR_CUDA;
     note_launches(1);
 
@@ -772,17 +773,17 @@ int launch_bwd_tc_d(const Problem& pr) {
     p.seed = pr.seed;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(bwd_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(bwd_tc_kernel<T, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::smem(false)) != cudaSuccess ||
-            cudaFuncSetAttribute(bwd_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(bwd_tc_kernel<T, D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::smem(true)) != cudaSuccess)
             return FA_ERR_CUDA;
         // setmaxnreg.inc takes registers from what the CTA was launched with
         // and waits (without bound) until they are free: refuse to launch
         // unless the budgets fit in that allocation
         cudaFuncAttributes a0{}, a1{};
-        if (cudaFuncGetAttributes(&a0, bwd_tc_kernel<D, false>) != cudaSuccess ||
-            cudaFuncGetAttributes(&a1, bwd_tc_kernel<D, true>) != cudaSuccess ||
+        if (cudaFuncGetAttributes(&a0, bwd_tc_kernel<T, D, false>) != cudaSuccess ||
+            cudaFuncGetAttributes(&a1, bwd_tc_kernel<T, D, true>) != cudaSuccess ||
             a0.numRegs * Cfg::kThreads < Cfg::kRegBudget || a1.numRegs * Cfg::kThreads < Cfg::kRegBudget) {
             if (std::getenv("FA_DEBUG"))
                 std::fprintf(stderr, "fa: bwd register budget %d exceeds the launch allocation (%d, %d regs)\n",
@@ -794,8 +795,8 @@ int launch_bwd_tc_d(const Problem& pr) {
     cfg.gridDim = dim3(BH, (pr.N + kTile - 1) / kTile);
     cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr);
-    cudaError_t e = pr.block_mask ? cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, true>, tq, tk, tv, tdo, p)
-                                  : cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, false>, tq, tk, tv, tdo, p);
+    cudaError_t e = pr.block_mask ? cudaLaunchKernelEx(&cfg, bwd_tc_kernel<T, D, true>, tq, tk, tv, tdo, p)
+                                  : cudaLaunchKernelEx(&cfg, bwd_tc_kernel<T, D, false>, tq, tk, tv, tdo, p);
     note_launches(1);
     if (e != cudaSuccess) {
         if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: bwd_tc launch: %s\n", cudaGetErrorString(e));
@@ -805,7 +806,7 @@ int launch_bwd_tc_d(const Problem& pr) {
     cfg.gridDim = dim3((unsigned)((n4 + 255) / 256));
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
-    e = cudaLaunchKernelEx(&cfg, dq_convert_kernel, reinterpret_cast<const float4*>(pr.dq_acc),
+    e = cudaLaunchKernelEx(&cfg, dq_convert_kernel<T>, reinterpret_cast<const float4*>(pr.dq_acc),
                            static_cast<uint2*>(pr.dq), pr.scale, n4);
     note_launches(1);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -815,7 +816,10 @@ int launch_bwd_tc_d(const Problem& pr) {
 
 int launch_bwd_tc(const Problem& p) {
     if (!(p.scale > 0.f)) return launch_bwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
-    return p.d == 64 ? launch_bwd_tc_d<64>(p) : launch_bwd_tc_d<128>(p);
+    if (p.dtype == FA_FP16) return p.d == 64 ? launch_bwd_tc_d<__half, 64>(p) : launch_bwd_tc_d<__half, 128>(p);
+    if (p.dtype == FA_BF16)
+        return p.d == 64 ? launch_bwd_tc_d<__nv_bfloat16, 64>(p) : launch_bwd_tc_d<__nv_bfloat16, 128>(p);
+    return FA_ERR_UNSUPPORTED;
 }
 
 }  // namespace fa

@@ -109,7 +109,7 @@ struct SharedPP {
     int n_list[2];  // kSplit: visible key tiles of each query tile
 };
 
-template <int D, bool kSplit, bool kPartial>
+template <typename T, int D, bool kSplit, bool kPartial>
 __global__ void __launch_bounds__(kThreadsPP, 1)
     fwd_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -280,8 +280,8 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
         // ------------------------------------------------------------ MMA issuer
         regs_dec<kIssueRegs>();
         if (n_max > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kBlockM, D, 0, 1);
+            constexpr uint32_t idesc_s = idesc_f32acc(Elem16<T>::kFmt, kBlockM, kBlockN, 0, 0);
+            constexpr uint32_t idesc_o = idesc_f32acc(Elem16<T>::kFmt, kBlockM, D, 0, 1);
             const uint32_t kv_base = smem_u32(sKV);
             const uint64_t qd0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t qd1 = smem_desc_sw128(smem_u32(sQ + Cfg::kQBytes), 16, 1024);
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                         const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
                         const int k = (x >> 1) & 3;
                         fadd2(ps[2 * k], ps[2 * k + 1], ps[2 * k], ps[2 * k + 1], e0, e1);
-                        sr[c][x >> 1] = pack_bf16x2(e0, e1);
+                        sr[c][x >> 1] = Elem16<T>::pack2(e0, e1);
                     }
                     tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
                 }
@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                         const int k = (x >> 1) & 3;
                         fadd2(ps[2 * k], ps[2 * k + 1], ps[2 * k], ps[2 * k + 1], e0, e1);
                         sr[c][x >> 1] =
-                            pack_bf16x2(((keep[c] >> x) & 1u) ? e0 : 0.f, ((keep[c] >> (x + 1)) & 1u) ? e1 : 0.f);
+                            Elem16<T>::pack2(((keep[c] >> x) & 1u) ? e0 : 0.f, ((keep[c] >> (x + 1)) & 1u) ? e1 : 0.f);
                     }
                     tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
                 }
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             tc_fence_before();
             mbar_arrive_warp(&st->p_full[t]);
         }
-        __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N) * D;
+        T* O = static_cast<T*>(p.o) + ((size_t)bh * p.N) * D;
         // split-KV partials of this split and head
         const size_t prow = ((size_t)split * p.BH + bh) * p.N;
         if (ok && n > 0) {
@@ -598,10 +598,10 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint4 w4;
-                            w4.x = pack_bf16x2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
-                            w4.y = pack_bf16x2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
-                            w4.z = pack_bf16x2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
-                            w4.w = pack_bf16x2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
+                            w4.x = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
+                            w4.y = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
+                            w4.z = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
+                            w4.w = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
                             dst[v] = w4;
                         }
                     }
@@ -657,15 +657,16 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-// [B*H, N, d] bf16 viewed as a 3-D tensor (d fastest); boxes of 64 x rows.
-bool make_tmap_bf16(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
+// [B*H, N, d] of a 16-bit type viewed as a 3-D tensor (d fastest); boxes of
+// 64 x rows.
+bool make_tmap16(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows, CUtensorMapDataType type) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = fn(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -677,10 +678,10 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int BH, int N, int d, in
 // "FlashAttention" blog post (section "Tiling") and of the paper summary's
 // incremental softmax (section "Pelacakan Softmax Inkremental"). One warp per
 // row; rows without a visible key (every LSE_s = -inf) get O = 0, LSE = -inf.
-template <int D>
+template <typename T, int D>
 __global__ void __launch_bounds__(256) splitkv_merge_kernel(const float* __restrict__ o_part,
                                                             const float* __restrict__ lse_part,
-                                                            __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                                            T* __restrict__ o, float* __restrict__ lse,
                                                             int n_splits, size_t rows) {
     pdl_wait();  // the partials come from the forward kernel
     const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -704,20 +705,21 @@ __global__ void __launch_bounds__(256) splitkv_merge_kernel(const float* __restr
         }
     }
     const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
-    __nv_bfloat16* dst = o + row * D + lane * PER;
+    T* dst = o + row * D + lane * PER;
 #pragma unroll
     for (int e = 0; e < PER; e += 2)
-        *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+        *reinterpret_cast<uint32_t*>(dst + e) = Elem16<T>::pack2(acc[e] * inv, acc[e + 1] * inv);
     if (lane == 0) lse[row] = (wsum > 0.f) ? mx + logf(wsum) : -INFINITY;
 }
 
-template <int D, bool kSplit, bool kPartial>
+template <typename T, int D, bool kSplit, bool kPartial>
 int launch_fwd_tc_d(const Problem& pr) {
     constexpr int kSmem = FwdPPCfg<D>::kSmem;
+    constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
     CUtensorMap tq, tk, tv;
     const int BH = pr.B * pr.H;
-    if (!make_tmap_bf16(&tq, pr.q, BH, pr.N, D, kBlockM) || !make_tmap_bf16(&tk, pr.k, BH, pr.N, D, kBlockN) ||
-        !make_tmap_bf16(&tv, pr.v, BH, pr.N, D, kBlockN))
+    if (!make_tmap16(&tq, pr.q, BH, pr.N, D, kBlockM, tt) || !make_tmap16(&tk, pr.k, BH, pr.N, D, kBlockN, tt) ||
+        !make_tmap16(&tv, pr.v, BH, pr.N, D, kBlockN, tt))
         return FA_ERR_CUDA;
     FwdParams p{};
     p.lse = pr.lse;
@@ -739,7 +741,7 @@ int launch_fwd_tc_d(const Problem& pr) {
     p.dropout = pr.dropout_p > 0.f;
     p.causal = pr.causal;
     p.seed = pr.seed;
-    auto kernel = fwd_pp_kernel<D, kSplit, kPartial>;
+    auto kernel = fwd_pp_kernel<T, D, kSplit, kPartial>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
@@ -779,24 +781,33 @@ int launch_fwd_tc_d(const Problem& pr) {
         cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = 0;
-        e = cudaLaunchKernelEx(&cfg, splitkv_merge_kernel<D>, (const float*)p.o_part, (const float*)p.lse_part,
-                               static_cast<__nv_bfloat16*>(pr.o), pr.lse, p.n_splits, rows);
+        e = cudaLaunchKernelEx(&cfg, splitkv_merge_kernel<T, D>, (const float*)p.o_part, (const float*)p.lse_part,
+                               static_cast<T*>(pr.o), pr.lse, p.n_splits, rows);
         note_launches(1);
         if (e != cudaSuccess) return FA_ERR_CUDA;
     }
     return FA_OK;
 }
 
-int launch_fwd_tc(const Problem& p) {
-    if (!(p.scale > 0.f)) return launch_fwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+template <typename T>
+int launch_fwd_tc_t(const Problem& p) {
     // without a block mask both tiles' key lists are prefixes of one list and
     // share its K/V loads; with one, each tile has its own list (kSplit)
     if (p.o_part) {  // split-KV
-        if (p.block_mask) return p.d == 64 ? launch_fwd_tc_d<64, true, true>(p) : launch_fwd_tc_d<128, true, true>(p);
-        return p.d == 64 ? launch_fwd_tc_d<64, false, true>(p) : launch_fwd_tc_d<128, false, true>(p);
+        if (p.block_mask)
+            return p.d == 64 ? launch_fwd_tc_d<T, 64, true, true>(p) : launch_fwd_tc_d<T, 128, true, true>(p);
+        return p.d == 64 ? launch_fwd_tc_d<T, 64, false, true>(p) : launch_fwd_tc_d<T, 128, false, true>(p);
     }
-    if (p.block_mask) return p.d == 64 ? launch_fwd_tc_d<64, true, false>(p) : launch_fwd_tc_d<128, true, false>(p);
-    return p.d == 64 ? launch_fwd_tc_d<64, false, false>(p) : launch_fwd_tc_d<128, false, false>(p);
+    if (p.block_mask)
+        return p.d == 64 ? launch_fwd_tc_d<T, 64, true, false>(p) : launch_fwd_tc_d<T, 128, true, false>(p);
+    return p.d == 64 ? launch_fwd_tc_d<T, 64, false, false>(p) : launch_fwd_tc_d<T, 128, false, false>(p);
+}
+
+int launch_fwd_tc(const Problem& p) {
+    if (!(p.scale > 0.f)) return launch_fwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    if (p.dtype == FA_FP16) return launch_fwd_tc_t<__half>(p);
+    if (p.dtype == FA_BF16) return launch_fwd_tc_t<__nv_bfloat16>(p);
+    return FA_ERR_UNSUPPORTED;
 }
 
 }  // namespace fa

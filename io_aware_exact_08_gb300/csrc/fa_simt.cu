@@ -1,4 +1,5 @@
-// CUDA-core (fp32 FMA) kernels for exact tiled attention, any element type.
+// CUDA-core (fp32 FMA) kernels for exact tiled attention, any element type
+// (fp32, bf16, fp16).
 //
 // These serve the fp32 inputs (where a single tf32 tensor-core pass cannot
 // meet 1e-4 on O) and act as a second, independent GPU path for the bf16
@@ -437,16 +438,19 @@ cudaError_t bwd_simt(const Problem& p) {
 
 cudaError_t launch_fwd_simt(const Problem& p) {
     if (p.dtype == FA_BF16) return p.d == 64 ? fwd_simt<__nv_bfloat16, 64>(p) : fwd_simt<__nv_bfloat16, 128>(p);
+    if (p.dtype == FA_FP16) return p.d == 64 ? fwd_simt<__half, 64>(p) : fwd_simt<__half, 128>(p);
     return p.d == 64 ? fwd_simt<float, 64>(p) : fwd_simt<float, 128>(p);
 }
 
 cudaError_t launch_bwd_preprocess(const Problem& p) {
     if (p.dtype == FA_BF16) return p.d == 64 ? bwd_pre<__nv_bfloat16, 64>(p) : bwd_pre<__nv_bfloat16, 128>(p);
+    if (p.dtype == FA_FP16) return p.d == 64 ? bwd_pre<__half, 64>(p) : bwd_pre<__half, 128>(p);
     return p.d == 64 ? bwd_pre<float, 64>(p) : bwd_pre<float, 128>(p);
 }
 
 cudaError_t launch_bwd_simt(const Problem& p) {
     if (p.dtype == FA_BF16) return p.d == 64 ? bwd_simt<__nv_bfloat16, 64>(p) : bwd_simt<__nv_bfloat16, 128>(p);
+    if (p.dtype == FA_FP16) return p.d == 64 ? bwd_simt<__half, 64>(p) : bwd_simt<__half, 128>(p);
     return p.d == 64 ? bwd_simt<float, 64>(p) : bwd_simt<float, 128>(p);
 }
 

@@ -6,6 +6,8 @@
 #include <cstdint>
 
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace fa {
@@ -331,13 +333,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t start, uint32_t lbo
 // the single MMA-issuing thread fast enough to keep the tensor core fed.
 __device__ __forceinline__ uint64_t desc_add(uint64_t base, uint32_t bytes) { return base + (uint64_t)(bytes >> 4); }
 
-// Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
-// Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B
-// format (1 = bf16), 15 A major (0 = K, 1 = MN), 16 B major, [17,23) N>>3,
-// [24,29) M>>4.
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 D and A, B of
+// the 16-bit format fmt (0 = fp16, 1 = bf16). Bits: [4,6) D format (1 = f32),
+// [7,10) A format, [10,13) B format, 15 A major (0 = K, 1 = MN), 16 B major,
+// [17,23) N>>3, [24,29) M>>4. One fmt feeds both operand fields: A and B of
+// one MMA always have the same type.
+__host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t fmt, int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4) | ((fmt & 7u) << 7) | ((fmt & 7u) << 10) | ((uint32_t)a_mn_major << 15) |
+           ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major, int b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    return idesc_f32acc(1u, M, N, a_mn_major, b_mn_major);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -351,6 +357,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The 16-bit element types of the tensor-core kernels: the tcgen05 operand
+// format code, the TMA element type, and conversions of two values at a time
+// (round to nearest even).
+template <typename T>
+struct Elem16;
+template <>
+struct Elem16<__nv_bfloat16> {
+    static constexpr uint32_t kFmt = 1;
+    static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    __device__ static __forceinline__ uint32_t pack2(float lo, float hi) { return pack_bf16x2(lo, hi); }
+    __device__ static __forceinline__ float2 unpack2(uint32_t w) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+    }
+};
+template <>
+struct Elem16<__half> {
+    static constexpr uint32_t kFmt = 0;
+    static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    __device__ static __forceinline__ uint32_t pack2(float lo, float hi) { return pack_f16x2(lo, hi); }
+    __device__ static __forceinline__ float2 unpack2(uint32_t w) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    }
+};
 
 // Paired fp32 arithmetic (one instruction for two lanes of work, each result
 // rounded exactly as the scalar fmaf / + / * would round it). The elementwise

@@ -26,11 +26,11 @@ def test_mask_hook_bit_exact(cuda_device, B, H, N, p, seed):
     assert np.array_equal(z_gpu, z_ref)
 
 
-def _reveal_inputs(B, H, N, d, shift):
+def _reveal_inputs(B, H, N, d, shift, dt=torch.bfloat16):
     nb = N // 128
-    q = torch.zeros(B, H, N, d, dtype=torch.bfloat16)
-    k = torch.randn(B, H, N, d, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
-    v = torch.zeros(B, H, N, d, dtype=torch.bfloat16)
+    q = torch.zeros(B, H, N, d, dtype=dt)
+    k = torch.randn(B, H, N, d, generator=torch.Generator().manual_seed(3)).to(dt)
+    v = torch.zeros(B, H, N, d, dtype=dt)
     for j in range(N):
         v[:, :, j, j % d] = 1.0
     bm = torch.zeros(nb, nb, dtype=torch.uint8)
@@ -39,10 +39,11 @@ def _reveal_inputs(B, H, N, d, shift):
     return q, k, v, bm
 
 
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
 @pytest.mark.parametrize("shift", [0, 1, 2, 3])
-def test_forward_applies_the_same_mask(cuda_device, shift):
+def test_forward_applies_the_same_mask(cuda_device, shift, dt):
     B, H, N, d, p, seed = 2, 2, 512, 128, 0.1, 1003
-    q, k, v, bm = _reveal_inputs(B, H, N, d, shift)
+    q, k, v, bm = _reveal_inputs(B, H, N, d, shift, dt)
     dev = lambda t: t.cuda().contiguous()
     o, lse = fa.attention_fwd(dev(q), dev(k), dev(v), scale=0.125, block_mask=dev(bm), dropout_p=p, seed=seed)
     o = o.float().cpu().numpy()
@@ -58,11 +59,12 @@ def test_forward_applies_the_same_mask(cuda_device, shift):
         assert np.allclose(kept, 1.0 / (128 * (1 - p)), rtol=1e-2)
 
 
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
 @pytest.mark.parametrize("shift", [0, 3])
-def test_backward_applies_the_same_mask(cuda_device, shift):
+def test_backward_applies_the_same_mask(cuda_device, shift, dt):
     B, H, N, d, p, seed = 2, 2, 512, 128, 0.1, 77
-    q, k, v, bm = _reveal_inputs(B, H, N, d, shift)
-    do = torch.zeros(B, H, N, d, dtype=torch.bfloat16)
+    q, k, v, bm = _reveal_inputs(B, H, N, d, shift, dt)
+    do = torch.zeros(B, H, N, d, dtype=dt)
     for i in range(N):
         do[:, :, i, i % d] = 1.0
     dev = lambda t: t.cuda().contiguous()

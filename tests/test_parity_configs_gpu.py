@@ -43,3 +43,16 @@ def test_sweep_forward_parity(cuda_device, w):
     heads = [0, w.B * w.H - 1]
     ref = oracle_fwd_bwd(inp, heads=heads, backward=False)
     compare(got, ref, w.dtype, keys=("o", "lse"), heads=heads)
+
+
+@pytest.mark.parametrize("name", ["gpt2_causal", "bert_pad_dropout", "long_causal"])
+def test_workload_parity_fp16(cuda_device, name):
+    """The same workloads with fp16 inputs, as `bench.py --dtype fp16` runs them."""
+    w = WORKLOADS[name].with_(dtype="fp16")
+    inp = make_inputs(w)
+    got = gpu_fwd_bwd(inp)
+    heads = SAMPLED_HEADS[name]
+    errs = compare(got, oracle_fwd_bwd(inp, heads=heads), "fp16", heads=heads)
+    print(name, "fp16", errs)
+    for key in ("o", "dq", "dk", "dv"):
+        assert np.isfinite(got[key]).all(), key

@@ -1,7 +1,7 @@
 """GPU vs fp64 oracle, element by element, on small seeded cases that span
 several 128-row tiles and a ragged tail, with every mask and dropout, for
-both the tensor-core (bf16) and the CUDA-core (fp32, and bf16 on request)
-kernels. Tolerances: see parity_utils.TOL."""
+both the tensor-core (bf16, fp16) and the CUDA-core (fp32, and bf16 or fp16
+on request) kernels. Tolerances: see parity_utils.TOL."""
 import pytest
 import torch
 
@@ -48,7 +48,7 @@ def _ids(c):
 
 
 @pytest.mark.parametrize("case", CASES, ids=_ids)
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 def test_parity_default_path(cuda_device, case, dtype):
     N, d, causal, pad, blocky, p = case
     inp = _case(N, d, dtype, causal, pad, blocky, p)
@@ -58,16 +58,17 @@ def test_parity_default_path(cuda_device, case, dtype):
 
 
 @pytest.mark.parametrize("case", CASES[::2], ids=_ids)
-def test_parity_cuda_core_path_bf16(cuda_device, case):
-    """The CUDA-core kernels on bf16 inputs (the tensor-core path's twin)."""
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_parity_cuda_core_path_16bit(cuda_device, case, dtype):
+    """The CUDA-core kernels on 16-bit inputs (the tensor-core path's twin)."""
     N, d, causal, pad, blocky, p = case
-    inp = _case(N, d, "bf16", causal, pad, blocky, p)
+    inp = _case(N, d, dtype, causal, pad, blocky, p)
     old = fa.fa_set_kernel_path(1)
     try:
         got = gpu_fwd_bwd(inp)
     finally:
         fa.fa_set_kernel_path(old)
-    compare(got, oracle_fwd_bwd(inp), "bf16")
+    compare(got, oracle_fwd_bwd(inp), dtype)
 
 
 def test_fully_masked_rows(cuda_device):

@@ -14,8 +14,8 @@ from workloads import Workload, make_inputs, random_block_mask
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(N, d, causal=False, pad=False, blocky=False, p=0.0, B=2, H=3, seed=11):
-    w = Workload("splitkv", 0, B=B, H=H, N=N, d=d, dtype="bf16", causal=causal,
+def _inputs(N, d, causal=False, pad=False, blocky=False, p=0.0, B=2, H=3, seed=11, dtype="bf16"):
+    w = Workload("splitkv", 0, B=B, H=H, N=N, d=d, dtype=dtype, causal=causal,
                  kv_len_range=((max(1, N // 2), N) if pad else None), dropout_p=p)
     inp = make_inputs(w, seed=seed, with_grad_out=False)
     if blocky:
@@ -52,6 +52,14 @@ def test_splitkv_matches_oracle(cuda_device, case):
     got = _run(inp, splits)
     ref = oracle_fwd_bwd(inp, backward=False)
     compare(got, ref, "bf16", keys=("o", "lse"))
+
+
+@pytest.mark.parametrize("case", CASES[::2], ids=lambda c: f"N{c[0]}-d{c[1]}-s{c[6]}")
+def test_splitkv_fp16_matches_oracle(cuda_device, case):
+    N, d, causal, pad, blocky, p, splits = case
+    inp = _inputs(N, d, causal, pad, blocky, p, dtype="fp16")
+    got = _run(inp, splits)
+    compare(got, oracle_fwd_bwd(inp, backward=False), "fp16", keys=("o", "lse"))
 
 
 def test_splitkv_agrees_with_single_pass(cuda_device):

@@ -15,7 +15,7 @@ N(0,1) from a seeded CPU generator.
 Recipe (identical for every workload):
   * ``torch.Generator('cpu').manual_seed(seed)``, seed = 1000 + workload index;
   * draw, in this order, fp32 N(0,1) tensors Q, K, V, dO of shape [B,H,N,d];
-  * round each to the workload dtype (bf16 rounding is round-to-nearest-even);
+  * round each to the workload dtype (bf16 and fp16 rounding is round-to-nearest-even);
   * then, if the workload pads keys, kv_len[b] ~ U{lo..hi} (inclusive);
   * the block mask (block 128 x 128) is a fixed pattern, not random.
 """
@@ -38,7 +38,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str  # "bf16" or "fp32"
+    dtype: str  # "bf16", "fp16" or "fp32"
     causal: bool = False
     kv_len_range: Optional[tuple] = None  # (lo, hi) inclusive, per sequence
     dropout_p: float = 0.0
@@ -56,7 +56,7 @@ class Workload:
 
     @property
     def torch_dtype(self):
-        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        return {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[self.dtype]
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
