@@ -15,7 +15,11 @@
  *    and the element type `dtype`. lse is fp32 [B, H, N] in natural log:
  *    lse = m + ln(l), which carries the same information as the pair (l, m)
  *    the pages keep for the backward pass.
- *  - d must be 64 or 128. B, H >= 1, N >= 0 (N == 0 is a no-op).
+ *  - d must be 64, 128 or 256. B, H >= 1, N >= 0 (N == 0 is a no-op).
+ *    d = 256, the largest head dimension of the FlashAttention-2 section of
+ *    "Penjelasan Flash Attention: Panduan Komprehensif" ("Dukungan untuk
+ *    dimensi head yang lebih besar"), runs on the CUDA-core kernels for
+ *    every dtype.
  *  - Masks combine by AND: causal (key j > query i is masked, top-left
  *    aligned), key padding (j >= kv_len[b] masked; kv_len is int32[B] in
  *    device memory, or NULL), block mask (block_mask[(i/128)*nb + j/128] == 0
@@ -58,7 +62,7 @@ typedef enum { FA_BF16 = 0, FA_FP32 = 1, FA_FP16 = 2 } fa_dtype;
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = -1,   /* null pointer, negative size, p outside [0,1), misalignment */
-    FA_ERR_UNSUPPORTED = -2,   /* d not in {64,128}, unknown dtype */
+    FA_ERR_UNSUPPORTED = -2,   /* d not in {64,128,256}, unknown dtype */
     FA_ERR_CUDA = -3,          /* a CUDA runtime call failed (launch, attribute, symbol) */
     FA_ERR_WORKSPACE = -4,     /* workspace missing or smaller than fa_bwd_workspace_size */
     FA_ERR_DEVICE_TIMEOUT = -5 /* a device-side bounded wait ran out (see fa_check_device_status) */

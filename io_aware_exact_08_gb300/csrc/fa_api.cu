@@ -35,7 +35,7 @@ int check_common(int B, int H, int N, int d, float scale, float dropout_p, fa_dt
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (!(dropout_p >= 0.f && dropout_p < 1.f)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_BF16 && dtype != FA_FP32 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if ((long long)B * H > 65535) return FA_ERR_UNSUPPORTED;
     if (N > (1 << 24)) return FA_ERR_UNSUPPORTED;
     return FA_OK;
@@ -67,6 +67,9 @@ int from_cuda(cudaError_t e) {
 
 bool use_tensor_cores(const Problem& p) {
     if (g_kernel_path != 0 || (p.dtype != FA_BF16 && p.dtype != FA_FP16)) return false;
+    // head dim 256 runs on the CUDA-core kernels: two 128-row tiles of S and
+    // O at d = 256 need 768 TMEM columns, more than the SM's 512
+    if (p.d == 256) return false;
     // the tile lists of a block mask must fit in the kernels' shared memory
     const int tiles = (p.N + kMaskBlock - 1) / kMaskBlock;
     if (p.block_mask && tiles > (p.d == 128 ? kMaskListCapBwd128 : kMaskListCap)) return false;
@@ -122,7 +125,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 }
 
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int n_splits) {
-    if (B < 1 || H < 1 || N < 0 || (d != 64 && d != 128) || n_splits < 1 || n_splits > kMaxSplits) return 0;
+    if (B < 1 || H < 1 || N < 0 || (d != 64 && d != 128 && d != 256) || n_splits < 1 || n_splits > kMaxSplits)
+        return 0;
     const size_t rows = (size_t)B * H * N;
     return round256((size_t)n_splits * rows * d * sizeof(float)) + round256((size_t)n_splits * rows * sizeof(float));
 }
@@ -162,7 +166,7 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
-    if (B < 1 || H < 1 || N < 0 || (d != 64 && d != 128)) return 0;
+    if (B < 1 || H < 1 || N < 0 || (d != 64 && d != 128 && d != 256)) return 0;
     const size_t rows = (size_t)B * H * N;
     return round256(rows * sizeof(float)) + round256(rows * (size_t)d * sizeof(float));
 }

@@ -62,12 +62,19 @@ __device__ __forceinline__ bool visible(const SimtArgs& a, int L, int i, int j) 
 // Forward: grid (ceil(N/16), B*H), 128 threads; warp w owns rows
 // row0 + 4w .. row0 + 4w + 3; lane l scores key j0 + l of each staged tile.
 // ---------------------------------------------------------------------------
+template <int D>
+constexpr size_t fwd_simt_smem() {
+    return sizeof(float) * ((size_t)kRowsPerCta * D + (size_t)kTile * (D + 1) + (size_t)kTile * D);
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(128) fwd_simt_kernel(SimtArgs a) {
     constexpr int DPL = D / 32;  // output columns per lane
-    __shared__ float sQ[kRowsPerCta][D];
-    __shared__ float sK[kTile][D + 1];
-    __shared__ float sV[kTile][D];
+    // dynamic shared memory (at d = 256 the tiles pass the 48 KB static limit)
+    extern __shared__ float simt_smem[];
+    float(*sQ)[D] = reinterpret_cast<float(*)[D]>(simt_smem);                        // [kRowsPerCta][D]
+    float(*sK)[D + 1] = reinterpret_cast<float(*)[D + 1]>(simt_smem + kRowsPerCta * D);  // [kTile][D + 1]
+    float(*sV)[D] = reinterpret_cast<float(*)[D]>(simt_smem + kRowsPerCta * D + kTile * (D + 1));  // [kTile][D]
 
     const int bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
     const int row0 = blockIdx.x * kRowsPerCta;
@@ -172,15 +179,22 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
 // Backward dK/dV: grid (ceil(N/16), B*H); warp w owns key rows
 // key0 + 4w .. +3; lane l handles query i0 + l of each staged query tile.
 // ---------------------------------------------------------------------------
+template <int D>
+constexpr size_t bwd_simt_smem() {  // either backward kernel
+    return sizeof(float) * (2 * (size_t)kRowsPerCta * D + 2 * (size_t)kTile * (D + 1) + 2 * (size_t)kTile);
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(SimtArgs a) {
     constexpr int DPL = D / 32;
-    __shared__ float sKr[kRowsPerCta][D];
-    __shared__ float sVr[kRowsPerCta][D];
-    __shared__ float sQ[kTile][D + 1];
-    __shared__ float sdO[kTile][D + 1];
-    __shared__ float sLse[kTile];
-    __shared__ float sDelta[kTile];
+    extern __shared__ float simt_smem[];
+    float(*sKr)[D] = reinterpret_cast<float(*)[D]>(simt_smem);                     // [kRowsPerCta][D]
+    float(*sVr)[D] = reinterpret_cast<float(*)[D]>(simt_smem + kRowsPerCta * D);   // [kRowsPerCta][D]
+    float(*sQ)[D + 1] = reinterpret_cast<float(*)[D + 1]>(simt_smem + 2 * kRowsPerCta * D);  // [kTile][D + 1]
+    float(*sdO)[D + 1] =
+        reinterpret_cast<float(*)[D + 1]>(simt_smem + 2 * kRowsPerCta * D + kTile * (D + 1));  // [kTile][D + 1]
+    float* sLse = simt_smem + 2 * kRowsPerCta * D + 2 * kTile * (D + 1);  // [kTile]
+    float* sDelta = sLse + kTile;                                          // [kTile]
 
     const int bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
     const int key0 = blockIdx.x * kRowsPerCta;
@@ -279,10 +293,12 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(SimtArgs a) {
 template <typename T, int D>
 __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(SimtArgs a) {
     constexpr int DPL = D / 32;
-    __shared__ float sQ[kRowsPerCta][D];
-    __shared__ float sdO[kRowsPerCta][D];
-    __shared__ float sK[kTile][D + 1];
-    __shared__ float sV[kTile][D + 1];
+    extern __shared__ float simt_smem[];
+    float(*sQ)[D] = reinterpret_cast<float(*)[D]>(simt_smem);                    // [kRowsPerCta][D]
+    float(*sdO)[D] = reinterpret_cast<float(*)[D]>(simt_smem + kRowsPerCta * D);  // [kRowsPerCta][D]
+    float(*sK)[D + 1] = reinterpret_cast<float(*)[D + 1]>(simt_smem + 2 * kRowsPerCta * D);  // [kTile][D + 1]
+    float(*sV)[D + 1] =
+        reinterpret_cast<float(*)[D + 1]>(simt_smem + 2 * kRowsPerCta * D + kTile * (D + 1));  // [kTile][D + 1]
 
     const int bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
     const int row0 = blockIdx.x * kRowsPerCta;
@@ -401,10 +417,23 @@ SimtArgs make_args(const Problem& p) {
     return a;
 }
 
+// Opts a kernel into more than 48 KB of dynamic shared memory (once).
+template <typename K>
+cudaError_t allow_smem(K kernel, size_t bytes, bool& done) {
+    if (done || bytes <= 48 * 1024) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done = true;
+    return e;
+}
+
 template <typename T, int D>
 cudaError_t fwd_simt(const Problem& p) {
+    constexpr size_t smem = fwd_simt_smem<D>();
+    static bool attr = false;
+    cudaError_t e = allow_smem(fwd_simt_kernel<T, D>, smem, attr);
+    if (e != cudaSuccess) return e;
     dim3 grid((p.N + kRowsPerCta - 1) / kRowsPerCta, p.B * p.H);
-    fwd_simt_kernel<T, D><<<grid, 128, 0, p.stream>>>(make_args(p));
+    fwd_simt_kernel<T, D><<<grid, 128, smem, p.stream>>>(make_args(p));
     note_launches(1);
     return cudaGetLastError();
 }
@@ -423,35 +452,42 @@ template <typename T, int D>
 cudaError_t bwd_simt(const Problem& p) {
     cudaError_t e = bwd_pre<T, D>(p);
     if (e != cudaSuccess) return e;
+    constexpr size_t smem = bwd_simt_smem<D>();
+    static bool attr_kv = false, attr_q = false;
+    if ((e = allow_smem(bwd_dkdv_simt_kernel<T, D>, smem, attr_kv)) != cudaSuccess) return e;
+    if ((e = allow_smem(bwd_dq_simt_kernel<T, D>, smem, attr_q)) != cudaSuccess) return e;
     dim3 grid((p.N + kRowsPerCta - 1) / kRowsPerCta, p.B * p.H);
     const SimtArgs a = make_args(p);
-    bwd_dkdv_simt_kernel<T, D><<<grid, 128, 0, p.stream>>>(a);
+    bwd_dkdv_simt_kernel<T, D><<<grid, 128, smem, p.stream>>>(a);
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dq_simt_kernel<T, D><<<grid, 128, 0, p.stream>>>(a);
+    bwd_dq_simt_kernel<T, D><<<grid, 128, smem, p.stream>>>(a);
     note_launches(1);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+// head dims 64, 128 and 256 (the caller has checked d)
+#define FA_SIMT_BY_D(fn, T) (p.d == 64 ? fn<T, 64>(p) : p.d == 128 ? fn<T, 128>(p) : fn<T, 256>(p))
+
 cudaError_t launch_fwd_simt(const Problem& p) {
-    if (p.dtype == FA_BF16) return p.d == 64 ? fwd_simt<__nv_bfloat16, 64>(p) : fwd_simt<__nv_bfloat16, 128>(p);
-    if (p.dtype == FA_FP16) return p.d == 64 ? fwd_simt<__half, 64>(p) : fwd_simt<__half, 128>(p);
-    return p.d == 64 ? fwd_simt<float, 64>(p) : fwd_simt<float, 128>(p);
+    if (p.dtype == FA_BF16) return FA_SIMT_BY_D(fwd_simt, __nv_bfloat16);
+    if (p.dtype == FA_FP16) return FA_SIMT_BY_D(fwd_simt, __half);
+    return FA_SIMT_BY_D(fwd_simt, float);
 }
 
 cudaError_t launch_bwd_preprocess(const Problem& p) {
-    if (p.dtype == FA_BF16) return p.d == 64 ? bwd_pre<__nv_bfloat16, 64>(p) : bwd_pre<__nv_bfloat16, 128>(p);
-    if (p.dtype == FA_FP16) return p.d == 64 ? bwd_pre<__half, 64>(p) : bwd_pre<__half, 128>(p);
-    return p.d == 64 ? bwd_pre<float, 64>(p) : bwd_pre<float, 128>(p);
+    if (p.dtype == FA_BF16) return FA_SIMT_BY_D(bwd_pre, __nv_bfloat16);
+    if (p.dtype == FA_FP16) return FA_SIMT_BY_D(bwd_pre, __half);
+    return FA_SIMT_BY_D(bwd_pre, float);
 }
 
 cudaError_t launch_bwd_simt(const Problem& p) {
-    if (p.dtype == FA_BF16) return p.d == 64 ? bwd_simt<__nv_bfloat16, 64>(p) : bwd_simt<__nv_bfloat16, 128>(p);
-    if (p.dtype == FA_FP16) return p.d == 64 ? bwd_simt<__half, 64>(p) : bwd_simt<__half, 128>(p);
-    return p.d == 64 ? bwd_simt<float, 64>(p) : bwd_simt<float, 128>(p);
+    if (p.dtype == FA_BF16) return FA_SIMT_BY_D(bwd_simt, __nv_bfloat16);
+    if (p.dtype == FA_FP16) return FA_SIMT_BY_D(bwd_simt, __half);
+    return FA_SIMT_BY_D(bwd_simt, float);
 }
 
 cudaError_t launch_dropout_mask(uint8_t* keep, int B, int H, int N, uint32_t thr, uint64_t seed, cudaStream_t s) {

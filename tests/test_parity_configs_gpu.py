@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 from parity_utils import compare, gpu_fwd_bwd, gpu_forward, oracle_fwd_bwd
-from workloads import WORKLOADS, make_inputs, sweep_workloads
+from workloads import WORKLOADS, headdim_workloads, make_inputs, sweep_workloads
 
 pytestmark = pytest.mark.gpu
 
@@ -56,3 +56,13 @@ def test_workload_parity_fp16(cuda_device, name):
     print(name, "fp16", errs)
     for key in ("o", "dq", "dk", "dv"):
         assert np.isfinite(got[key]).all(), key
+
+
+@pytest.mark.parametrize("w", headdim_workloads(), ids=lambda w: w.name)
+def test_headdim_workload_parity(cuda_device, w):
+    """Head dim 256 at full size, as the benchmark runs it, on two sampled heads."""
+    inp = make_inputs(w)
+    got = gpu_fwd_bwd(inp)
+    heads = [0, w.B * w.H - 1]
+    errs = compare(got, oracle_fwd_bwd(inp, heads=heads), w.dtype, heads=heads)
+    print(w.name, errs)

@@ -57,6 +57,24 @@ def test_parity_default_path(cuda_device, case, dtype):
     compare(got, ref, dtype)
 
 
+# head dim 256 (CUDA-core kernels for every dtype)
+CASES_D256 = [
+    (1, 256, False, False, False, 0.0),
+    (129, 256, True, False, False, 0.0),
+    (300, 256, True, True, False, 0.0),
+    (384, 256, False, False, True, 0.1),
+    (520, 256, True, False, False, 0.2),
+]
+
+
+@pytest.mark.parametrize("case", CASES_D256, ids=_ids)
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+def test_parity_head_dim_256(cuda_device, case, dtype):
+    N, d, causal, pad, blocky, p = case
+    inp = _case(N, d, dtype, causal, pad, blocky, p)
+    compare(gpu_fwd_bwd(inp), oracle_fwd_bwd(inp), dtype)
+
+
 @pytest.mark.parametrize("case", CASES[::2], ids=_ids)
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_parity_cuda_core_path_16bit(cuda_device, case, dtype):

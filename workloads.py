@@ -101,6 +101,14 @@ def splitkv_workloads():
                      note="few heads, long context")]
 
 
+def headdim_workloads():
+    """Head dimension 256, the widest the FlashAttention-2 section of the
+    "Flash Attention" guide supports ("Dukungan untuk dimensi head yang lebih
+    besar"), at 16K tokens per step like the sweep."""
+    return [Workload("d256_causal", 30, B=2, H=8, N=4096, d=256, dtype="bf16", causal=True,
+                     note="head dim 256")]
+
+
 def band_butterfly_block_mask(nb: int, band: int = 2) -> torch.Tensor:
     """Block mask M[i][j] (uint8, nb x nb): |i-j| <= band, or j == i XOR 2^k.
 
