@@ -65,11 +65,11 @@ int from_cuda(cudaError_t e) {
     return FA_ERR_CUDA;
 }
 
-bool use_tensor_cores(const Problem& p) {
+// The forward runs on tensor cores for d = 64, 128 and 256; the backward for
+// d = 64 and 128 (at d = 256 its dK and dV accumulators alone fill TMEM).
+bool use_tensor_cores(const Problem& p, bool backward) {
     if (g_kernel_path != 0 || (p.dtype != FA_BF16 && p.dtype != FA_FP16)) return false;
-    // head dim 256 runs on the CUDA-core kernels: two 128-row tiles of S and
-    // O at d = 256 need 768 TMEM columns, more than the SM's 512
-    if (p.d == 256) return false;
+    if (backward && p.d == 256) return false;
     // the tile lists of a block mask must fit in the kernels' shared memory
     const int tiles = (p.N + kMaskBlock - 1) / kMaskBlock;
     if (p.block_mask && tiles > (p.d == 128 ? kMaskListCapBwd128 : kMaskListCap)) return false;
@@ -120,7 +120,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     p.lse = lse;
     rc = status_address(&p.status);
     if (rc != FA_OK) return rc;
-    if (use_tensor_cores(p)) return launch_fwd_tc(p);
+    if (use_tensor_cores(p, false)) return launch_fwd_tc(p);
     return from_cuda(launch_fwd_simt(p));
 }
 
@@ -154,8 +154,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
     if (rc != FA_OK) return rc;
     // one split, the CUDA-core kernels or a non-positive scale: the plain
     // forward computes the same result
-    if (n_splits == 1 || !use_tensor_cores(p) || !(scale > 0.f)) {
-        if (use_tensor_cores(p)) return launch_fwd_tc(p);
+    if (n_splits == 1 || !use_tensor_cores(p, false) || !(scale > 0.f)) {
+        if (use_tensor_cores(p, false)) return launch_fwd_tc(p);
         return from_cuda(launch_fwd_simt(p));
     }
     const size_t rows = (size_t)B * H * N;
@@ -200,7 +200,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)));
     rc = status_address(&p.status);
     if (rc != FA_OK) return rc;
-    if (use_tensor_cores(p)) return launch_bwd_tc(p);
+    if (use_tensor_cores(p, true)) return launch_bwd_tc(p);
     return from_cuda(launch_bwd_simt(p));
 }
 

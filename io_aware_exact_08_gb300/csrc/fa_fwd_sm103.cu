@@ -635,6 +635,403 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Head dim 256: one 128-row query tile per CTA. Two query tiles would need
+// 2 x (128 + 256) = 768 TMEM columns; one tile with a double-buffered S needs
+// 2 x 128 + 256 = 512, the whole TMEM. S(u) lives in buffer u % 2 (columns
+// 128 (u % 2)), O in columns 256-511. The MMA warp issues S(u+1) before
+// P(u) V, so the softmax of key tile u+1 runs while the tensor core computes
+// P(u) V_u and S(u+2):
+//     S(0), S(1), [P(0)] P(0) V_0, S(2), [P(1)] P(1) V_1, S(3), ...
+// Because P(u) V may still be running when the softmax of tile u+1 wants to
+// rescale O, that rescale (rare: only when the row max rises by more than
+// 2^8) first waits for the P(u) V commit.
+// Roles (192 threads): warps 0-3 softmax (one thread per query row), warp 4
+// TMA producer, warp 5 MMA issuer (all lanes run its loop, one elected lane
+// issues). K/V tiles are 64 KB, so the ring has two stages; each load has
+// the softmax of one key tile to land in.
+// ---------------------------------------------------------------------------
+constexpr int kThreads256 = 192;
+
+struct Fwd256Cfg {
+    static constexpr int D = 256;
+    static constexpr int kStages = 2;
+    static constexpr int kTileBytes = kBlockN * D * 2;  // one K or V tile, 64 KB
+    static constexpr int kQBytes = kBlockM * D * 2;     // 64 KB
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kBoxBytes = kBlockN * 128;
+    // + the query tile's list of visible key tiles (block masks)
+    static constexpr int kSmem = 1024 + kQBytes + kStages * kTileBytes + 256 + kMaskListCap * 2;
+};
+
+struct Shared256 {
+    uint64_t kv_full[2];
+    uint64_t kv_empty[2];
+    uint64_t q_full;
+    uint64_t s_full[2];  // buffer b: S(u) for u % 2 == b
+    uint64_t p_full[2];  // buffer b: P(u) written over S(u)
+    uint64_t o_done;     // one commit after every P(u) V
+    uint64_t o_final;
+    uint64_t teardown;
+    uint32_t tmem_base;
+    int abort_flag;
+    int n_list;
+};
+static_assert(sizeof(Shared256) <= 256, "barrier block");
+
+template <typename T, bool kSplit, bool kPartial>
+__global__ void __launch_bounds__(kThreads256, 1)
+    fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using Cfg = Fwd256Cfg;
+    constexpr int D = Cfg::D;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sKV = smem + Cfg::kQBytes;
+    Shared256* st = reinterpret_cast<Shared256*>(sKV + Cfg::kStages * Cfg::kTileBytes);
+    uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);  // [kMaskListCap]
+
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // grid (B*H, query tiles x splits), x fastest: every head's heaviest
+    // causal tile goes out first
+    const int bh = blockIdx.x;
+    const int b = bh / p.H, h = bh % p.H;
+    const int rank = kPartial ? (int)blockIdx.y / p.n_splits : (int)blockIdx.y;
+    const int split = kPartial ? (int)blockIdx.y % p.n_splits : 0;
+    const int qt = p.causal ? (p.n_qtiles - 1 - rank) : rank;
+    const int L = p.kv_len ? min(max(p.kv_len[b], 0), p.N) : p.N;
+    const int nkt = (L + kBlockN - 1) / kBlockN;
+    int n = p.causal ? min(nkt, qt + 1) : nkt;
+    // this CTA's range [kb, ke) of key tiles (all of them unless split-KV)
+    int kb = 0, ke = 1 << 30;
+    if constexpr (kPartial) {
+        const int chunk = (n + p.n_splits - 1) / p.n_splits;
+        kb = split * chunk;
+        ke = kb + chunk;
+        n = max(0, min(n, ke) - kb);
+    }
+    WaitCtx wctx{&st->abort_flag, p.status};
+    if (kSplit && warp == 0) {
+        int e = p.causal ? min(nkt, qt + 1) : nkt;
+        e = min(e, ke);
+        const uint8_t* row = p.block_mask + (size_t)qt * p.nb;
+        int cnt = 0;
+        for (int c = kb & ~31; c < e; c += 32) {
+            const int j = c + lane;
+            const bool act = j >= kb && j < e && row[j] != 0;
+            const uint32_t bal = __ballot_sync(0xffffffffu, act);
+            if (act) sList[cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)j;
+            cnt += __popc(bal);
+        }
+        if (lane == 0) st->n_list = cnt;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            mbar_init(&st->kv_full[s], 1);
+            mbar_init(&st->kv_empty[s], 1);
+        }
+        mbar_init(&st->q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&st->s_full[s], 1);
+            mbar_init(&st->p_full[s], kSoftmaxThreads / 32);
+        }
+        mbar_init(&st->o_done, 1);
+        mbar_init(&st->o_final, 1);
+        mbar_init(&st->teardown, 1);
+        st->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&st->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = st->tmem_base;
+    if constexpr (kSplit) n = st->n_list;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        // load order: K(0), K(1), then per step u: V(u), K(u+2)
+        if (lane == 0 && n > 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(&st->q_full, Cfg::kQBytes);
+#pragma unroll
+            for (int x = 0; x < Cfg::kBoxes; ++x)
+                tma_load_3d(sQ + x * Cfg::kBoxBytes, &tm_q, &st->q_full, x * 64, qt * kBlockM, bh);
+            int t = 0;  // load counter
+            auto load = [&](const CUtensorMap* map, int u) -> bool {
+                const int j = kSplit ? (int)sList[u] : kb + u;
+                const int s = t % Cfg::kStages;
+                const uint32_t ph = (t / Cfg::kStages) & 1;
+                if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 161)) return false;
+                mbar_arrive_expect_tx(&st->kv_full[s], Cfg::kTileBytes);
+                uint8_t* dst = sKV + s * Cfg::kTileBytes;
+#pragma unroll
+                for (int x = 0; x < Cfg::kBoxes; ++x)
+                    tma_load_3d(dst + x * Cfg::kBoxBytes, map, &st->kv_full[s], x * 64, j * kBlockN, bh);
+                ++t;
+                return true;
+            };
+            bool okp = load(&tm_k, 0);
+            if (okp && n > 1) okp = load(&tm_k, 1);
+            for (int u = 0; okp && u < n; ++u) {
+                okp = load(&tm_v, u);
+                if (okp && u + 2 < n) okp = load(&tm_k, u + 2);
+            }
+            // drain: the last load issued into each stage has landed
+            for (int l = max(0, t - Cfg::kStages); l < t; ++l)
+                mbar_wait(&st->kv_full[l % Cfg::kStages], (l / Cfg::kStages) & 1, wctx, 162);
+            mbar_wait(&st->q_full, 0, wctx, 163);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (n > 0) {
+            constexpr uint32_t idesc_s = idesc_f32acc(Elem16<T>::kFmt, kBlockM, kBlockN, 0, 0);
+            constexpr uint32_t idesc_o = idesc_f32acc(Elem16<T>::kFmt, kBlockM, D, 0, 1);
+            constexpr uint32_t kStageUnits = Cfg::kTileBytes >> 4;
+            const uint32_t kv_base = smem_u32(sKV);
+            const uint64_t qd = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t kvd_k = smem_desc_sw128(kv_base, 16, 1024);              // K tiles, K-major
+            const uint64_t kvd_v = smem_desc_sw128(kv_base, Cfg::kBoxBytes, 1024);  // V tiles, MN-major
+            bool ok = mbar_wait_warp(&st->q_full, 0, wctx, 170);
+            tc_fence_after();
+            int ld = 0;  // next load to use, in the producer's order
+            // S(u) = Q K_u^T into buffer u % 2
+            auto issue_s = [&](int u) -> bool {
+                const int s = ld % Cfg::kStages;
+                if (!mbar_wait_warp(&st->kv_full[s], (ld / Cfg::kStages) & 1, wctx, 171)) return false;
+                tc_fence_after();
+                const uint64_t kd = kvd_k + (uint64_t)(s * kStageUnits);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+                    mma_ss_warp(tmem + (u & 1) * 128, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0);
+                }
+                mma_commit_warp(&st->s_full[u & 1]);
+                mma_commit_warp(&st->kv_empty[s]);
+                ++ld;
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            if (ok && n > 1) ok = issue_s(1);
+            for (int u = 0; ok && u < n; ++u) {
+                // O += P(u) V_u, A = P(u) from TMEM
+                if (!mbar_wait_warp(&st->p_full[u & 1], (u >> 1) & 1, wctx, 172)) break;
+                tc_fence_after();
+                const int s = ld % Cfg::kStages;
+                if (!mbar_wait_warp(&st->kv_full[s], (ld / Cfg::kStages) & 1, wctx, 174)) break;
+                tc_fence_after();
+                const uint64_t vd = kvd_v + (uint64_t)(s * kStageUnits);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ts_warp(tmem + 256, tmem + (u & 1) * 128 + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
+                                (u > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_warp(&st->kv_empty[s]);
+                ++ld;
+                mma_commit_warp(&st->o_done);
+                if (u + 1 == n) mma_commit_warp(&st->o_final);
+                // S(u+2) over the P(u) columns just read (MMAs run in order)
+                if (u + 2 < n) ok = issue_s(u + 2);
+            }
+            mma_commit_warp(&st->teardown);
+            mbar_wait_warp(&st->teardown, 0, wctx, 173);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int r = tid;  // 0..127
+        const int i = qt * kBlockM + r;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t obase = tmem + lane_base + 256;
+        float m = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+        for (int u = 0; u < n; ++u) {
+            const int ktile = kSplit ? (int)sList[u] : kb + u;
+            const uint32_t sbase = tmem + lane_base + (u & 1) * 128;
+            uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+            if (p.dropout) {
+#pragma unroll 8
+                for (int g = 0; g < 32; ++g) {
+                    const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, i, ktile * (kBlockN / 4) + g);
+                    if (g == 0) keep[0] = keep[1] = keep[2] = keep[3] = 0;
+                    const uint32_t sh = bits << (4 * (g & 7));
+                    if ((g >> 3) == 0) keep[0] |= sh;
+                    else if ((g >> 3) == 1) keep[1] |= sh;
+                    else if ((g >> 3) == 2) keep[2] |= sh;
+                    else keep[3] |= sh;
+                }
+            }
+            if (!mbar_wait_warp(&st->s_full[u & 1], (u >> 1) & 1, wctx, 180)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int k0 = ktile * kBlockN;
+            int lim = min(kBlockN, L - k0);
+            if (p.causal) lim = min(lim, i - k0 + 1);
+            const bool full = lim >= kBlockN;
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(sbase + c * 32, sr[c]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+            if (!full) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        if (c * 32 + x >= lim) sr[c][x] = __float_as_uint(-INFINITY);
+            }
+            float pm[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) pm[x] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int x = 0; x < 32; x += 2)
+                    pm[(x >> 1) & 7] =
+                        fmax3(pm[(x >> 1) & 7], __uint_as_float(sr[c][x]), __uint_as_float(sr[c][x + 1]));
+            pm[0] = fmax3(pm[0], pm[1], pm[2]);
+            pm[3] = fmax3(pm[3], pm[4], pm[5]);
+            pm[6] = fmaxf(pm[6], pm[7]);
+            pm[0] = fmax3(pm[0], pm[3], pm[6]);
+            const float mt = pm[0] * p.scale_log2;
+            const bool raise = mt > m + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, raise) && u > 0) {
+                // O must hold P(u-1) V before it is rescaled
+                if (!mbar_wait_warp(&st->o_done, (u - 1) & 1, wctx, 181)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float alpha = raise ? ex2_approx(m - mt) : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 8; ++c) {
+                    uint32_t orr[8];
+                    tmem_ld8(obase + c * 8, orr);
+                    tmem_ld_wait();
+                    reg_fence8(orr);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) orr[x] = __float_as_uint(__uint_as_float(orr[x]) * alpha);
+                    tmem_st8(obase + c * 8, orr);
+                }
+                if (raise) l *= alpha;
+            }
+            if (raise) m = mt;
+            const float nmref = (m == -INFINITY) ? 0.f : -m;
+            const float sl2 = p.scale_log2;
+            float ps[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) ps[x] = 0.f;
+            // exponentials packed in place (P chunk c in columns 16c..16c+15,
+            // already read); the sum takes every exponential, the dropout
+            // mask only what goes to P
+            if (!p.dropout) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 2) {
+                        float a0, a1;
+                        ffma2(a0, a1, __uint_as_float(sr[c][x]), __uint_as_float(sr[c][x + 1]), sl2, sl2, nmref, nmref);
+                        const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+                        const int k = (x >> 1) & 3;
+                        fadd2(ps[2 * k], ps[2 * k + 1], ps[2 * k], ps[2 * k + 1], e0, e1);
+                        sr[c][x >> 1] = Elem16<T>::pack2(e0, e1);
+                    }
+                    tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 2) {
+                        float a0, a1;
+                        ffma2(a0, a1, __uint_as_float(sr[c][x]), __uint_as_float(sr[c][x + 1]), sl2, sl2, nmref, nmref);
+                        const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+                        const int k = (x >> 1) & 3;
+                        fadd2(ps[2 * k], ps[2 * k + 1], ps[2 * k], ps[2 * k + 1], e0, e1);
+                        sr[c][x >> 1] =
+                            Elem16<T>::pack2(((keep[c] >> x) & 1u) ? e0 : 0.f, ((keep[c] >> (x + 1)) & 1u) ? e1 : 0.f);
+                    }
+                    tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
+                }
+            }
+            fadd2(ps[0], ps[1], ps[0], ps[1], ps[4], ps[5]);
+            fadd2(ps[2], ps[3], ps[2], ps[3], ps[6], ps[7]);
+            fadd2(ps[0], ps[1], ps[0], ps[1], ps[2], ps[3]);
+            l += ps[0] + ps[1];
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive_warp(&st->p_full[u & 1]);
+        }
+        T* O = static_cast<T*>(p.o) + ((size_t)bh * p.N) * D;
+        const size_t prow = ((size_t)split * p.BH + bh) * p.N;  // split-KV partials
+        if (ok && n > 0) {
+            if (mbar_wait_warp(&st->o_final, 0, wctx, 182)) {
+                tc_fence_after();
+                const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(obase + c * 32, orr);
+                    tmem_ld_wait();
+                    reg_fence(orr);
+                    if (kPartial && i < p.N) {
+                        float4* dst = reinterpret_cast<float4*>(p.o_part + (prow + i) * D + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(__uint_as_float(orr[4 * v]) * inv, __uint_as_float(orr[4 * v + 1]) * inv,
+                                                 __uint_as_float(orr[4 * v + 2]) * inv,
+                                                 __uint_as_float(orr[4 * v + 3]) * inv);
+                    } else if (i < p.N) {
+                        uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w4;
+                            w4.x = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
+                            w4.y = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
+                            w4.z = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
+                            w4.w = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
+                            dst[v] = w4;
+                        }
+                    }
+                }
+                if (i < p.N) {
+                    const float lse_i = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+                    if (kPartial) p.lse_part[prow + i] = lse_i;
+                    else p.lse[(size_t)bh * p.N + i] = lse_i;
+                }
+            }
+        } else if (n == 0 && i < p.N) {
+            if (kPartial) {
+                float4* dst = reinterpret_cast<float4*>(p.o_part + (prow + i) * D);
+#pragma unroll 4
+                for (int v = 0; v < D / 4; ++v) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                p.lse_part[prow + i] = -INFINITY;
+            } else {
+                uint4 z = make_uint4(0, 0, 0, 0);
+                uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D);
+#pragma unroll 4
+                for (int v = 0; v < D / 8; ++v) dst[v] = z;
+                p.lse[(size_t)bh * p.N + i] = -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -712,15 +1109,8 @@ __global__ void __launch_bounds__(256) splitkv_merge_kernel(const float* __restr
     if (lane == 0) lse[row] = (wsum > 0.f) ? mx + logf(wsum) : -INFINITY;
 }
 
-template <typename T, int D, bool kSplit, bool kPartial>
-int launch_fwd_tc_d(const Problem& pr) {
-    constexpr int kSmem = FwdPPCfg<D>::kSmem;
-    constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
-    CUtensorMap tq, tk, tv;
+FwdParams fwd_params(const Problem& pr) {
     const int BH = pr.B * pr.H;
-    if (!make_tmap16(&tq, pr.q, BH, pr.N, D, kBlockM, tt) || !make_tmap16(&tk, pr.k, BH, pr.N, D, kBlockN, tt) ||
-        !make_tmap16(&tv, pr.v, BH, pr.N, D, kBlockN, tt))
-        return FA_ERR_CUDA;
     FwdParams p{};
     p.lse = pr.lse;
     p.o = pr.o;
@@ -741,6 +1131,33 @@ int launch_fwd_tc_d(const Problem& pr) {
     p.dropout = pr.dropout_p > 0.f;
     p.causal = pr.causal;
     p.seed = pr.seed;
+    return p;
+}
+
+// split-KV: merges the partial results into O and LSE (launched behind the
+// forward kernel with programmatic stream serialization)
+template <typename T, int D>
+int launch_merge(const Problem& pr, const FwdParams& p, cudaLaunchConfig_t cfg) {
+    const size_t rows = (size_t)p.BH * pr.N;
+    cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, splitkv_merge_kernel<T, D>, (const float*)p.o_part,
+                                             (const float*)p.lse_part, static_cast<T*>(pr.o), pr.lse, p.n_splits, rows);
+    note_launches(1);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <typename T, int D, bool kSplit, bool kPartial>
+int launch_fwd_tc_d(const Problem& pr) {
+    constexpr int kSmem = FwdPPCfg<D>::kSmem;
+    constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
+    CUtensorMap tq, tk, tv;
+    const int BH = pr.B * pr.H;
+    if (!make_tmap16(&tq, pr.q, BH, pr.N, D, kBlockM, tt) || !make_tmap16(&tk, pr.k, BH, pr.N, D, kBlockN, tt) ||
+        !make_tmap16(&tv, pr.v, BH, pr.N, D, kBlockN, tt))
+        return FA_ERR_CUDA;
+    const FwdParams p = fwd_params(pr);
     auto kernel = fwd_pp_kernel<T, D, kSplit, kPartial>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -775,22 +1192,55 @@ int launch_fwd_tc_d(const Problem& pr) {
         if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: fwd_tc launch: %s\n", cudaGetErrorString(e));
         return FA_ERR_CUDA;
     }
-    if (p.o_part) {
-        // split-KV: merge the partial results into O and LSE
-        const size_t rows = (size_t)BH * pr.N;
-        cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
-        cfg.blockDim = dim3(256);
-        cfg.dynamicSmemBytes = 0;
-        e = cudaLaunchKernelEx(&cfg, splitkv_merge_kernel<T, D>, (const float*)p.o_part, (const float*)p.lse_part,
-                               static_cast<T*>(pr.o), pr.lse, p.n_splits, rows);
-        note_launches(1);
-        if (e != cudaSuccess) return FA_ERR_CUDA;
+    if (p.o_part) return launch_merge<T, D>(pr, p, cfg);
+    return FA_OK;
+}
+
+template <typename T, bool kSplit, bool kPartial>
+int launch_fwd256(const Problem& pr) {
+    constexpr int kSmem = Fwd256Cfg::kSmem;
+    constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
+    CUtensorMap tq, tk, tv;
+    const int BH = pr.B * pr.H;
+    if (!make_tmap16(&tq, pr.q, BH, pr.N, 256, kBlockM, tt) || !make_tmap16(&tk, pr.k, BH, pr.N, 256, kBlockN, tt) ||
+        !make_tmap16(&tv, pr.v, BH, pr.N, 256, kBlockN, tt))
+        return FA_ERR_CUDA;
+    const FwdParams p = fwd_params(pr);
+    auto kernel = fwd_d256_kernel<T, kSplit, kPartial>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+            return FA_ERR_CUDA;
+        attr_set = true;
     }
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    const long long grid_y = (long long)p.n_qtiles * p.n_splits;
+    if (grid_y > 65535) return FA_ERR_UNSUPPORTED;
+    cfg.gridDim = dim3(BH, (unsigned)grid_y);
+    cfg.blockDim = dim3(kThreads256);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = pr.stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
+    note_launches(1);
+    if (e != cudaSuccess) {
+        if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: fwd_d256 launch: %s\n", cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    }
+    if (p.o_part) return launch_merge<T, 256>(pr, p, cfg);
     return FA_OK;
 }
 
 template <typename T>
 int launch_fwd_tc_t(const Problem& p) {
+    if (p.d == 256) {  // one query tile per CTA
+        if (p.o_part) return p.block_mask ? launch_fwd256<T, true, true>(p) : launch_fwd256<T, false, true>(p);
+        return p.block_mask ? launch_fwd256<T, true, false>(p) : launch_fwd256<T, false, false>(p);
+    }
     // without a block mask both tiles' key lists are prefixes of one list and
     // share its K/V loads; with one, each tile has its own list (kSplit)
     if (p.o_part) {  // split-KV

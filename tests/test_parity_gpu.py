@@ -57,7 +57,8 @@ def test_parity_default_path(cuda_device, case, dtype):
     compare(got, ref, dtype)
 
 
-# head dim 256 (CUDA-core kernels for every dtype)
+# head dim 256 (forward on the one-tile tensor-core kernel for 16-bit inputs,
+# backward on the CUDA cores)
 CASES_D256 = [
     (1, 256, False, False, False, 0.0),
     (129, 256, True, False, False, 0.0),
@@ -75,7 +76,7 @@ def test_parity_head_dim_256(cuda_device, case, dtype):
     compare(gpu_fwd_bwd(inp), oracle_fwd_bwd(inp), dtype)
 
 
-@pytest.mark.parametrize("case", CASES[::2], ids=_ids)
+@pytest.mark.parametrize("case", CASES[::2] + CASES_D256[1::2], ids=_ids)
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_parity_cuda_core_path_16bit(cuda_device, case, dtype):
     """The CUDA-core kernels on 16-bit inputs (the tensor-core path's twin)."""

@@ -42,6 +42,8 @@ CASES = [
     (300, 64, True, True, False, 0.2, 4),   # more splits than key tiles for the first pairs
     (1024, 64, True, False, False, 0.0, 8),
     (520, 128, True, False, True, 0.0, 3),
+    (520, 256, True, False, False, 0.0, 3),
+    (384, 256, False, True, True, 0.1, 2),
 ]
 
 
