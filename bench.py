@@ -92,9 +92,9 @@ def recorded_traffic(workload, call):
 
 def traffic_key(w, splits=1):
     """Key of a (workload, dtype, split count) in the DRAM traffic record."""
-    from workloads import WORKLOADS, headdim_workloads, splitkv_workloads, sweep_workloads
+    from workloads import WORKLOADS, headdim_workloads, sparse_workloads, splitkv_workloads, sweep_workloads
     base = {x.name: x for x in list(WORKLOADS.values()) + sweep_workloads() + splitkv_workloads() +
-            headdim_workloads()}.get(w.name)
+            headdim_workloads() + sparse_workloads()}.get(w.name)
     key = w.name
     if base is not None and base.dtype != w.dtype:
         key += f"/{w.dtype}"
@@ -452,9 +452,10 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    from workloads import WORKLOADS, headdim_workloads, splitkv_workloads, sweep_workloads
+    from workloads import WORKLOADS, headdim_workloads, sparse_workloads, splitkv_workloads, sweep_workloads
     table = dict(WORKLOADS)
-    table.update({w.name: w for w in sweep_workloads() + splitkv_workloads() + headdim_workloads()})
+    table.update({w.name: w for w in sweep_workloads() + splitkv_workloads() + headdim_workloads() +
+                  sparse_workloads()})
     w = table[args.workload]
     if args.dtype is not None:
         if w.dtype not in ("bf16", "fp16"):

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 from parity_utils import compare, gpu_fwd_bwd, gpu_forward, oracle_fwd_bwd
-from workloads import WORKLOADS, headdim_workloads, make_inputs, sweep_workloads
+from workloads import WORKLOADS, headdim_workloads, make_inputs, sparse_workloads, sweep_workloads
 
 pytestmark = pytest.mark.gpu
 
@@ -66,3 +66,25 @@ def test_headdim_workload_parity(cuda_device, w):
     heads = [0, w.B * w.H - 1]
     errs = compare(got, oracle_fwd_bwd(inp, heads=heads), w.dtype, heads=heads)
     print(w.name, errs)
+
+
+@pytest.mark.parametrize("w", sparse_workloads(), ids=lambda w: w.name)
+def test_sparse_workload_parity(cuda_device, w):
+    """Block-sparse at 64K and with a second pattern, as the benchmark runs
+    them: the oracle on one sampled head, and on every head two identities
+    that hold at any size. Softmax rows sum to 1, so sum_j dS_ij = 0 and
+    sum_j dK_j = scale sum_i (sum_j dS_ij) Q_i = 0; without dropout
+    sum_j dV_j = sum_i (sum_j P_ij) dO_i = sum_i dO_i (every row sees its
+    diagonal block)."""
+    inp = make_inputs(w)
+    got = gpu_fwd_bwd(inp)
+    heads = [w.B * w.H - 1]
+    errs = compare(got, oracle_fwd_bwd(inp, heads=heads), w.dtype, heads=heads)
+    print(w.name, errs)
+    dk, dv = got["dk"], got["dv"]
+    do = inp["do"].double().numpy()
+    for b in range(w.B):
+        for h in range(w.H):
+            assert np.abs(dk[b, h].sum(0)).max() <= 1e-3 * np.abs(dk[b, h]).sum(0).max()
+            gap = np.abs(dv[b, h].sum(0) - do[b, h].sum(0)).max()
+            assert gap <= 1e-3 * np.abs(dv[b, h]).sum(0).max()

@@ -43,6 +43,7 @@ class Workload:
     kv_len_range: Optional[tuple] = None  # (lo, hi) inclusive, per sequence
     dropout_p: float = 0.0
     block_sparse: bool = False
+    mask_pattern: str = "band_butterfly"  # block-sparse pattern: "band_butterfly" or "local_global"
     scale: Optional[float] = None  # default 1/sqrt(d)
     note: str = ""
 
@@ -131,6 +132,30 @@ def band_butterfly_block_mask(nb: int, band: int = 2) -> torch.Tensor:
     return m
 
 
+def local_global_block_mask(nb: int, window: int = 1, n_global: int = 1) -> torch.Tensor:
+    """Block mask M[i][j] (uint8, nb x nb): |i-j| <= window, or i < n_global,
+    or j < n_global: a sliding window of blocks plus global blocks that see
+    and are seen by every block. A second fixed pattern for the block-sparse
+    iterator, which accepts any M."""
+    m = torch.zeros(nb, nb, dtype=torch.uint8)
+    for i in range(nb):
+        m[i, max(0, i - window):min(nb, i + window + 1)] = 1
+    m[:n_global, :] = 1
+    m[:, :n_global] = 1
+    return m
+
+
+def sparse_workloads():
+    """Block-sparse attention beyond the 16K workload: the band + butterfly
+    pattern at N = 64K (the length of the Path-256 task in the paper
+    summary's results, "Hasil (beserta Angka Terpenting)"), and a second
+    pattern (sliding window + global blocks) at 16K."""
+    return [Workload("block_sparse_64k", 40, B=1, H=8, N=65536, d=64, dtype="bf16", block_sparse=True,
+                     note="band(2)+butterfly block-sparse attention at 64K"),
+            Workload("block_sparse_local_global", 41, B=1, H=8, N=16384, d=64, dtype="bf16", block_sparse=True,
+                     mask_pattern="local_global", note="window(1)+global(1) block-sparse attention")]
+
+
 def block_mask_density(mask: torch.Tensor) -> float:
     return float(mask.to(torch.float64).mean())
 
@@ -162,7 +187,10 @@ def make_inputs(w: Workload, seed: Optional[int] = None, with_grad_out: bool = T
     block_mask = None
     if w.block_sparse:
         nb = (w.N + BLOCK - 1) // BLOCK
-        block_mask = band_butterfly_block_mask(nb)
+        if w.mask_pattern == "local_global":
+            block_mask = local_global_block_mask(nb)
+        else:
+            block_mask = band_butterfly_block_mask(nb)
     return dict(q=q, k=k, v=v, do=do, kv_len=kv_len, block_mask=block_mask,
                 scale=w.softmax_scale, causal=w.causal, dropout_p=w.dropout_p,
                 seed=seed)
