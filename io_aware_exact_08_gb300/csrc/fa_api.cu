@@ -65,14 +65,12 @@ int from_cuda(cudaError_t e) {
     return FA_ERR_CUDA;
 }
 
-// The forward runs on tensor cores for d = 64, 128 and 256; the backward for
-// d = 64 and 128 (at d = 256 its dK and dV accumulators alone fill TMEM).
 bool use_tensor_cores(const Problem& p, bool backward) {
     if (g_kernel_path != 0 || (p.dtype != FA_BF16 && p.dtype != FA_FP16)) return false;
-    if (backward && p.d == 256) return false;
     // the tile lists of a block mask must fit in the kernels' shared memory
     const int tiles = (p.N + kMaskBlock - 1) / kMaskBlock;
-    if (p.block_mask && tiles > (p.d == 128 ? kMaskListCapBwd128 : kMaskListCap)) return false;
+    const int cap = p.d == 128 ? kMaskListCapBwd128 : (p.d == 256 && backward) ? kMaskListCapBwd256 : kMaskListCap;
+    if (p.block_mask && tiles > cap) return false;
     return true;
 }
 

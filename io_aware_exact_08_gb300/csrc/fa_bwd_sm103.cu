@@ -816,6 +816,7 @@ int launch_bwd_tc_d(const Problem& pr) {
 
 int launch_bwd_tc(const Problem& p) {
     if (!(p.scale > 0.f)) return launch_bwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    if (p.d == 256) return launch_bwd256_tc(p);
     if (p.dtype == FA_FP16) return p.d == 64 ? launch_bwd_tc_d<__half, 64>(p) : launch_bwd_tc_d<__half, 128>(p);
     if (p.dtype == FA_BF16)
         return p.d == 64 ? launch_bwd_tc_d<__nv_bfloat16, 64>(p) : launch_bwd_tc_d<__nv_bfloat16, 128>(p);

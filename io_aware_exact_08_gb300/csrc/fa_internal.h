@@ -48,10 +48,12 @@ constexpr int kMaxSplits = 64;
 constexpr int kMaskBlock = 128;
 // With a block mask the tensor-core kernels keep each CTA's list of visible
 // tiles in shared memory: at most kMaskListCap entries (kMaskListCapBwd128
-// in the d = 128 backward, whose shared memory is otherwise full). Larger
-// masks run on the CUDA-core kernels.
+// in the d = 128 backward and kMaskListCapBwd256 in the d = 256 backward,
+// whose shared memory is otherwise full). Larger masks run on the CUDA-core
+// kernels.
 constexpr int kMaskListCap = 1024;
 constexpr int kMaskListCapBwd128 = 256;
+constexpr int kMaskListCapBwd256 = 256;
 
 // Counts kernel launches for fa_launch_count (thread-safe).
 void note_launches(int n);
@@ -60,15 +62,17 @@ void note_launches(int n);
 // per device).
 int status_address(int** out);
 
-// CUDA-core kernels (any dtype, d in {64,128}); implemented in fa_simt.cu.
+// CUDA-core kernels (any dtype, d in {64,128,256}); implemented in fa_simt.cu.
 cudaError_t launch_fwd_simt(const Problem& p);
 cudaError_t launch_bwd_simt(const Problem& p);
 cudaError_t launch_bwd_preprocess(const Problem& p);
 cudaError_t launch_dropout_mask(uint8_t* keep, int B, int H, int N, uint32_t thr, uint64_t seed,
                                 cudaStream_t s);
 
-// tcgen05 kernels (bf16, d in {64,128}); implemented in fa_fwd_sm103.cu / fa_bwd_sm103.cu.
+// tcgen05 kernels (bf16, fp16): forward d in {64,128,256} (fa_fwd_sm103.cu),
+// backward d in {64,128} (fa_bwd_sm103.cu) and d = 256 (fa_bwd256_sm103.cu).
 int launch_fwd_tc(const Problem& p);
 int launch_bwd_tc(const Problem& p);
+int launch_bwd256_tc(const Problem& p);
 
 }  // namespace fa
