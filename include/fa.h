@@ -16,10 +16,10 @@
  *    lse = m + ln(l), which carries the same information as the pair (l, m)
  *    the pages keep for the backward pass.
  *  - d must be 64, 128 or 256. B, H >= 1, N >= 0 (N == 0 is a no-op).
- *    d = 256, the largest head dimension of the FlashAttention-2 section of
- *    "Penjelasan Flash Attention: Panduan Komprehensif" ("Dukungan untuk
- *    dimensi head yang lebih besar"), runs on the CUDA-core kernels for
- *    every dtype.
+ *    d = 256 is the largest head dimension of the FlashAttention-2 section
+ *    of "Penjelasan Flash Attention: Panduan Komprehensif" ("Dukungan untuk
+ *    dimensi head yang lebih besar"); its backward runs in three passes
+ *    (dV, dK, dQ) on the tensor cores for 16-bit inputs.
  *  - Masks combine by AND: causal (key j > query i is masked, top-left
  *    aligned), key padding (j >= kv_len[b] masked; kv_len is int32[B] in
  *    device memory, or NULL), block mask (block_mask[(i/128)*nb + j/128] == 0

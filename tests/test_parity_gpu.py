@@ -57,8 +57,8 @@ def test_parity_default_path(cuda_device, case, dtype):
     compare(got, ref, dtype)
 
 
-# head dim 256 (forward on the one-tile tensor-core kernel for 16-bit inputs,
-# backward on the CUDA cores)
+# head dim 256 (16-bit inputs: the one-tile tensor-core forward and the
+# three-pass tensor-core backward; fp32: the CUDA-core kernels)
 CASES_D256 = [
     (1, 256, False, False, False, 0.0),
     (129, 256, True, False, False, 0.0),
