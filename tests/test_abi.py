@@ -71,6 +71,29 @@ def test_forward_argument_errors(kw, expect):
     assert fa.fa_fwd(**args) == expect
 
 
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dtype=3), -2), (dict(d=512), -2), (dict(d=256, B=0), -1), (dict(d=256, o=FAKE + 8), -1),
+    (dict(d=256, dropout_p=1.5), -1), (dict(d=256, q=None), -1),
+])
+def test_forward_argument_errors_fp16_and_d256(kw, expect):
+    """fp16 inputs and head dim 256 go through the same host-side checks."""
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=16, d=64, scale=0.125, causal=0,
+                block_mask=None, dropout_p=0.0, seed=0, dtype=fa.FA_FP16, kv_len=None, stream=None)
+    args.update(kw)
+    assert fa.fa_fwd(**args) == expect
+
+
+def test_dtype_codes_match_the_header():
+    torch = pytest.importorskip("torch")
+    assert (fa.FA_BF16, fa.FA_FP32, fa.FA_FP16) == (0, 1, 2)
+    header = open(os.path.join(os.path.dirname(__file__), "..", "include", "fa.h")).read()
+    assert "FA_BF16 = 0, FA_FP32 = 1, FA_FP16 = 2" in header
+    assert fa._dtype_code(torch.empty(1, dtype=torch.float16)) == fa.FA_FP16
+    assert fa._dtype_code(torch.empty(1, dtype=torch.bfloat16)) == fa.FA_BF16
+    with pytest.raises(TypeError):
+        fa._dtype_code(torch.empty(1, dtype=torch.float64))
+
+
 def test_zero_length_is_a_noop():
     assert fa.fa_fwd(None, None, None, None, None, 1, 1, 0, 64, 0.1, 0, None, 0.0, 0, fa.FA_BF16, None, None) == 0
 

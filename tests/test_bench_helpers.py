@@ -32,3 +32,20 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
 def test_source_hash_tracks_kernel_files():
     h1 = bench.kernel_source_hash()
     assert len(h1) == 64 and h1 == bench.kernel_source_hash()
+
+
+def test_traffic_key_separates_dtype_and_splits():
+    w = WORKLOADS["long_causal"]
+    assert bench.traffic_key(w) == "long_causal"
+    assert bench.traffic_key(w.with_(dtype="fp16")) == "long_causal/fp16"
+    assert bench.traffic_key(w, 2) == "long_causal/splits=2"
+    assert bench.traffic_key(w.with_(dtype="fp16"), 4) == "long_causal/fp16/splits=4"
+
+
+def test_byte_model_uses_the_element_size():
+    w = WORKLOADS["gpt2_causal"]
+    f16, b16 = bench.algorithmic_bytes(w.with_(dtype="fp16"))
+    assert (f16, b16) == bench.algorithmic_bytes(w)  # bf16 and fp16 are both 2 bytes
+    f32, _ = bench.algorithmic_bytes(w.with_(dtype="fp32"))
+    bhn = w.B * w.H * w.N
+    assert f32 - f16 == 4 * bhn * w.d * (4 - 2)
