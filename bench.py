@@ -103,6 +103,16 @@ def traffic_key(w, splits=1):
     return key
 
 
+def workload_config(w, density, splits, ws):
+    """The `config` object of a bench line: the workload and the step, the
+    same for the library arm and the reference arm."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype, "causal": w.causal,
+            "dropout_p": w.dropout_p, "kv_len_range": w.kv_len_range, "block_density": round(density, 5),
+            "scale": w.softmax_scale,
+            "step": "fa_fwd + fa_bwd" if splits == 1 else f"fa_fwd_splitkv ({splits} splits) + fa_bwd",
+            "l2": "flushed before every timed step", "parallelism": f"replicas x{ws}"}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -386,11 +396,7 @@ def run_fa(args, w, ws, rank, device):
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
-                   "dropout_p": w.dropout_p, "kv_len_range": w.kv_len_range, "block_density": round(dens, 5),
-                   "scale": scale, "step": "fa_fwd + fa_bwd" if splits == 1 else f"fa_fwd_splitkv ({splits} splits) + fa_bwd",
-                   "l2": "flushed before every timed step",
-                   "parallelism": f"replicas x{ws}"},
+        "config": workload_config(w, dens, splits, ws),
         "fwd_tflops": round(fwd_tflops, 3), "bwd_tflops": round(bwd_tflops, 3),
         "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
         "frac_of_bf16_peak": round(value / ws / peaks["bf16"], 4) if sixteen else None,
@@ -428,7 +434,7 @@ def run_reference(args, w, ws, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "config": workload_config(w, dens, max(1, int(getattr(args, "splits", 1))), ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
                          "sample": "; ".join(samples[:3])},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
