@@ -1,9 +1,10 @@
 """Exact IO-aware attention for GB300 (sm_103a): Python binding.
 
 A thin ctypes layer over the C ABI in ``include/fa.h`` (``libfa_gb300.so``,
-built in-tree by ``build.py``). The functions ``fa_fwd``, ``fa_bwd``,
-``fa_bwd_workspace_size``, ``fa_dropout_mask``, ``fa_check_device_status``,
-``fa_status_string`` and ``fa_set_kernel_path`` take the same arguments as
+built in-tree by ``build.py``). The functions ``fa_fwd``, ``fa_fwd_splitkv``,
+``fa_fwd_splitkv_workspace_size``, ``fa_bwd``, ``fa_bwd_workspace_size``,
+``fa_dropout_mask``, ``fa_check_device_status``, ``fa_status_string`` and
+``fa_set_kernel_path`` take the same arguments as
 their C counterparts (device pointers as integers, sizes, a stream handle)
 and only marshal them. ``attention_fwd`` / ``attention_bwd`` and
 ``FlashAttention`` add the tensor plumbing: PyTorch allocates the outputs
@@ -20,8 +21,8 @@ import os
 import threading
 
 __all__ = [
-    "FA_BF16", "FA_FP32", "FaError", "load_library", "library_path",
-    "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
+    "FA_BF16", "FA_FP32", "FA_FP16", "FaError", "load_library", "library_path",
+    "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
     "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
     "fa_bwd_noalloc", "FA_BWD_NOALLOC_SCRATCH_BYTES", "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
 ]
