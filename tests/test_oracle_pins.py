@@ -268,7 +268,8 @@ def test_rowsum_identity_for_backward_preprocess():
 
 @pytest.mark.parametrize("N,d,causal,kv,blocky", [
     (33, 8, False, None, False), (64, 16, True, None, False),
-    (50, 8, False, 31, False), (40, 8, True, None, True), (48, 4, False, 29, True)])
+    (50, 8, False, 31, False), (40, 8, True, None, True), (48, 4, False, 29, True),
+    (20, 256, True, None, False), (24, 128, False, 17, True)])
 def test_matches_torch_fp64_sdpa(N, d, causal, kv, blocky):
     B, H, block = 2, 3, 8
     q, k, v, do = (torch.from_numpy(_rand((B, H, N, d), s)) for s in (41, 42, 43, 44))
