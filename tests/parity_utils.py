@@ -93,21 +93,56 @@ def max_err(got, ref, heads=None, H=None, allowance=None):
     return float(np.max(d))
 
 
-def compare(got, ref, dtype, keys=("o", "lse", "dq", "dk", "dv"), heads=None):
-    """Checks every output against its tolerance.
+def _select(got, ref, heads):
+    if heads is None:
+        return got, ref
+    g = got.reshape((-1,) + got.shape[2:])[list(heads)]
+    r = ref.reshape((-1,) + ref.shape[2:])[list(heads)]
+    return g, r
 
-    O, dQ, dK, dV are stored in the input dtype; bf16 storage alone is off by
-    up to half an ulp (0.0156 for |x| in [4, 8)), so the tolerance applies to
-    the error beyond that rounding. LSE is fp32 and is compared as is. The
-    raw max-abs errors are returned too (key + "_raw").
+
+def compare(got, ref, dtype, keys=("o", "lse", "dq", "dk", "dv"), heads=None):
+    """Checks every output against its tolerance, on the raw error first.
+
+    O, dQ, dK, dV are stored in the input dtype. Where half an ulp of the
+    stored type at the reference value is at most a quarter of the bar
+    (bf16: |O| < 1 and gradients below 2 in magnitude; fp16: |x| < 2), the
+    raw max-abs error must be within the bar. Only the remaining entries,
+    where the storage rounding alone is a sizeable part of the bar (large
+    values of early causal rows, or scaled by dropout's 1/(1-p)), are
+    compared after that rounding is taken off; they are counted
+    (key + "_n_allow"). LSE is fp32 and is always compared raw. Returned: per key the error used for the
+    check, the raw max-abs error over all entries (key + "_raw") and the
+    count of entries that needed the rounding allowance.
     """
     tol = TOL[dtype]
     errs = {}
+    bad = {}
     for key in keys:
-        if key in ref:
-            allow = None if key == "lse" else dtype
-            errs[key] = max_err(got[key], ref[key], heads, allowance=allow)
-            errs[key + "_raw"] = max_err(got[key], ref[key], heads)
-    bad = {k: (e, tol[k]) for k, e in errs.items() if k in tol and not e <= tol[k]}
+        if key not in ref:
+            continue
+        t = tol[key]
+        raw = max_err(got[key], ref[key], heads)
+        errs[key + "_raw"] = raw
+        if key == "lse" or dtype == "fp32":
+            errs[key] = raw
+            errs[key + "_n_allow"] = 0
+            if not raw <= t:
+                bad[key] = (raw, t)
+            continue
+        g, r = _select(got[key], ref[key], heads)
+        hu = half_ulp(r, dtype)
+        strict = hu <= t / 4
+        d = np.abs(g - r)
+        strict_err = float(d[strict].max()) if strict.any() else 0.0
+        loose = ~strict
+        allow_err = float(np.maximum(d[loose] - hu[loose], 0.0).max()) if loose.any() else 0.0
+        errs[key] = max(strict_err, allow_err)
+        errs[key + "_strict"] = strict_err
+        errs[key + "_n_allow"] = int(loose.sum())
+        if not strict_err <= t:
+            bad[key + "_strict"] = (strict_err, t)
+        if not allow_err <= t:
+            bad[key + "_allow"] = (allow_err, t)
     assert not bad, f"tolerance exceeded: {bad} (all errors: {errs})"
     return errs
