@@ -6,8 +6,9 @@ One step = one forward and one backward over one batch of the workload
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl fa|reference] [--no-cpu-baseline]
 
-Default workload: the GPT-2-small-shaped causal attention (B=8 H=12 N=1024
-d=64, bf16). Metric: TFLOP/s with FLOPs = 4*B*H*N^2*d for the forward and
+Default workload: long-context dense causal attention (B=2 H=16 N=8192
+d=128, bf16), the largest configuration and one the N >= 4K throughput
+target applies to; --workload selects any other. Metric: TFLOP/s with FLOPs = 4*B*H*N^2*d for the forward and
 2.5x that for the backward, halved for causal and scaled by the block
 density for block-sparse masks (the literal formula; key padding counts the
 dense N^2). For N > 1 GPUs (torchrun), every rank runs the same workload on
@@ -62,6 +63,25 @@ def algorithmic_bytes(w):
     return 4 * bhnd * e + 4 * bhn, 8 * bhnd * e + 8 * bhn
 
 
+def bwd_main_bytes(w):
+    """Algorithmic bytes of the backward's main kernel: read Q, K, V, dO,
+    LSE and rowsum(dO o O); write dQ, dK, dV."""
+    e = 2 if w.dtype in ("bf16", "fp16") else 4
+    bhnd = w.B * w.H * w.N * w.d
+    bhn = w.B * w.H * w.N
+    return 7 * bhnd * e + 8 * bhn
+
+
+def main_kernel_names(w, splits=1):
+    """(forward, backward) main kernels of a workload's calls, as the events
+    of fa_set_main_kernel_events bracket them."""
+    if w.dtype not in ("bf16", "fp16"):
+        return "fwd_simt_kernel", "bwd_simt_kernels"
+    fwd = "fwd_d256_kernel" if w.d == 256 else "fwd_pp_kernel"
+    bwd = "bwd256_kernel (3 passes)" if w.d == 256 else "bwd_tc_kernel"
+    return fwd, bwd
+
+
 def kernel_source_hash():
     """SHA-256 over the CUDA sources of the library (file names and bytes)."""
     import hashlib
@@ -74,17 +94,17 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
-def recorded_traffic(workload, call):
-    """DRAM bytes (read + write) of one `call` ("fa_fwd" or "fa_bwd") on
-    `workload`, as ncu counted them in the capture recorded under profiles/,
-    or None when there is no record or the kernel sources have changed since."""
+def recorded_traffic(workload, kernel):
+    """DRAM bytes (read + write) of one launch of `kernel` on `workload`, as
+    ncu counted them in the capture recorded under profiles/, or None when
+    there is no record or the kernel sources have changed since."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    ent = rec.get("calls", {}).get(workload, {}).get(call)
+    ent = rec.get("kernels", {}).get(workload, {}).get(kernel)
     if not ent or rec.get("source_sha256") != kernel_source_hash():
         return None
     return int(ent["dram_bytes"])
@@ -227,29 +247,57 @@ def barrier(device=None):
 # CPU baseline: the oracle, as it stands, on a bounded sample of heads
 # ---------------------------------------------------------------------------
 
+def cpu_model():
+    """Model name of the host CPU (lscpu, else /proc/cpuinfo, else the ISA)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def oracle_heads_for(w, inp, budget_s, backward=True):
+    """How many whole heads of the workload the oracle runs in about
+    budget_s seconds (at least one), from one timed head."""
+    t1 = oracle_run(w, inp, [0], backward)
+    return max(1, min(w.B * w.H, int(budget_s / max(t1, 1e-6))))
+
+
+def oracle_run(w, inp, heads, backward=True):
+    """Wall time of the fp64 oracle on `heads` (forward, and backward)."""
+    import oracle
+    kw = dict(causal=w.causal, block_mask=inp["block_mask"], block=128, kv_len=inp["kv_len"],
+              dropout_p=w.dropout_p, seed=inp["seed"])
+    q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q, k, v, w.softmax_scale, heads=heads, **kw)
+    if backward:
+        oracle.attention_bwd(q, k, v, do, w.softmax_scale, heads=heads, **kw)
+    return time.perf_counter() - t0
+
+
 def oracle_sample(w, inp, budget_s=12.0, backward=True):
     """Times the fp64 oracle on whole heads of the workload (fwd+bwd)."""
     import oracle
     total_heads = w.B * w.H
     fwd_f, bwd_f = flops(w, density_of(inp, w))
     per_head = (fwd_f + (bwd_f if backward else 0.0)) / total_heads
-    kw = dict(causal=w.causal, block_mask=inp["block_mask"], block=128, kv_len=inp["kv_len"],
-              dropout_p=w.dropout_p, seed=inp["seed"])
-    q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
-
-    def run(heads):
-        t0 = time.perf_counter()
-        oracle.attention_fwd(q, k, v, w.softmax_scale, heads=heads, **kw)
-        if backward:
-            oracle.attention_bwd(q, k, v, do, w.softmax_scale, heads=heads, **kw)
-        return time.perf_counter() - t0
-
-    t1 = run([0])
-    n = max(1, min(total_heads, int(budget_s / max(t1, 1e-6))))
-    heads = list(range(n))
-    t = run(heads) if n > 1 else t1
+    n = oracle_heads_for(w, inp, budget_s, backward)
+    t = oracle_run(w, inp, list(range(n)), backward)
     value = per_head * n / t / 1e12
-    return {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+    return {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "cpu_model": cpu_model(),
+            "kind": "oracle",
             "sample": f"{n} of {total_heads} heads, fp64 {'fwd+bwd' if backward else 'fwd'}, {t:.2f} s"}
 
 
@@ -360,17 +408,40 @@ def run_fa(args, w, ws, rank, device):
     torch.cuda.synchronize(device)
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / e2e_steps, device)
 
+    # the main kernel of each call, timed on its own in a second pass of K
+    # steps (same L2 flush): the library records the events right around its
+    # launch (fa_set_main_kernel_events), so the backward's preprocess and dQ
+    # conversion are outside them
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for e in sum(kev, []):
+        e.record(stream)  # torch reads elapsed times only of events it has seen recorded
+    barrier(device)
+    torch.cuda.synchronize(device)
+    for i in range(args.steps):
+        flush.zero_()
+        fa.fa_set_main_kernel_events(kev[i][0].cuda_event, kev[i][1].cuda_event)
+        fwd()
+        fa.fa_set_main_kernel_events(kev[i][2].cuda_event, kev[i][3].cuda_event)
+        bwd()
+        fa.fa_set_main_kernel_events(None, None)
+    torch.cuda.synchronize(device)
+    fwd_k_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in kev) / args.steps, device)
+    bwd_k_ms = max_over_ranks(sum(e[2].elapsed_time(e[3]) for e in kev) / args.steps, device)
+
     total_f = (fwd_f + bwd_f) * ws
     e2e_value = total_f / (e2e_ms * 1e-3) / 1e12
     fwd_tflops = fwd_f * ws / (fwd_avg * 1e-3) / 1e12
     bwd_tflops = bwd_f * ws / (bwd_avg * 1e-3) / 1e12
     peaks = load_peaks()
-    # dominant call of the step; the forward is one kernel launch, the
-    # backward call is three (preprocess, main, dq convert)
-    dominant = "fa_bwd" if bwd_avg >= fwd_avg else "fa_fwd"
-    dom_ms = bwd_avg if dominant == "fa_bwd" else fwd_avg
-    dom_f = bwd_f if dominant == "fa_bwd" else fwd_f
-    dom_b = bwd_b if dominant == "fa_bwd" else fwd_b
+    # dominant kernel of the step: the forward kernel, or the backward's main
+    # kernel (all of the backward's FLOPs; its algorithmic bytes are those of
+    # the call minus the O read that the preprocess does)
+    names = main_kernel_names(w, splits)
+    fwd_is_dom = fwd_k_ms > bwd_k_ms
+    dom_name = names[0] if fwd_is_dom else names[1]
+    dom_ms = fwd_k_ms if fwd_is_dom else bwd_k_ms
+    dom_f = fwd_f if fwd_is_dom else bwd_f
+    dom_b = fwd_b if fwd_is_dom else bwd_main_bytes(w)
     tensor_ach = dom_f / (dom_ms * 1e-3) / 1e12
     hbm_ach = dom_b / (dom_ms * 1e-3) / 1e9
     # fp16 and bf16 share the dense tensor rate (2.25 PFLOP/s nominal each), so
@@ -386,11 +457,12 @@ def run_fa(args, w, ws, rank, device):
                 "frac": round(hbm_frac, 4)}
     else:
         roof = {"bound": "alu", "achieved": round(tensor_ach, 3), "peak": None, "unit": "TFLOP/s", "frac": None}
-    roof.update({"kernel": dominant,
-                 "traffic": recorded_traffic(traffic_key(w, splits), dominant),
+    roof.update({"kernel": dom_name,
+                 "traffic": recorded_traffic(traffic_key(w, splits), dom_name),
                  "peak_source": peaks["source"] + " (burst)" + (", bf16 peak x 1 for fp16" if w.dtype == "fp16" else ""),
                  "tensor_frac": round(tensor_frac, 4), "hbm_frac": round(hbm_frac, 4),
-                 "algorithmic_flops": dom_f, "algorithmic_bytes": dom_b, "avg_ms": round(dom_ms, 4)})
+                 "algorithmic_flops": dom_f, "algorithmic_bytes": dom_b, "kernel_avg_ms": round(dom_ms, 4),
+                 "kernel_ms": {names[0]: round(fwd_k_ms, 4), names[1]: round(bwd_k_ms, 4)}})
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -412,31 +484,36 @@ def run_fa(args, w, ws, rank, device):
 
 
 def run_reference(args, w, ws, rank):
-    """The oracle (fp64, host cores) timed on a bounded sample of the workload."""
+    """The oracle (fp64, host cores) as the reference arm: each step runs it
+    on the same fixed sample of whole heads of the workload, and the step's
+    wall time is measured (nothing is extrapolated)."""
     from workloads import make_inputs
     if rank != 0:
         return None
-    inp = make_inputs(w)
-    vals = []
-    samples = []
-    for _ in range(args.warmup):
-        oracle_sample(w, inp, budget_s=1.0)
-    for _ in range(args.steps):
-        r = oracle_sample(w, inp, budget_s=args.cpu_budget / max(1, args.steps))
-        vals.append(r["value"])
-        samples.append(r["sample"])
-    value = statistics.mean(vals)
     import oracle
+    inp = make_inputs(w)
     dens = density_of(inp, w)
     fwd_f, bwd_f = flops(w, dens)
-    ms = (fwd_f + bwd_f) / (value * 1e12) * 1e3
+    total_heads = w.B * w.H
+    # sample size: whole heads filling about cpu_budget / steps seconds per step
+    n = oracle_heads_for(w, inp, args.cpu_budget / max(1, args.steps))
+    heads = list(range(n))
+    for _ in range(args.warmup):
+        oracle_run(w, inp, [0])
+    times = [oracle_run(w, inp, heads) for _ in range(args.steps)]
+    step_s = sum(times) / len(times)
+    sample_f = (fwd_f + bwd_f) * n / total_heads
+    value = sample_f / step_s / 1e12
+    sample = f"{n} of {total_heads} heads per step, fp64 fwd+bwd"
+    cfg = workload_config(w, dens, max(1, int(getattr(args, "splits", 1))), ws)
+    cfg["sample"] = sample
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, dens, max(1, int(getattr(args, "splits", 1))), ws),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-                         "sample": "; ".join(samples[:3])},
+        "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "cpu_model": cpu_model(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -446,7 +523,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="gpt2_causal")
+    ap.add_argument("--workload", default="long_causal")
     ap.add_argument("--impl", default="fa", choices=["fa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)

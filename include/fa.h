@@ -37,8 +37,15 @@
  *    (clamped to 2^32 - 1). It is independent of tiling, so the forward,
  *    the backward and fa_dropout_mask agree bit for bit.
  *  - stream is a cudaStream_t (NULL = the legacy default stream). Calls are
- *    asynchronous on it; the library allocates no device memory and
- *    synchronises nothing except fa_check_device_status.
+ *    asynchronous on it and synchronise nothing except
+ *    fa_check_device_status. The library allocates no device memory per
+ *    call; the only device memory it holds is static: a status word of two
+ *    ints and the fixed FA_BWD_NOALLOC_SCRATCH_BYTES (32 MiB) array of
+ *    fa_bwd_noalloc, present on every GPU that loads the library.
+ *  - The device addresses of those two static objects are looked up once
+ *    per device and cached for the life of the process, so resetting a
+ *    device (cudaDeviceReset, or a reset of its primary context) while the
+ *    library is in use is not supported.
  *  - Every call returns FA_OK (0) or a negative fa_status. Argument errors
  *    are detected on the host before any launch; nothing is thrown across
  *    the ABI. Device-side bounded waits that run out set a status word that
@@ -62,7 +69,8 @@ typedef enum { FA_BF16 = 0, FA_FP32 = 1, FA_FP16 = 2 } fa_dtype;
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = -1,   /* null pointer, negative size, p outside [0,1), misalignment */
-    FA_ERR_UNSUPPORTED = -2,   /* d not in {64,128,256}, unknown dtype */
+    FA_ERR_UNSUPPORTED = -2,   /* d not in {64,128,256}, unknown dtype, or a 16-bit problem the
+                                  tensor-core kernels do not take (see fa_fwd) */
     FA_ERR_CUDA = -3,          /* a CUDA runtime call failed (launch, attribute, symbol) */
     FA_ERR_WORKSPACE = -4,     /* workspace missing or smaller than fa_bwd_workspace_size */
     FA_ERR_DEVICE_TIMEOUT = -5 /* a device-side bounded wait ran out (see fa_check_device_status) */
@@ -74,6 +82,13 @@ typedef enum {
  * Inputs q, k, v; outputs o (dtype) and lse (fp32). All device pointers,
  * owned by the caller. bf16 and fp16 run on the tcgen05 tensor-core kernel;
  * fp32 on an fp32 CUDA-core kernel.
+ * 16-bit problems the tensor-core kernels do not take are refused with
+ * FA_ERR_UNSUPPORTED before any launch, not run on the (far slower)
+ * CUDA-core kernels: scale <= 0, or a block mask with more than 1024 key
+ * tiles per row (N > 131072). The backward's limit on block masks is 1024
+ * tiles at d = 64 and 256 tiles (N <= 32768) at d = 128 and 256. Callers who
+ * want the CUDA-core kernels for such a problem select them explicitly with
+ * fa_set_kernel_path(1).
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal,
@@ -191,6 +206,20 @@ int fa_test_wait_timeout(uint64_t limit_ns, void* stream);
  * calling process (all devices, all entry points).
  */
 uint64_t fa_launch_count(void);
+
+/*
+ * Diagnostic timing of a call's main kernel. While set, every fa_fwd,
+ * fa_fwd_splitkv and fa_bwd call records ev_start (a cudaEvent_t) on its
+ * stream immediately before launching its main kernel (the forward kernel;
+ * the backward's tile kernel, or its three d = 256 passes; the CUDA-core
+ * kernels) and ev_stop immediately after, so that cudaEventElapsedTime gives
+ * that kernel's duration without the backward's preprocess and dQ
+ * conversion. An event between two launches ends their programmatic
+ * overlap, so set the events only for timing runs. Both NULL turns it off;
+ * exactly one NULL returns FA_ERR_INVALID_ARG. Process-wide, not
+ * thread-safe; the events stay owned by the caller.
+ */
+int fa_set_main_kernel_events(void* ev_start, void* ev_stop);
 
 #ifdef __cplusplus
 }

@@ -24,7 +24,7 @@ __all__ = [
     "FA_BF16", "FA_FP32", "FA_FP16", "FaError", "load_library", "library_path",
     "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
     "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
-    "fa_bwd_noalloc", "FA_BWD_NOALLOC_SCRATCH_BYTES", "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
+    "fa_set_main_kernel_events", "fa_bwd_noalloc", "FA_BWD_NOALLOC_SCRATCH_BYTES", "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
 ]
 
 FA_BF16 = 0
@@ -38,7 +38,8 @@ _lock = threading.Lock()
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
             "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
-            "fa_bwd_noalloc", "fa_test_wait_timeout", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size")
+            "fa_bwd_noalloc", "fa_test_wait_timeout", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size",
+            "fa_set_main_kernel_events")
 
 # Size of the fixed device array fa_bwd_noalloc takes its workspace from.
 FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -89,6 +90,8 @@ def load_library(build_if_missing: bool = True):
         lib.fa_bwd_noalloc.restype = I
         lib.fa_test_wait_timeout.argtypes = [U64, P]
         lib.fa_test_wait_timeout.restype = I
+        lib.fa_set_main_kernel_events.argtypes = [P, P]
+        lib.fa_set_main_kernel_events.restype = I
         lib.fa_launch_count.argtypes = []
         lib.fa_launch_count.restype = ctypes.c_uint64
         _lib = lib
@@ -163,6 +166,12 @@ def fa_test_wait_timeout(limit_ns, stream):
 
 def fa_launch_count():
     return int(load_library().fa_launch_count())
+
+
+def fa_set_main_kernel_events(ev_start, ev_stop):
+    """Events (cudaEvent_t handles as integers, or None) recorded around the
+    main kernel of the following calls; see include/fa.h."""
+    return load_library().fa_set_main_kernel_events(ev_start, ev_stop)
 
 
 # ---------------------------------------------------------------------------

@@ -18,6 +18,9 @@ __device__ int g_status[2];
 
 int g_kernel_path = 0;  // 0 = default, 1 = CUDA-core kernels only
 std::atomic<uint64_t> g_launches{0};
+// fa_set_main_kernel_events: events recorded around the next calls' main
+// kernels (null = off)
+cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -65,18 +68,40 @@ int from_cuda(cudaError_t e) {
     return FA_ERR_CUDA;
 }
 
-bool use_tensor_cores(const Problem& p, bool backward) {
-    if (g_kernel_path != 0 || (p.dtype != FA_BF16 && p.dtype != FA_FP16)) return false;
-    // the tile lists of a block mask must fit in the kernels' shared memory
-    const int tiles = (p.N + kMaskBlock - 1) / kMaskBlock;
-    const int cap = p.d == 128 ? kMaskListCapBwd128 : (p.d == 256 && backward) ? kMaskListCapBwd256 : kMaskListCap;
-    if (p.block_mask && tiles > cap) return false;
-    return true;
+// Which kernels serve a problem. 16-bit inputs run on the tensor-core
+// kernels and fp32 on the CUDA-core kernels (or every dtype, when the caller
+// forced them with fa_set_kernel_path(1)). A 16-bit problem the tensor-core
+// kernels do not take is refused with FA_ERR_UNSUPPORTED rather than sent to
+// the far slower CUDA-core kernels behind the caller's back: scale <= 0
+// (their online softmax takes the running maximum of the unscaled scores), or
+// a block mask with more key tiles per row (query tiles per column in the
+// backward) than their shared-memory tile lists hold.
+int pick_path(const Problem& p, bool backward, bool* tensor_cores) {
+    *tensor_cores = false;
+    if (g_kernel_path != 0 || (p.dtype != FA_BF16 && p.dtype != FA_FP16)) return FA_OK;
+    if (!(p.scale > 0.f)) return FA_ERR_UNSUPPORTED;
+    if (p.block_mask) {
+        const int tiles = (p.N + kMaskBlock - 1) / kMaskBlock;
+        const int cap = !backward ? kMaskListCap
+                        : p.d == 64 ? kMaskListCap
+                        : p.d == 128 ? kMaskListCapBwd128 : kMaskListCapBwd256;
+        if (tiles > cap) return FA_ERR_UNSUPPORTED;
+    }
+    *tensor_cores = true;
+    return FA_OK;
 }
 
 }  // namespace
 
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+void record_main_start(cudaStream_t s) {
+    if (g_main_start) cudaEventRecord(g_main_start, s);
+}
+
+void record_main_stop(cudaStream_t s) {
+    if (g_main_stop) cudaEventRecord(g_main_stop, s);
+}
 
 int status_address(int** out) {
     int dev = 0;
@@ -116,10 +141,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     p.v = v;
     p.o = o;
     p.lse = lse;
+    bool tc = false;
+    rc = pick_path(p, false, &tc);
+    if (rc != FA_OK) return rc;
     rc = status_address(&p.status);
     if (rc != FA_OK) return rc;
-    if (use_tensor_cores(p, false)) return launch_fwd_tc(p);
-    return from_cuda(launch_fwd_simt(p));
+    if (tc) return launch_fwd_tc(p);
+    record_main_start(p.stream);
+    rc = from_cuda(launch_fwd_simt(p));
+    record_main_stop(p.stream);
+    return rc;
 }
 
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int n_splits) {
@@ -148,13 +179,19 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
     p.v = v;
     p.o = o;
     p.lse = lse;
+    bool tc = false;
+    rc = pick_path(p, false, &tc);
+    if (rc != FA_OK) return rc;
     rc = status_address(&p.status);
     if (rc != FA_OK) return rc;
-    // one split, the CUDA-core kernels or a non-positive scale: the plain
-    // forward computes the same result
-    if (n_splits == 1 || !use_tensor_cores(p, false) || !(scale > 0.f)) {
-        if (use_tensor_cores(p, false)) return launch_fwd_tc(p);
-        return from_cuda(launch_fwd_simt(p));
+    // one split, or the CUDA-core kernels: the plain forward computes the
+    // same result
+    if (n_splits == 1 || !tc) {
+        if (tc) return launch_fwd_tc(p);
+        record_main_start(p.stream);
+        rc = from_cuda(launch_fwd_simt(p));
+        record_main_stop(p.stream);
+        return rc;
     }
     const size_t rows = (size_t)B * H * N;
     p.n_splits = n_splits;
@@ -196,10 +233,16 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     const size_t rows = (size_t)B * H * N;
     p.delta = static_cast<float*>(workspace);
     p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)));
+    bool tc = false;
+    rc = pick_path(p, true, &tc);
+    if (rc != FA_OK) return rc;
     rc = status_address(&p.status);
     if (rc != FA_OK) return rc;
-    if (use_tensor_cores(p, true)) return launch_bwd_tc(p);
-    return from_cuda(launch_bwd_simt(p));
+    if (tc) return launch_bwd_tc(p);
+    record_main_start(p.stream);
+    rc = from_cuda(launch_bwd_simt(p));
+    record_main_stop(p.stream);
+    return rc;
 }
 
 int fa_dropout_mask(uint8_t* keep, int B, int H, int N, float p, uint64_t seed, void* stream) {
@@ -234,6 +277,13 @@ const char* fa_status_string(int status) {
 }
 
 uint64_t fa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int fa_set_main_kernel_events(void* ev_start, void* ev_stop) {
+    if ((ev_start == nullptr) != (ev_stop == nullptr)) return FA_ERR_INVALID_ARG;
+    g_main_start = static_cast<cudaEvent_t>(ev_start);
+    g_main_stop = static_cast<cudaEvent_t>(ev_stop);
+    return FA_OK;
+}
 
 int fa_set_kernel_path(int path) {
     const int old = g_kernel_path;

@@ -502,9 +502,11 @@ int launch_bwd256_t(const Problem& pr) {
         return FA_ERR_CUDA;
     // delta_i = sum_c dO_ic O_ic, then the three passes
     if (launch_bwd_preprocess(pr) != cudaSuccess) return FA_ERR_CUDA;
+    record_main_start(pr.stream);
     int rc = launch_pass<T, kDV, kMask>(pr, tk, tk, tq, tdo, pr.dv);
     if (rc == FA_OK) rc = launch_pass<T, kDK, kMask>(pr, tk, tv, tq, tdo, pr.dk);
     if (rc == FA_OK) rc = launch_pass<T, kDQ, kMask>(pr, tq, tdo, tk, tv, pr.dq);
+    record_main_stop(pr.stream);
     return rc;
 }
 

@@ -795,8 +795,10 @@ int launch_bwd_tc_d(const Problem& pr) {
     cfg.gridDim = dim3(BH, (pr.N + kTile - 1) / kTile);
     cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr);
+    record_main_start(pr.stream);
     cudaError_t e = pr.block_mask ? cudaLaunchKernelEx(&cfg, bwd_tc_kernel<T, D, true>, tq, tk, tv, tdo, p)
                                   : cudaLaunchKernelEx(&cfg, bwd_tc_kernel<T, D, false>, tq, tk, tv, tdo, p);
+    record_main_stop(pr.stream);
     note_launches(1);
     if (e != cudaSuccess) {
         if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: bwd_tc launch: %s\n", cudaGetErrorString(e));
@@ -815,7 +817,12 @@ int launch_bwd_tc_d(const Problem& pr) {
 }  // namespace
 
 int launch_bwd_tc(const Problem& p) {
-    if (!(p.scale > 0.f)) return launch_bwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    if (!(p.scale > 0.f)) {
+        record_main_start(p.stream);
+        const cudaError_t e = launch_bwd_simt(p);
+        record_main_stop(p.stream);
+        return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    }
     if (p.d == 256) return launch_bwd256_tc(p);
     if (p.dtype == FA_FP16) return p.d == 64 ? launch_bwd_tc_d<__half, 64>(p) : launch_bwd_tc_d<__half, 128>(p);
     if (p.dtype == FA_BF16)

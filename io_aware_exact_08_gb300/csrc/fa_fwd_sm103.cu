@@ -1186,7 +1186,9 @@ int launch_fwd_tc_d(const Problem& pr) {
     cfg.stream = pr.stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
+    record_main_start(pr.stream);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
+    record_main_stop(pr.stream);
     note_launches(1);
     if (e != cudaSuccess) {
         if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: fwd_tc launch: %s\n", cudaGetErrorString(e));
@@ -1225,7 +1227,9 @@ int launch_fwd256(const Problem& pr) {
     cfg.stream = pr.stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
+    record_main_start(pr.stream);
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
+    record_main_stop(pr.stream);
     note_launches(1);
     if (e != cudaSuccess) {
         if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: fwd_d256 launch: %s\n", cudaGetErrorString(e));
@@ -1254,7 +1258,12 @@ int launch_fwd_tc_t(const Problem& p) {
 }
 
 int launch_fwd_tc(const Problem& p) {
-    if (!(p.scale > 0.f)) return launch_fwd_simt(p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    if (!(p.scale > 0.f)) {
+        record_main_start(p.stream);
+        const cudaError_t e = launch_fwd_simt(p);
+        record_main_stop(p.stream);
+        return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    }
     if (p.dtype == FA_FP16) return launch_fwd_tc_t<__half>(p);
     if (p.dtype == FA_BF16) return launch_fwd_tc_t<__nv_bfloat16>(p);
     return FA_ERR_UNSUPPORTED;

@@ -58,6 +58,12 @@ constexpr int kMaskListCapBwd256 = 256;
 // Counts kernel launches for fa_launch_count (thread-safe).
 void note_launches(int n);
 
+// Diagnostic timing (fa_set_main_kernel_events): record the caller's events
+// on `s` right before and right after the launch(es) of a call's main
+// kernel; no-ops while no events are set.
+void record_main_start(cudaStream_t s);
+void record_main_stop(cudaStream_t s);
+
 // Device address of the status word on the current device (looked up once
 // per device).
 int status_address(int** out);

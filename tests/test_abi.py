@@ -110,6 +110,36 @@ def test_backward_argument_errors(kw, expect):
     assert fa.fa_bwd(**args) == expect
 
 
+@pytest.mark.parametrize("dtype", [fa.FA_BF16, fa.FA_FP16])
+@pytest.mark.parametrize("kw", [
+    dict(scale=0.0), dict(scale=-0.125),
+    dict(N=1024 * 128 + 1, block_mask=FAKE),        # 1025 key tiles per row: over the forward's list
+])
+def test_forward_refuses_what_the_tensor_cores_do_not_take(kw, dtype):
+    """16-bit problems outside the tensor-core kernels are refused on the
+    host (FA_ERR_UNSUPPORTED), not run on the CUDA-core kernels."""
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=16, d=64, scale=0.125, causal=0,
+                block_mask=None, dropout_p=0.0, seed=0, dtype=dtype, kv_len=None, stream=None)
+    args.update(kw)
+    assert fa.fa_fwd(**args) == -2
+    split = dict(args, n_splits=2, workspace=FAKE, workspace_bytes=1 << 40)
+    assert fa.fa_fwd_splitkv(**split) == -2
+
+
+@pytest.mark.parametrize("kw", [
+    dict(scale=0.0), dict(scale=-1.0),
+    dict(d=128, N=256 * 128 + 1, block_mask=FAKE),  # 257 query tiles per key tile at d = 128
+    dict(d=256, N=256 * 128 + 1, block_mask=FAKE),
+    dict(d=64, N=1024 * 128 + 1, block_mask=FAKE),
+])
+def test_backward_refuses_what_the_tensor_cores_do_not_take(kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dO=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, H=1, N=16,
+                d=64, scale=0.125, causal=0, block_mask=None, dropout_p=0.0, seed=0, dtype=fa.FA_BF16,
+                kv_len=None, workspace=FAKE, workspace_bytes=1 << 40, stream=None)
+    args.update(kw)
+    assert fa.fa_bwd(**args) == -2
+
+
 def test_status_strings():
     for code in (0, -1, -2, -3, -4, -5):
         s = fa.fa_status_string(code)

@@ -15,18 +15,18 @@ def test_flop_model_matches_formula():
 
 def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     rec = {"source_sha256": bench.kernel_source_hash(),
-           "calls": {"gpt2_causal": {"fa_bwd": {"dram_bytes": 1234}}}}
+           "kernels": {"gpt2_causal": {"bwd_tc_kernel": {"dram_bytes": 1234}}}}
     prof = tmp_path / "profiles"
     prof.mkdir()
     (prof / "dram_traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     # the hash is taken from the package sources under ROOT: point it back
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["source_sha256"])
-    assert bench.recorded_traffic("gpt2_causal", "fa_bwd") == 1234
-    assert bench.recorded_traffic("gpt2_causal", "fa_fwd") is None
-    assert bench.recorded_traffic("long_causal", "fa_bwd") is None
+    assert bench.recorded_traffic("gpt2_causal", "bwd_tc_kernel") == 1234
+    assert bench.recorded_traffic("gpt2_causal", "fwd_pp_kernel") is None
+    assert bench.recorded_traffic("long_causal", "bwd_tc_kernel") is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 64)
-    assert bench.recorded_traffic("gpt2_causal", "fa_bwd") is None
+    assert bench.recorded_traffic("gpt2_causal", "bwd_tc_kernel") is None
 
 
 def test_source_hash_tracks_kernel_files():
@@ -49,3 +49,14 @@ def test_byte_model_uses_the_element_size():
     f32, _ = bench.algorithmic_bytes(w.with_(dtype="fp32"))
     bhn = w.B * w.H * w.N
     assert f32 - f16 == 4 * bhn * w.d * (4 - 2)
+
+
+def test_main_kernel_names_and_bytes():
+    w = WORKLOADS["long_causal"]
+    assert bench.main_kernel_names(w) == ("fwd_pp_kernel", "bwd_tc_kernel")
+    assert bench.main_kernel_names(w.with_(d=256))[0] == "fwd_d256_kernel"
+    assert bench.main_kernel_names(WORKLOADS["single_head_fp32"])[0] == "fwd_simt_kernel"
+    # the backward's main kernel reads Q, K, V, dO, LSE, delta and writes dQ, dK, dV
+    bhnd, bhn = w.B * w.H * w.N * w.d, w.B * w.H * w.N
+    assert bench.bwd_main_bytes(w) == 7 * bhnd * 2 + 8 * bhn
+    assert bench.bwd_main_bytes(w) < bench.algorithmic_bytes(w)[1]

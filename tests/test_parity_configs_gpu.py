@@ -88,3 +88,36 @@ def test_sparse_workload_parity(cuda_device, w):
             assert np.abs(dk[b, h].sum(0)).max() <= 1e-3 * np.abs(dk[b, h]).sum(0).max()
             gap = np.abs(dv[b, h].sum(0) - do[b, h].sum(0)).max()
             assert gap <= 1e-3 * np.abs(dv[b, h]).sum(0).max()
+
+
+def test_forward_64k_d128_block_mask_on_tensor_cores(cuda_device):
+    """A block mask with 512 key tiles per row at d = 128 fits the forward's
+    tile lists: the forward runs on the tensor-core kernel (timed: the
+    CUDA-core kernels would take far longer than the bound) and matches the
+    oracle on the head. The backward's lists at d = 128 hold 256 tiles, so
+    the backward is refused (FA_ERR_UNSUPPORTED) instead of being sent to the
+    CUDA-core kernels."""
+    import torch
+    import io_aware_exact_08_gb300 as fa
+    from workloads import Workload
+    w = Workload("block_sparse_64k_d128", 42, B=1, H=1, N=65536, d=128, dtype="bf16", block_sparse=True)
+    inp = make_inputs(w)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for e in ev:
+        e.record()
+    gpu_forward(inp)  # warm-up
+    fa.fa_set_main_kernel_events(ev[0].cuda_event, ev[1].cuda_event)
+    try:
+        q, k, v, o, lse = gpu_forward(inp)
+    finally:
+        fa.fa_set_main_kernel_events(None, None)
+    torch.cuda.synchronize()
+    kernel_ms = ev[0].elapsed_time(ev[1])
+    assert kernel_ms < 3.0, kernel_ms  # ~51 GFLOP of visible work
+    got = {"o": o.float().cpu().numpy().astype(np.float64), "lse": lse.cpu().numpy().astype(np.float64)}
+    errs = compare(got, oracle_fwd_bwd(inp, heads=[0], backward=False), "bf16", keys=("o", "lse"), heads=[0])
+    print(w.name, kernel_ms, errs)
+    do = torch.zeros_like(q)
+    with pytest.raises(fa.FaError) as e:
+        fa.attention_bwd(q, k, v, o, lse, do, scale=inp["scale"], block_mask=inp["block_mask"].cuda())
+    assert e.value.status == -2
