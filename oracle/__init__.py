@@ -62,6 +62,8 @@ def _load():
         lib.oracle_bwd.restype = I
         lib.oracle_probs.argtypes = [P, P, P, P, I, I, I, I, D, I, P, I, P, I]
         lib.oracle_probs.restype = I
+        lib.oracle_e4m3_dequantize.argtypes = [P, P, ctypes.c_long, ctypes.c_long, ctypes.c_long, P]
+        lib.oracle_e4m3_dequantize.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = I
         _lib = lib
@@ -173,3 +175,39 @@ def attention_probs(q, k, scale, head=0, causal=False, block_mask=None, block=12
     _load().oracle_probs(_ptr(q), _ptr(k), _ptr(s), _ptr(p), B, H, N, d, float(scale),
                          int(bool(causal)), _ptr(bm), int(block), _ptr(kl), int(head))
     return s, p
+
+
+def e4m3_dequantize(codes, descale=None, rows_per_scale=None):
+    """Decodes E4M3 bytes (uint8 array of shape [..., n]) to fp64, each block
+    of ``rows_per_scale`` rows multiplied by its factor in ``descale``
+    (one factor per head for [B,H,N,d]: rows_per_scale = N). Without
+    ``descale`` the plain decoded values are returned."""
+    u = _u8(codes)
+    shape = u.shape
+    row_len = shape[-1] if u.ndim else 1
+    rows = u.size // max(row_len, 1)
+    if descale is None:
+        ds = np.ones(1)
+        rows_per_scale = rows
+    else:
+        ds = _f64(descale).reshape(-1)
+        rows_per_scale = rows // ds.size if rows_per_scale is None else int(rows_per_scale)
+        assert rows_per_scale * ds.size == rows, "descale does not divide the rows"
+    out = np.empty(shape, dtype=np.float64)
+    _load().oracle_e4m3_dequantize(_ptr(u), _ptr(out), int(ds.size), int(rows_per_scale), int(row_len), _ptr(ds))
+    return out
+
+
+def attention_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, scale, causal=False, block_mask=None,
+                      block=128, kv_len=None, heads=None, nthreads=0):
+    """Forward attention on E4M3 inputs: q8, k8, v8 are uint8 codes
+    [B,H,N,d] (V in its natural layout) with one dequantisation factor per
+    head (fp32 or fp64 arrays of B*H). The inputs are decoded exactly and
+    scaled, then the fp64 definition runs on them: (O, LSE) in fp64."""
+    q8, k8, v8 = _u8(q8), _u8(k8), _u8(v8)
+    N = q8.shape[2]
+    q = e4m3_dequantize(q8, descale_q, N)
+    k = e4m3_dequantize(k8, descale_k, N)
+    v = e4m3_dequantize(v8, descale_v, N)
+    return attention_fwd(q, k, v, scale, causal=causal, block_mask=block_mask, block=block, kv_len=kv_len,
+                         heads=heads, nthreads=nthreads)

@@ -328,3 +328,35 @@ int oracle_probs(const double* q, const double* k, double* s_out, double* p_out,
 }
 
 int oracle_max_threads(void) { return nthreads_or_default(0); }
+
+/* ---------------------------------------------------------------------- */
+/* 8-bit floating point inputs (the FP8 forward of the "Flash Attention"  */
+/* guide, section "Flash Attention 3 / Presisi FP8 native"). The format is */
+/* E4M3 of the OCP 8-bit floating point specification: 1 sign bit, 4       */
+/* exponent bits with bias 7, 3 mantissa bits; exponent 0 holds the        */
+/* subnormals m/8 * 2^-6; there are no infinities and S.1111.111 is NaN,   */
+/* so the largest finite magnitude is 1.75 * 2^8 = 448. Each code decodes  */
+/* exactly to a double, times the caller's per-head dequantisation factor. */
+/* ---------------------------------------------------------------------- */
+static double e4m3_decode(uint8_t x) {
+    const int sign = x >> 7, e = (x >> 3) & 15, m = x & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);          /* (m / 8) * 2^(1 - 7) */
+    else
+        v = ldexp(8.0 + (double)m, e - 10); /* (1 + m / 8) * 2^(e - 7) */
+    return sign ? -v : v;
+}
+
+/* out[r * row_len + c] = decode(in[...]) * descale[r / rows_per_scale]:
+ * a [n_scales * rows_per_scale, row_len] array with one factor per block of
+ * rows (per head for [B,H,N,d]). */
+void oracle_e4m3_dequantize(const uint8_t* in, double* out, long n_scales, long rows_per_scale, long row_len,
+                            const double* descale) {
+    for (long s = 0; s < n_scales; ++s) {
+        const long base = s * rows_per_scale * row_len;
+        for (long e = 0; e < rows_per_scale * row_len; ++e)
+            out[base + e] = e4m3_decode(in[base + e]) * descale[s];
+    }
+}

@@ -204,3 +204,39 @@ def random_block_mask(nb: int, density: float, seed: int) -> torch.Tensor:
     for i in range(nb):
         m[i, i] = 1
     return m
+
+
+FP8_MAX = 448.0  # largest finite E4M3 magnitude
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-head E4M3 quantisation of a [B,H,N,d] tensor for the FP8 forward.
+
+    Returns (codes, descale): codes are the uint8 E4M3 bytes of x / descale,
+    rounded to nearest even by torch's float8_e4m3fn conversion, and descale
+    (fp32 [B*H]) is each head's max |x| / 448, so the real input is
+    code * descale (1 where a head is all zeros). Only input preparation: the
+    oracle and the library both take these bytes and factors as they are.
+    """
+    B, H, N, d = x.shape
+    xf = x.to(torch.float32).reshape(B * H, N * d)
+    amax = xf.abs().amax(dim=1)
+    descale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
+    scaled = (xf / descale[:, None]).clamp_(-FP8_MAX, FP8_MAX)
+    codes = scaled.to(torch.float8_e4m3fn).view(torch.uint8).reshape(B, H, N, d).contiguous()
+    return codes, descale.contiguous()
+
+
+def make_fp8_inputs(w: Workload, seed: Optional[int] = None):
+    """The workload's Q, K, V (drawn as for the 16-bit workloads, in fp32)
+    quantised per head to E4M3: codes q8, k8, v8 ([B,H,N,d] uint8), their
+    factors (fp32 [B*H]), and v8 transposed to [B,H,d,N] for the library."""
+    w32 = w.with_(dtype="fp32")
+    inp = make_inputs(w32, seed=seed, with_grad_out=False)
+    out = dict(inp)
+    for n in ("q", "k", "v"):
+        codes, ds = quantize_e4m3(inp[n])
+        out[n + "8"] = codes
+        out["descale_" + n] = ds
+    out["vt8"] = out["v8"].transpose(2, 3).contiguous()
+    return out
