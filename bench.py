@@ -267,6 +267,27 @@ def cpu_model():
     return platform.machine()
 
 
+def head_sample(inp, w, n):
+    """The first n heads (flat order b*H + h) of the inputs as a smaller
+    problem the oracle can run on its own (heads are independent): the
+    first n heads of batch 0 if n <= H, else the first ceil(n/H) whole
+    batches. Returns (inputs, heads taken)."""
+    if n <= w.H:
+        nb, nh = 1, n
+    else:
+        nb, nh = min(w.B, -(-n // w.H)), w.H
+    out = dict(inp)
+    for key in ("q", "k", "v", "do", "q8", "k8", "v8"):
+        if inp.get(key) is not None:
+            out[key] = inp[key][:nb, :nh].contiguous()
+    for key in ("descale_q", "descale_k", "descale_v"):
+        if inp.get(key) is not None:
+            out[key] = inp[key].reshape(w.B, w.H)[:nb, :nh].reshape(-1).contiguous()
+    if inp.get("kv_len") is not None:
+        out["kv_len"] = inp["kv_len"][:nb].contiguous()
+    return out, nb * nh
+
+
 def oracle_heads_for(w, inp, budget_s, backward=True):
     """How many whole heads of the workload the oracle runs in about
     budget_s seconds (at least one), from one timed head."""
@@ -275,15 +296,18 @@ def oracle_heads_for(w, inp, budget_s, backward=True):
 
 
 def oracle_run(w, inp, heads, backward=True):
-    """Wall time of the fp64 oracle on `heads` (forward, and backward)."""
+    """Wall time of the fp64 oracle on the first len(heads) heads (forward,
+    and backward), given only those heads' inputs. The dropout mask is drawn
+    for the heads' own (b, h) indices, which the sample keeps."""
     import oracle
-    kw = dict(causal=w.causal, block_mask=inp["block_mask"], block=128, kv_len=inp["kv_len"],
-              dropout_p=w.dropout_p, seed=inp["seed"])
-    q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
+    sub, _ = head_sample(inp, w, len(heads))
+    kw = dict(causal=w.causal, block_mask=sub["block_mask"], block=128, kv_len=sub["kv_len"],
+              dropout_p=w.dropout_p, seed=sub["seed"])
+    q, k, v, do = (sub[n] for n in ("q", "k", "v", "do"))
     t0 = time.perf_counter()
-    oracle.attention_fwd(q, k, v, w.softmax_scale, heads=heads, **kw)
+    oracle.attention_fwd(q, k, v, w.softmax_scale, **kw)
     if backward:
-        oracle.attention_bwd(q, k, v, do, w.softmax_scale, heads=heads, **kw)
+        oracle.attention_bwd(q, k, v, do, w.softmax_scale, **kw)
     return time.perf_counter() - t0
 
 
@@ -293,7 +317,7 @@ def oracle_sample(w, inp, budget_s=12.0, backward=True):
     total_heads = w.B * w.H
     fwd_f, bwd_f = flops(w, density_of(inp, w))
     per_head = (fwd_f + (bwd_f if backward else 0.0)) / total_heads
-    n = oracle_heads_for(w, inp, budget_s, backward)
+    n = head_sample(inp, w, oracle_heads_for(w, inp, budget_s, backward))[1]
     t = oracle_run(w, inp, list(range(n)), backward)
     value = per_head * n / t / 1e12
     return {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "cpu_model": cpu_model(),
@@ -483,6 +507,162 @@ def run_fa(args, w, ws, rank, device):
     return line
 
 
+def oracle_run_fp8(inp, w, heads):
+    """Wall time of the oracle's FP8 forward on the first len(heads) heads."""
+    import oracle
+    sub, _ = head_sample(inp, w, len(heads))
+    t0 = time.perf_counter()
+    oracle.attention_fwd_fp8(sub["q8"], sub["k8"], sub["v8"], sub["descale_q"], sub["descale_k"], sub["descale_v"],
+                             w.softmax_scale, causal=w.causal, block_mask=sub["block_mask"], block=128,
+                             kv_len=sub["kv_len"])
+    return time.perf_counter() - t0
+
+
+def fp8_config(w, density, ws):
+    cfg = workload_config(w, density, 1, ws)
+    cfg.update({"dtype": "e4m3", "step": "fa_fwd_fp8 (forward only; E4M3 Q, K, V with per-head factors, bf16 O)"})
+    return cfg
+
+
+def run_fa_fp8(args, w, ws, rank, device):
+    """The E4M3 forward alone: one step = one fa_fwd_fp8 call over the
+    workload (inputs resident in HBM), FLOPs = the forward's 4 B H N^2 d
+    (halved for causal, times the block density)."""
+    import torch
+    import io_aware_exact_08_gb300 as fa
+    from workloads import make_fp8_inputs
+
+    inp = make_fp8_inputs(w)
+    dens = density_of(inp, w)
+    fwd_f, _ = flops(w, dens)
+    dev = lambda t: None if t is None else t.to(device).contiguous()
+    q8, k8, vt8 = dev(inp["q8"]), dev(inp["k8"]), dev(inp["vt8"])
+    dsq, dsk, dsv = dev(inp["descale_q"]), dev(inp["descale_k"]), dev(inp["descale_v"])
+    bm, kl = dev(inp["block_mask"]), dev(inp["kv_len"])
+    B, H, N, d = w.B, w.H, w.N, w.d
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    ptr = lambda t: None if t is None else t.data_ptr()
+
+    def fwd():
+        rc = fa.fa_fwd_fp8(ptr(q8), ptr(k8), ptr(vt8), ptr(dsq), ptr(dsk), ptr(dsv), ptr(o), ptr(lse), B, H, N, d,
+                           w.softmax_scale, int(w.causal), ptr(bm), ptr(kl), sh)
+        assert rc == 0, fa.fa_status_string(rc)
+
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    launches0 = fa.fa_launch_count()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    launches = fa.fa_launch_count() - launches0
+    barrier(device)
+    clk = clocks.stop()
+    st, site = fa.fa_check_device_status(sh)
+    assert st == 0, f"device status {st} at site {site}"
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    value, step_ms_max = whole_job_tflops(fwd_f, step_ms, ws, device)
+
+    host_in = [inp[n].pin_memory() for n in ("q8", "k8", "vt8")]
+    host_out = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    barrier(device)
+    torch.cuda.synchronize(device)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        for dst, src in zip((q8, k8, vt8), host_in):
+            dst.copy_(src, non_blocking=True)
+        fwd()
+        host_out.copy_(o, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / e2e_steps, device)
+
+    peaks = load_peaks()
+    # E4M3 dense tensor rate is twice the bf16 rate (4.5 vs 2.25 PFLOP/s
+    # nominal): the measured bf16 peak times 2
+    peak = 2.0 * peaks["bf16"]
+    ach = value / ws
+    e = 1
+    bhnd = B * H * N * d
+    alg_bytes = 3 * bhnd * e + 2 * bhnd + 4 * B * H * N
+    roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+            "frac": round(ach / peak, 4), "kernel": "fwd_fp8_kernel",
+            "traffic": recorded_traffic(w.name + "/fp8", "fwd_fp8_kernel"),
+            "peak_source": peaks["source"] + " (burst) bf16 peak x 2 for E4M3",
+            "algorithmic_flops": fwd_f, "algorithmic_bytes": alg_bytes, "kernel_avg_ms": round(step_ms_max, 4)}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": fp8_config(w, dens, ws),
+        "fwd_tflops": round(value, 3), "fwd_ms": round(step_ms_max, 4),
+        "frac_of_bf16_peak": round(ach / peaks["bf16"], 4),
+        "roofline": roof,
+        "e2e": {"value": round(fwd_f * ws / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        import oracle
+        t1 = oracle_run_fp8(inp, w, [0])
+        n = head_sample(inp, w, max(1, min(B * H, int(args.cpu_budget / max(t1, 1e-6)))))[1]
+        t = oracle_run_fp8(inp, w, list(range(n))) if n > 1 else t1
+        line["cpu_baseline"] = {"value": fwd_f / (B * H) * n / t / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+                                "cpu_model": cpu_model(), "kind": "oracle",
+                                "sample": f"{n} of {B * H} heads, fp64 forward on the dequantised inputs, {t:.2f} s"}
+    return line
+
+
+def run_reference_fp8(args, w, ws, rank):
+    """The oracle's FP8 forward (fp64 on the dequantised inputs) as the
+    reference arm, on a fixed sample of whole heads per step."""
+    from workloads import make_fp8_inputs
+    if rank != 0:
+        return None
+    import oracle
+    inp = make_fp8_inputs(w)
+    dens = density_of(inp, w)
+    fwd_f, _ = flops(w, dens)
+    total = w.B * w.H
+    t1 = oracle_run_fp8(inp, w, [0])
+    n = head_sample(inp, w, max(1, min(total, int(args.cpu_budget / max(1, args.steps) / max(t1, 1e-6)))))[1]
+    heads = list(range(n))
+    for _ in range(args.warmup):
+        oracle_run_fp8(inp, w, [0])
+    times = [oracle_run_fp8(inp, w, heads) for _ in range(args.steps)]
+    step_s = sum(times) / len(times)
+    value = fwd_f * n / total / step_s / 1e12
+    sample = f"{n} of {total} heads per step, fp64 forward on the dequantised E4M3 inputs"
+    cfg = fp8_config(w, dens, ws)
+    cfg["sample"] = sample
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "cpu_model": cpu_model(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, w, ws, rank):
     """The oracle (fp64, host cores) as the reference arm: each step runs it
     on the same fixed sample of whole heads of the workload, and the step's
@@ -496,7 +676,7 @@ def run_reference(args, w, ws, rank):
     fwd_f, bwd_f = flops(w, dens)
     total_heads = w.B * w.H
     # sample size: whole heads filling about cpu_budget / steps seconds per step
-    n = oracle_heads_for(w, inp, args.cpu_budget / max(1, args.steps))
+    n = head_sample(inp, w, oracle_heads_for(w, inp, args.cpu_budget / max(1, args.steps)))[1]
     heads = list(range(n))
     for _ in range(args.warmup):
         oracle_run(w, inp, [0])
@@ -527,8 +707,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="fa", choices=["fa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
-                    help="run a 16-bit workload with this input type instead of its own")
+    ap.add_argument("--dtype", choices=["bf16", "fp16", "fp8"], default=None,
+                    help="run a 16-bit workload with this input type instead of its own; fp8 times the "
+                         "E4M3 forward (fa_fwd_fp8, head dim 128) alone")
     ap.add_argument("--splits", type=int, default=1,
                     help="forward through fa_fwd_splitkv with this many key-tile ranges per query-tile pair")
     args = ap.parse_args(argv)
@@ -540,14 +721,19 @@ def main(argv=None):
     table.update({w.name: w for w in sweep_workloads() + splitkv_workloads() + headdim_workloads() +
                   sparse_workloads()})
     w = table[args.workload]
+    fp8 = args.dtype == "fp8"
     if args.dtype is not None:
         if w.dtype not in ("bf16", "fp16"):
             ap.error("--dtype applies to the 16-bit workloads only")
-        w = w.with_(dtype=args.dtype)
+        if fp8:
+            if w.d != 128 or w.dropout_p > 0 or args.splits > 1:
+                ap.error("--dtype fp8 needs a head-dim-128 workload without dropout or splits")
+        else:
+            w = w.with_(dtype=args.dtype)
     ws, rank, local = dist_env()
 
     if args.impl == "reference":
-        line = run_reference(args, w, ws, rank)
+        line = run_reference_fp8(args, w, ws, rank) if fp8 else run_reference(args, w, ws, rank)
         if line is not None:
             print(json.dumps(line), flush=True)
         return 0
@@ -561,7 +747,7 @@ def main(argv=None):
     torch.cuda.set_device(device)
     import io_aware_exact_08_gb300 as fa
     fa.load_library()
-    line = run_fa(args, w, ws, rank, device)
+    line = run_fa_fp8(args, w, ws, rank, device) if fp8 else run_fa(args, w, ws, rank, device)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -159,6 +159,35 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    fa_dtype dtype, const int32_t* kv_len, int n_splits,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * FP8 forward ("Flash Attention" guide, section "Flash Attention 3 / Presisi
+ * FP8 native"): o = softmax(scale * Q K^T + mask) V on 8-bit inputs, both
+ * products on the tensor cores in E4M3 with fp32 accumulation.
+ *   q, k       E4M3 codes (OCP 8-bit floating point, 1-4-3, bias 7), uint8
+ *              [B, H, N, 128], device memory, 16-byte aligned.
+ *   vt         V transposed: E4M3 codes [B, H, 128, N] (keys contiguous), so
+ *              that every operand of both products is K-major.
+ *   descale_q, descale_k, descale_v
+ *              per-head dequantisation factors, fp32 [B*H] in device memory:
+ *              the real input is code * factor (per-tensor, per-head
+ *              scaling; the caller chooses them, e.g. max|x| / 448).
+ *   o          bf16 [B, H, N, 128]; lse fp32 [B, H, N] (natural log).
+ *   causal, block_mask, kv_len as in fa_fwd; no dropout.
+ * P is quantised to E4M3 for the P V product, scaled by 2^8 before
+ * rounding (the running maximum is raised whenever a row's maximum exceeds
+ * it by 1/2 in log2 units, so the scaled values stay below 2^8.5 < 448);
+ * the row sum uses the unquantised values. The error this adds to O is that
+ * of rounding each P_ij to E4M3 (relative 2^-4): |dO_ic| is within a few
+ * (2^-4/sqrt 3) sqrt(sum_j P_ij^2 V_jc^2) for independent roundings.
+ * Returns FA_ERR_UNSUPPORTED for d != 128, N not a multiple of 16 (the rows
+ * of vt must be 16-byte aligned), scale <= 0 or a block mask with more than
+ * 1024 key tiles per row; otherwise as fa_fwd.
+ */
+int fa_fwd_fp8(const void* q, const void* k, const void* vt,
+               const float* descale_q, const float* descale_k, const float* descale_v,
+               void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+               const uint8_t* block_mask, const int32_t* kv_len, void* stream);
+
 /* Bytes of split-KV workspace: n_splits * B*H*N*(d + 1) floats (partial O,
  * then partial LSE), each part rounded up to 256 bytes; 0 for invalid sizes. */
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int n_splits);
@@ -209,7 +238,7 @@ uint64_t fa_launch_count(void);
 
 /*
  * Diagnostic timing of a call's main kernel. While set, every fa_fwd,
- * fa_fwd_splitkv and fa_bwd call records ev_start (a cudaEvent_t) on its
+ * fa_fwd_splitkv, fa_fwd_fp8 and fa_bwd call records ev_start (a cudaEvent_t) on its
  * stream immediately before launching its main kernel (the forward kernel;
  * the backward's tile kernel, or its three d = 256 passes; the CUDA-core
  * kernels) and ev_stop immediately after, so that cudaEventElapsedTime gives

@@ -24,7 +24,7 @@ __all__ = [
     "FA_BF16", "FA_FP32", "FA_FP16", "FaError", "load_library", "library_path",
     "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
     "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
-    "fa_set_main_kernel_events", "fa_bwd_noalloc", "FA_BWD_NOALLOC_SCRATCH_BYTES", "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
+    "fa_set_main_kernel_events", "fa_bwd_noalloc", "fa_fwd_fp8", "attention_fwd_fp8", "FA_BWD_NOALLOC_SCRATCH_BYTES", "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
 ]
 
 FA_BF16 = 0
@@ -39,7 +39,7 @@ _lock = threading.Lock()
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
             "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
             "fa_bwd_noalloc", "fa_test_wait_timeout", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size",
-            "fa_set_main_kernel_events")
+            "fa_set_main_kernel_events", "fa_fwd_fp8")
 
 # Size of the fixed device array fa_bwd_noalloc takes its workspace from.
 FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -70,6 +70,8 @@ def load_library(build_if_missing: bool = True):
         P, I, F, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
         lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, P]
         lib.fa_fwd.restype = I
+        lib.fa_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, P, P]
+        lib.fa_fwd_fp8.restype = I
         lib.fa_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, I, P, SZ, P]
         lib.fa_fwd_splitkv.restype = I
         lib.fa_fwd_splitkv_workspace_size.argtypes = [I, I, I, I, I]
@@ -105,6 +107,12 @@ def load_library(build_if_missing: bool = True):
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, block_mask, dropout_p, seed, dtype, kv_len, stream):
     return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, int(causal), block_mask, dropout_p,
                                  seed & 0xFFFFFFFFFFFFFFFF, dtype, kv_len, stream)
+
+
+def fa_fwd_fp8(q, k, vt, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale, causal, block_mask, kv_len,
+               stream):
+    return load_library().fa_fwd_fp8(q, k, vt, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale,
+                                     int(causal), block_mask, kv_len, stream)
 
 
 def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, block_mask, dropout_p, seed, dtype, kv_len,
@@ -243,6 +251,33 @@ def attention_fwd(q, k, v, scale=None, causal=False, block_mask=None, dropout_p=
                 float(dropout_p), int(seed), _dtype_code(q), _ptr(kv_len), _stream(stream))
     if rc != 0:
         raise FaError(rc, "fa_fwd")
+    return o, l
+
+
+def attention_fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, scale=None, causal=False, block_mask=None,
+                      kv_len=None, stream=None):
+    """O (bf16), LSE = attention on E4M3 inputs (fa_fwd_fp8).
+
+    q8, k8: uint8 E4M3 codes [B,H,N,128]; vt8: V's codes transposed,
+    [B,H,128,N]; descale_*: fp32 [B*H] per-head factors (real value =
+    code * factor). All CUDA tensors."""
+    torch = _torch()
+    for name, t in (("q8", q8), ("k8", k8), ("vt8", vt8)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous() or t.dtype != torch.uint8:
+            raise ValueError(f"{name} must be a contiguous uint8 CUDA tensor of E4M3 codes")
+    for name, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+            raise ValueError(f"{name} must be a float32 CUDA tensor [B*H]")
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or tuple(vt8.shape) != (B, H, d, N):
+        raise ValueError("k8 must match q8 and vt8 must be [B,H,d,N]")
+    scale = (1.0 / d ** 0.5) if scale is None else float(scale)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    rc = fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(descale_q), _ptr(descale_k), _ptr(descale_v), _ptr(o),
+                    _ptr(l), B, H, N, d, scale, causal, _ptr(block_mask), _ptr(kv_len), _stream(stream))
+    if rc != 0:
+        raise FaError(rc, "fa_fwd_fp8")
     return o, l
 
 

@@ -153,6 +153,32 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return rc;
 }
 
+int fa_fwd_fp8(const void* q, const void* k, const void* vt, const float* descale_q, const float* descale_k,
+               const float* descale_v, void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+               const uint8_t* block_mask, const int32_t* kv_len, void* stream) {
+    int rc = check_common(B, H, N, d, scale, 0.f, FA_BF16);
+    if (rc != FA_OK) return rc;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!(scale > 0.f)) return FA_ERR_UNSUPPORTED;
+    if (N == 0) return FA_OK;
+    if (N % 16 != 0) return FA_ERR_UNSUPPORTED;  // rows of vt must start 16-byte aligned
+    if (!q || !k || !vt || !o || !lse || !descale_q || !descale_k || !descale_v) return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(vt, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        !aligned(descale_q, 4) || !aligned(descale_k, 4) || !aligned(descale_v, 4))
+        return FA_ERR_INVALID_ARG;
+    if (block_mask && (N + kMaskBlock - 1) / kMaskBlock > kMaskListCap) return FA_ERR_UNSUPPORTED;
+    Problem p{};
+    fill_common(p, B, H, N, d, scale, causal, block_mask, 0.f, 0, FA_BF16, kv_len, stream);
+    p.q = q;
+    p.k = k;
+    p.v = vt;
+    p.o = o;
+    p.lse = lse;
+    rc = status_address(&p.status);
+    if (rc != FA_OK) return rc;
+    return launch_fwd_fp8(p, Fp8Inputs{descale_q, descale_k, descale_v});
+}
+
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int n_splits) {
     if (B < 1 || H < 1 || N < 0 || (d != 64 && d != 128 && d != 256) || n_splits < 1 || n_splits > kMaxSplits)
         return 0;

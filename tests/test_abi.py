@@ -173,3 +173,14 @@ def test_splitkv_argument_errors(kw, expect):
                 workspace=FAKE, workspace_bytes=1 << 20, stream=None)
     args.update(kw)
     assert fa.fa_fwd_splitkv(**args) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=64), -2), (dict(d=256), -2), (dict(N=100), -2), (dict(scale=0.0), -2), (dict(q=None), -1),
+    (dict(descale_v=None), -1), (dict(vt=FAKE + 8), -1), (dict(B=0), -1), (dict(N=1024 * 128 + 16, block_mask=FAKE), -2),
+])
+def test_fp8_forward_argument_errors(kw, expect):
+    args = dict(q=FAKE, k=FAKE, vt=FAKE, descale_q=FAKE, descale_k=FAKE, descale_v=FAKE, o=FAKE, lse=FAKE, B=1, H=1,
+                N=16, d=128, scale=0.125, causal=0, block_mask=None, kv_len=None, stream=None)
+    args.update(kw)
+    assert fa.fa_fwd_fp8(**args) == expect
