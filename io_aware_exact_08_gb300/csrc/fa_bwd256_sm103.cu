@@ -155,15 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kMask && warp == 0) {
         // dV, dK: query tiles i with block (i, own) set; dQ: key tiles j with
         // block (own, j) set; within the unmasked range, 32 at a time
-        int cnt = 0;
-        for (int c = sched.first; c < sched.end; c += 32) {
-            const int t = c + lane;
-            const bool act = t < sched.end &&
-                             p.block_mask[kKeyRows ? (size_t)t * p.nb + own : (size_t)own * p.nb + t] != 0;
-            const uint32_t bal = __ballot_sync(0xffffffffu, act);
-            if (act) sList[cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)t;
-            cnt += __popc(bal);
-        }
+        const int cnt = kKeyRows ? warp_list_visible(p.block_mask + own, (size_t)p.nb, sched.first, sched.end, sList, lane)
+                                 : warp_list_visible(p.block_mask + (size_t)own * p.nb, 1, sched.first, sched.end,
+                                                     sList, lane);
         if (lane == 0) st->n_list = cnt;
     }
     if (tid == 0) {

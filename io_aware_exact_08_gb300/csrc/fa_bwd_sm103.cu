@@ -214,14 +214,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     // (strided loads of one mask column, 32 at a time, and a ballot)
     if (kMask && warp == 0) {
         const int first = p.causal ? jt : 0;
-        int cnt = 0;
-        for (int c = first; c < sched.nqt; c += 32) {
-            const int i = c + lane;
-            const bool act = i < sched.nqt && p.block_mask[(size_t)i * p.nb + jt] != 0;
-            const uint32_t bal = __ballot_sync(0xffffffffu, act);
-            if (act) sList[cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)i;
-            cnt += __popc(bal);
-        }
+        const int cnt = warp_list_visible(p.block_mask + jt, (size_t)p.nb, first, sched.nqt, sList, lane);
         if (lane == 0) st->n_list = cnt;
     }
 

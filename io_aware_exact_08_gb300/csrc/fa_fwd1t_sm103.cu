@@ -1,0 +1,454 @@
+// Forward attention at head dimension 64, one 128-row query tile per CTA,
+// two CTAs per SM.
+//
+// The same per-block update as the two-tile kernel ("FlashAttention: Fast
+// and Memory-Efficient Exact Attention with IO-Awareness", section "Metode",
+// steps 1-4; the division by l deferred to the end as in the FlashAttention-2
+// section of the "Flash Attention" guide), laid out so that two CTAs fit on
+// one SM: TMEM holds one S (128 columns, P written over it) and O (64
+// columns) in a 256-column allocation, and shared memory holds Q and a
+// five-stage K/V ring (about 100 KB). Within a CTA the S, softmax and P V of
+// consecutive key tiles run one after the other; the tensor core alternates
+// between the two CTAs of the SM, and one CTA's start (barriers, TMEM, the Q
+// and first K/V loads) and end (the O and LSE stores) overlap the other's
+// main loop. At head dimension 64 the per-CTA fixed costs are as large as a
+// few key tiles' work, which is what this layout hides; with one tile per
+// CTA the grid also has twice as many, smaller work units.
+// Roles (256 threads): warps 0-3 softmax (thread = query row), warp 4 TMA
+// producer, warp 5 MMA issuer (all 32 lanes run its loop, one elected lane
+// issues), warps 6-7 idle. setmaxnreg gives the softmax warpgroup 208
+// registers a thread and the other 48 (launched at 128).
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "fa_device.cuh"
+#include "fa_internal.h"
+#include "fa_sm103.cuh"
+
+namespace fa {
+
+bool make_tmap16(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows, CUtensorMapDataType type);
+
+namespace {
+
+using namespace sm103;
+
+constexpr int kD = 64;
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+constexpr int kThreads = 256;
+constexpr int kSoftRegs = 208, kIssueRegs = 48;
+static_assert(128 * kSoftRegs + 128 * kIssueRegs <= kThreads * 128, "register budgets above the launch");
+constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in the two-tile kernel
+constexpr int kStages = 5;
+constexpr int kTileBytes = kBlockN * kD * 2;  // one 128 x 64 16-bit tile (one 128-byte-wide box)
+constexpr int kSmem = 1024 + kTileBytes + kStages * kTileBytes + 256 + kMaskListCap * 2;
+static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
+constexpr uint32_t kColS = 0, kColO = 128, kTmemCols = 256;
+
+struct Fwd1tParams {
+    float* lse;
+    void* o;
+    const uint8_t* block_mask;
+    const int32_t* kv_len;
+    int* status;
+    int H, N, nb, n_qtiles;
+    float scale_log2;
+    float out_scale;  // 1/(1-p)
+    uint32_t drop_thr;
+    int dropout;
+    int causal;
+    uint64_t seed;
+};
+
+struct Shared1t {
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t q_full;
+    uint64_t s_full;
+    uint64_t p_full;
+    uint64_t o_final;
+    uint64_t teardown;
+    uint32_t tmem_base;
+    int abort_flag;
+    int n_list;
+};
+static_assert(sizeof(Shared1t) <= 256, "barrier block");
+
+template <typename T, bool kSplit>
+__global__ void __launch_bounds__(kThreads, 2)
+    fwd_1t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const Fwd1tParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sKV = smem + kTileBytes;
+    Shared1t* st = reinterpret_cast<Shared1t*>(sKV + kStages * kTileBytes);
+    uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);  // [kMaskListCap]
+
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // grid (B*H, query tiles), x fastest: every head's heaviest causal tile first
+    const int bh = blockIdx.x;
+    const int b = bh / p.H, h = bh % p.H;
+    const int qt = p.causal ? (p.n_qtiles - 1 - (int)blockIdx.y) : (int)blockIdx.y;
+    const int L = p.kv_len ? min(max(p.kv_len[b], 0), p.N) : p.N;
+    const int nkt = (L + kBlockN - 1) / kBlockN;
+    int n = p.causal ? min(nkt, qt + 1) : nkt;
+    WaitCtx wctx{&st->abort_flag, p.status};
+    if (kSplit && warp == 0) {
+        const int cnt = warp_list_visible(p.block_mask + (size_t)qt * p.nb, 1, 0, n, sList, lane);
+        if (lane == 0) st->n_list = cnt;
+    }
+    if (warp == 4 && lane == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&st->kv_full[s], 1);
+            mbar_init(&st->kv_empty[s], 1);
+        }
+        mbar_init(&st->q_full, 1);
+        mbar_init(&st->s_full, 1);
+        mbar_init(&st->p_full, 4);
+        mbar_init(&st->o_final, 1);
+        mbar_init(&st->teardown, 1);
+        st->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&st->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = st->tmem_base;
+    if constexpr (kSplit) n = st->n_list;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        regs_dec<kIssueRegs>();
+        if (lane == 0 && n > 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(&st->q_full, kTileBytes);
+            tma_load_3d(sQ, &tm_q, &st->q_full, 0, qt * kBlockM, bh);
+            // load 2u = K of key tile u, 2u + 1 = V of it
+            int t = 0;
+            bool okp = true;
+            for (int u = 0; okp && u < n; ++u) {
+                const int j = kSplit ? (int)sList[u] : u;
+#pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    const int s = t % kStages;
+                    const uint32_t ph = (t / kStages) & 1;
+                    if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 361)) {
+                        okp = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&st->kv_full[s], kTileBytes);
+                    tma_load_3d(sKV + s * kTileBytes, which ? &tm_v : &tm_k, &st->kv_full[s], 0, j * kBlockN, bh);
+                    ++t;
+                }
+            }
+            // drain: the last load issued into each stage has landed
+            for (int l = max(0, t - kStages); l < t; ++l)
+                mbar_wait(&st->kv_full[l % kStages], (l / kStages) & 1, wctx, 362);
+            mbar_wait(&st->q_full, 0, wctx, 363);
+        }
+    } else if (warp == 6 || warp == 7) {
+        regs_dec<kIssueRegs>();  // idle: the rest of the producer / MMA warpgroup
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        regs_dec<kIssueRegs>();
+        if (n > 0) {
+            constexpr uint32_t idesc_s = idesc_f32acc(Elem16<T>::kFmt, kBlockM, kBlockN, 0, 0);
+            constexpr uint32_t idesc_o = idesc_f32acc(Elem16<T>::kFmt, kBlockM, kD, 0, 1);
+            constexpr uint32_t kStageUnits = kTileBytes >> 4;
+            const uint32_t kv_base = smem_u32(sKV);
+            const uint64_t qd = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t kvd_k = smem_desc_sw128(kv_base, 16, 1024);               // K tiles, K-major
+            const uint64_t kvd_v = smem_desc_sw128(kv_base, kBlockN * 128, 1024);    // V tiles, MN-major
+            bool ok = mbar_wait_warp(&st->q_full, 0, wctx, 370);
+            tc_fence_after();
+            int ld = 0;  // next load to use
+            // S(u) = Q K_u^T over the S columns (P(u-1) there has been read:
+            // MMAs run in issue order)
+            auto issue_s = [&]() -> bool {
+                const int s = ld % kStages;
+                if (!mbar_wait_warp(&st->kv_full[s], (ld / kStages) & 1, wctx, 371)) return false;
+                tc_fence_after();
+                const uint64_t kd = kvd_k + (uint64_t)(s * kStageUnits);
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    mma_ss_warp(tmem + kColS, desc_add(qd, kk * 32), desc_add(kd, kk * 32), idesc_s, kk > 0);
+                mma_commit_warp(&st->s_full);
+                mma_commit_warp(&st->kv_empty[s]);
+                ++ld;
+                return true;
+            };
+            if (ok) ok = issue_s();
+            for (int u = 0; ok && u < n; ++u) {
+                // O += P(u) V_u, A = P(u) from TMEM
+                if (!mbar_wait_warp(&st->p_full, u & 1, wctx, 372)) break;
+                tc_fence_after();
+                const int s = ld % kStages;
+                if (!mbar_wait_warp(&st->kv_full[s], (ld / kStages) & 1, wctx, 374)) break;
+                tc_fence_after();
+                const uint64_t vd = kvd_v + (uint64_t)(s * kStageUnits);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ts_warp(tmem + kColO, tmem + kColS + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
+                                (u > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_warp(&st->kv_empty[s]);
+                ++ld;
+                if (u + 1 == n) mma_commit_warp(&st->o_final);
+                else ok = issue_s();
+            }
+            mma_commit_warp(&st->teardown);
+            mbar_wait_warp(&st->teardown, 0, wctx, 373);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        regs_inc<kSoftRegs>();
+        const int r = tid;  // 0..127
+        const int i = qt * kBlockM + r;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t sbase = tmem + lane_base + kColS;
+        const uint32_t obase = tmem + lane_base + kColO;
+        float m = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+        for (int u = 0; u < n; ++u) {
+            const int ktile = kSplit ? (int)sList[u] : u;
+            // dropout keep bits of this row's 128 keys (bit x of keep[c] is
+            // key 32c + x), drawn before S arrives
+            uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+            if (p.dropout) {
+#pragma unroll 8
+                for (int g = 0; g < 32; ++g) {
+                    const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, i, ktile * (kBlockN / 4) + g);
+                    if (g == 0) keep[0] = keep[1] = keep[2] = keep[3] = 0;
+                    const uint32_t sh = bits << (4 * (g & 7));
+                    if ((g >> 3) == 0) keep[0] |= sh;
+                    else if ((g >> 3) == 1) keep[1] |= sh;
+                    else if ((g >> 3) == 2) keep[2] |= sh;
+                    else keep[3] |= sh;
+                }
+            }
+            if (!mbar_wait_warp(&st->s_full, u & 1, wctx, 380)) {
+                ok = false;
+                break;
+            }
+            // S(u) was issued after P(u-1) V: O is complete here
+            tc_fence_after();
+            const int k0 = ktile * kBlockN;
+            int lim = min(kBlockN, L - k0);
+            if (p.causal) lim = min(lim, i - k0 + 1);
+            const bool full = lim >= kBlockN;
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(sbase + c * 32, sr[c]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+            if (!full) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        if (c * 32 + x >= lim) sr[c][x] = __float_as_uint(-INFINITY);
+            }
+            float pm[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) pm[x] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int x = 0; x < 32; x += 2)
+                    pm[(x >> 1) & 7] =
+                        fmax3(pm[(x >> 1) & 7], __uint_as_float(sr[c][x]), __uint_as_float(sr[c][x + 1]));
+            pm[0] = fmax3(pm[0], pm[1], pm[2]);
+            pm[3] = fmax3(pm[3], pm[4], pm[5]);
+            pm[6] = fmaxf(pm[6], pm[7]);
+            pm[0] = fmax3(pm[0], pm[3], pm[6]);
+            const float mt = pm[0] * p.scale_log2;
+            const bool raise = mt > m + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, raise) && u > 0) {
+                const float alpha = raise ? ex2_approx(m - mt) : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < kD / 8; ++c) {
+                    uint32_t orr[8];
+                    tmem_ld8(obase + c * 8, orr);
+                    tmem_ld_wait();
+                    reg_fence8(orr);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) orr[x] = __float_as_uint(__uint_as_float(orr[x]) * alpha);
+                    tmem_st8(obase + c * 8, orr);
+                }
+                if (raise) l *= alpha;
+            }
+            if (raise) m = mt;
+            const float nmref = (m == -INFINITY) ? 0.f : -m;
+            const float sl2 = p.scale_log2;
+            float ps[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) ps[x] = 0.f;
+            // exponentials packed in place (P chunk c in columns 16c..16c+15,
+            // already read); the sum takes every exponential, the dropout
+            // mask only what goes to P
+            if (!p.dropout) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 2) {
+                        float a0, a1;
+                        ffma2(a0, a1, __uint_as_float(sr[c][x]), __uint_as_float(sr[c][x + 1]), sl2, sl2, nmref, nmref);
+                        const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+                        const int k = (x >> 1) & 3;
+                        fadd2(ps[2 * k], ps[2 * k + 1], ps[2 * k], ps[2 * k + 1], e0, e1);
+                        sr[c][x >> 1] = Elem16<T>::pack2(e0, e1);
+                    }
+                    tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 2) {
+                        float a0, a1;
+                        ffma2(a0, a1, __uint_as_float(sr[c][x]), __uint_as_float(sr[c][x + 1]), sl2, sl2, nmref, nmref);
+                        const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+                        const int k = (x >> 1) & 3;
+                        fadd2(ps[2 * k], ps[2 * k + 1], ps[2 * k], ps[2 * k + 1], e0, e1);
+                        sr[c][x >> 1] =
+                            Elem16<T>::pack2(((keep[c] >> x) & 1u) ? e0 : 0.f, ((keep[c] >> (x + 1)) & 1u) ? e1 : 0.f);
+                    }
+                    tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
+                }
+            }
+            fadd2(ps[0], ps[1], ps[0], ps[1], ps[4], ps[5]);
+            fadd2(ps[2], ps[3], ps[2], ps[3], ps[6], ps[7]);
+            fadd2(ps[0], ps[1], ps[0], ps[1], ps[2], ps[3]);
+            l += ps[0] + ps[1];
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive_warp(&st->p_full);
+        }
+        T* O = static_cast<T*>(p.o) + ((size_t)bh * p.N) * kD;
+        if (ok && n > 0) {
+            if (mbar_wait_warp(&st->o_final, 0, wctx, 381)) {
+                tc_fence_after();
+                const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+#pragma unroll
+                for (int c = 0; c < kD / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(obase + c * 32, orr);
+                    tmem_ld_wait();
+                    reg_fence(orr);
+                    if (i < p.N) {
+                        uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * kD + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w4;
+                            w4.x = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
+                            w4.y = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
+                            w4.z = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
+                            w4.w = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
+                            dst[v] = w4;
+                        }
+                    }
+                }
+                if (i < p.N) p.lse[(size_t)bh * p.N + i] = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+            }
+        } else if (n == 0 && i < p.N) {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * kD);
+#pragma unroll
+            for (int v = 0; v < kD / 8; ++v) dst[v] = z;
+            p.lse[(size_t)bh * p.N + i] = -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <typename T, bool kSplit>
+int launch_1t(const Problem& pr) {
+    constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
+    CUtensorMap tq, tk, tv;
+    const int BH = pr.B * pr.H;
+    if (!make_tmap16(&tq, pr.q, BH, pr.N, kD, kBlockM, tt) || !make_tmap16(&tk, pr.k, BH, pr.N, kD, kBlockN, tt) ||
+        !make_tmap16(&tv, pr.v, BH, pr.N, kD, kBlockN, tt))
+        return FA_ERR_CUDA;
+    Fwd1tParams p{};
+    p.lse = pr.lse;
+    p.o = pr.o;
+    p.block_mask = pr.block_mask;
+    p.kv_len = pr.kv_len;
+    p.status = pr.status;
+    p.H = pr.H;
+    p.N = pr.N;
+    p.nb = pr.nb;
+    p.n_qtiles = (pr.N + kBlockM - 1) / kBlockM;
+    p.scale_log2 = pr.scale * kLog2e;
+    p.out_scale = 1.0f / (1.0f - pr.dropout_p);
+    p.drop_thr = pr.drop_threshold;
+    p.dropout = pr.dropout_p > 0.f;
+    p.causal = pr.causal;
+    p.seed = pr.seed;
+    auto kernel = fwd_1t_kernel<T, kSplit>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+            return FA_ERR_CUDA;
+        // the setmaxnreg budgets must fit in the registers the kernel is
+        // launched with, or the softmax warps would wait forever
+        cudaFuncAttributes a{};
+        if (cudaFuncGetAttributes(&a, kernel) != cudaSuccess ||
+            a.numRegs * kThreads < 128 * kSoftRegs + 128 * kIssueRegs) {
+            if (std::getenv("FA_DEBUG"))
+                std::fprintf(stderr, "fa: fwd_1t register budget exceeds the launch allocation (%d regs)\n", a.numRegs);
+            return FA_ERR_CUDA;
+        }
+        attr_set = true;
+    }
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    if (p.n_qtiles > 65535) return FA_ERR_UNSUPPORTED;
+    cfg.gridDim = dim3(BH, p.n_qtiles);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = pr.stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    record_main_start(pr.stream);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
+    record_main_stop(pr.stream);
+    note_launches(1);
+    if (e != cudaSuccess) {
+        if (std::getenv("FA_DEBUG")) std::fprintf(stderr, "fa: fwd_1t launch: %s\n", cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+}  // namespace
+
+int launch_fwd_1t(const Problem& p) {
+    if (p.dtype == FA_FP16) return p.block_mask ? launch_1t<__half, true>(p) : launch_1t<__half, false>(p);
+    if (p.dtype == FA_BF16) return p.block_mask ? launch_1t<__nv_bfloat16, true>(p) : launch_1t<__nv_bfloat16, false>(p);
+    return FA_ERR_UNSUPPORTED;
+}
+
+}  // namespace fa

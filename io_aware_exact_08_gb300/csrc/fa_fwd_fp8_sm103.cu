@@ -120,15 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             const int qt = 2 * pair + t;
             const int e = n_t[t];
-            const uint8_t* row = p.block_mask + (size_t)qt * p.nb;
-            int cnt = 0;
-            for (int c = 0; c < e; c += 32) {
-                const int j = c + lane;
-                const bool act = j < e && row[j] != 0;
-                const uint32_t bal = __ballot_sync(0xffffffffu, act);
-                if (act) sList[t * kMaskListCap + cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)j;
-                cnt += __popc(bal);
-            }
+            const int cnt =
+                warp_list_visible(p.block_mask + (size_t)qt * p.nb, 1, 0, e, sList + t * kMaskListCap, lane);
             if (lane == 0) st->n_list[t] = cnt;
         }
     }

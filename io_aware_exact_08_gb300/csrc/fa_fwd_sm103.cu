@@ -167,15 +167,8 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             int e = (qt < p.n_qtiles) ? nkt : 0;
             if (p.causal) e = min(e, qt + 1);
             e = min(e, ke);
-            const uint8_t* row = p.block_mask + (size_t)qt * p.nb;
-            int cnt = 0;
-            for (int c = kb & ~31; c < e; c += 32) {
-                const int j = c + lane;
-                const bool act = j >= kb && j < e && row[j] != 0;
-                const uint32_t bal = __ballot_sync(0xffffffffu, act);
-                if (act) sList[t * kMaskListCap + cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)j;
-                cnt += __popc(bal);
-            }
+            const int cnt =
+                warp_list_visible(p.block_mask + (size_t)qt * p.nb, 1, kb, e, sList + t * kMaskListCap, lane);
             if (lane == 0) st->n_list[t] = cnt;
         }
     }
@@ -716,15 +709,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
     if (kSplit && warp == 0) {
         int e = p.causal ? min(nkt, qt + 1) : nkt;
         e = min(e, ke);
-        const uint8_t* row = p.block_mask + (size_t)qt * p.nb;
-        int cnt = 0;
-        for (int c = kb & ~31; c < e; c += 32) {
-            const int j = c + lane;
-            const bool act = j >= kb && j < e && row[j] != 0;
-            const uint32_t bal = __ballot_sync(0xffffffffu, act);
-            if (act) sList[cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)j;
-            cnt += __popc(bal);
-        }
+        const int cnt = warp_list_visible(p.block_mask + (size_t)qt * p.nb, 1, kb, e, sList, lane);
         if (lane == 0) st->n_list = cnt;
     }
     if (tid == 0) {
@@ -1245,6 +1230,8 @@ int launch_fwd_tc_t(const Problem& p) {
         if (p.o_part) return p.block_mask ? launch_fwd256<T, true, true>(p) : launch_fwd256<T, false, true>(p);
         return p.block_mask ? launch_fwd256<T, true, false>(p) : launch_fwd256<T, false, false>(p);
     }
+    // head dim 64 (not split-KV): one query tile per CTA, two CTAs per SM
+    if (p.d == 64 && !p.o_part) return launch_fwd_1t(p);
     // without a block mask both tiles' key lists are prefixes of one list and
     // share its K/V loads; with one, each tile has its own list (kSplit)
     if (p.o_part) {  // split-KV

@@ -78,6 +78,8 @@ cudaError_t launch_dropout_mask(uint8_t* keep, int B, int H, int N, uint32_t thr
 // tcgen05 kernels (bf16, fp16): forward d in {64,128,256} (fa_fwd_sm103.cu),
 // backward d in {64,128} (fa_bwd_sm103.cu) and d = 256 (fa_bwd256_sm103.cu).
 int launch_fwd_tc(const Problem& p);
+// head dim 64, one query tile per CTA, two CTAs per SM (fa_fwd1t_sm103.cu)
+int launch_fwd_1t(const Problem& p);
 
 // FP8 forward (fa_fwd_fp8.cu): E4M3 q, k (Problem::q, k) and the transposed
 // vt (Problem::v), with per-head dequantisation factors; head dim 128.
