@@ -63,6 +63,55 @@ def algorithmic_bytes(w):
     return 4 * bhnd * e + 4 * bhn, 8 * bhnd * e + 8 * bhn
 
 
+def visible_pairs(w, inp):
+    """Number of unmasked (query, key) pairs of the workload: the
+    exponentials the forward needs (the backward recomputes each once more)."""
+    import numpy as np
+    N = w.N
+    kv = inp["kv_len"].numpy().astype(np.int64) if inp.get("kv_len") is not None else np.full(w.B, N)
+    bm = inp["block_mask"].numpy().astype(bool) if inp.get("block_mask") is not None else None
+    total = 0
+    rows = np.arange(N)
+    for b in range(w.B):
+        L = int(min(max(kv[b], 0), N))
+        if bm is None:
+            per_row = np.minimum(rows + 1, L) if w.causal else np.full(N, L)
+            total += int(per_row.sum())
+            continue
+        # block mask: per query block, count keys block by block
+        nb = bm.shape[0]
+        for ib in range(nb):
+            r = rows[ib * 128:(ib + 1) * 128]
+            for jb in np.nonzero(bm[ib])[0]:
+                lo, hi = jb * 128, min((jb + 1) * 128, L)
+                if hi <= lo:
+                    continue
+                if w.causal:
+                    total += int(np.clip(np.minimum(r + 1, hi) - lo, 0, None).sum())
+                else:
+                    total += (hi - lo) * len(r)
+    return total * w.H
+
+
+def measure_ex2_rate(device):
+    """Exponentials per second of the GPU's ex2.approx.f32 (the library's
+    throughput probe, timed with CUDA events)."""
+    import torch
+    import io_aware_exact_08_gb300 as fa
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    blocks, iters = sms * 4, 4096
+    out = torch.empty(blocks * 512, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(2):
+        assert fa.fa_ex2_probe(out.data_ptr(), blocks, iters, stream.cuda_stream) == 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    assert fa.fa_ex2_probe(out.data_ptr(), blocks, iters, stream.cuda_stream) == 0
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    return blocks * 512 * iters * 8 / (a.elapsed_time(b) * 1e-3)
+
+
 def bwd_main_bytes(w):
     """Algorithmic bytes of the backward's main kernel: read Q, K, V, dO,
     LSE and rowsum(dO o O); write dQ, dK, dV."""
@@ -82,22 +131,39 @@ def main_kernel_names(w, splits=1):
     return fwd, bwd
 
 
-def kernel_source_hash():
-    """SHA-256 over the CUDA sources of the library (file names and bytes)."""
+KERNEL_SOURCES = {
+    "fwd_pp_kernel": ["fa_fwd_sm103.cu"],
+    "fwd_d256_kernel": ["fa_fwd_sm103.cu"],
+    "fwd_1t_kernel": ["fa_fwd1t_sm103.cu"],
+    "fwd_fp8_kernel": ["fa_fwd_fp8_sm103.cu"],
+    "bwd_tc_kernel": ["fa_bwd_sm103.cu"],
+    "bwd256_kernel (3 passes)": ["fa_bwd256_sm103.cu"],
+    "fwd_simt_kernel": ["fa_simt.cu"],
+    "bwd_simt_kernels": ["fa_simt.cu"],
+}
+SHARED_HEADERS = ["fa_sm103.cuh", "fa_device.cuh", "fa_internal.h"]
+
+
+def kernel_source_hash(kernel=None):
+    """SHA-256 over the CUDA sources a kernel is built from (its own file and
+    the shared device headers; every source file when kernel is None)."""
     import hashlib
     d = os.path.join(ROOT, "io_aware_exact_08_gb300", "csrc")
+    if kernel is None:
+        files = sorted(fn for fn in os.listdir(d) if fn.endswith((".cu", ".cuh", ".h")))
+    else:
+        files = sorted(KERNEL_SOURCES.get(kernel, []) + SHARED_HEADERS)
     h = hashlib.sha256()
-    for fn in sorted(os.listdir(d)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            h.update(fn.encode())
-            h.update(open(os.path.join(d, fn), "rb").read())
+    for fn in files:
+        h.update(fn.encode())
+        h.update(open(os.path.join(d, fn), "rb").read())
     return h.hexdigest()
 
 
 def recorded_traffic(workload, kernel):
     """DRAM bytes (read + write) of one launch of `kernel` on `workload`, as
     ncu counted them in the capture recorded under profiles/, or None when
-    there is no record or the kernel sources have changed since."""
+    there is no record or the kernel's sources have changed since."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -105,7 +171,7 @@ def recorded_traffic(workload, kernel):
     except (OSError, ValueError):
         return None
     ent = rec.get("kernels", {}).get(workload, {}).get(kernel)
-    if not ent or rec.get("source_sha256") != kernel_source_hash():
+    if not ent or ent.get("source_sha256") != kernel_source_hash(kernel):
         return None
     return int(ent["dram_bytes"])
 
@@ -488,6 +554,16 @@ def run_fa(args, w, ws, rank, device):
                  "algorithmic_flops": dom_f, "algorithmic_bytes": dom_b, "kernel_avg_ms": round(dom_ms, 4),
                  "kernel_ms": {names[0]: round(fwd_k_ms, 4), names[1]: round(bwd_k_ms, 4)}})
 
+    # secondary roofline: the exponentials (one per visible score in the
+    # forward, one more in the backward's recompute) against the measured
+    # ex2 throughput
+    ex2_rate = measure_ex2_rate(device)
+    exps = 2 * visible_pairs(w, inp)
+    exp_ms = exps / ex2_rate * 1e3
+    mufu = {"exp_per_step": exps, "ex2_per_s": round(ex2_rate, 1), "bound_ms": round(exp_ms, 5),
+            "frac_of_step": round(exp_ms / step_ms_max, 4),
+            "fwd_frac": round(exp_ms / 2 / fwd_avg, 4), "bwd_frac": round(exp_ms / 2 / bwd_avg, 4)}
+
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4), "higher_is_better": True,
@@ -498,6 +574,7 @@ def run_fa(args, w, ws, rank, device):
         "frac_of_bf16_peak": round(value / ws / peaks["bf16"], 4) if sixteen else None,
         "fwd_frac_of_bf16_peak": round(fwd_tflops / ws / peaks["bf16"], 4) if sixteen else None,
         "roofline": roof,
+        "exp_roofline": mufu,
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "clocks": clk,

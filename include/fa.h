@@ -231,6 +231,16 @@ int fa_set_kernel_path(int path);
 int fa_test_wait_timeout(uint64_t limit_ns, void* stream);
 
 /*
+ * Diagnostic for the exponential roofline: launches n_blocks blocks of 512
+ * threads, each thread running iters rounds of 8 independent ex2.approx.f32
+ * (the softmax's exponential), so that timing the call gives the GPU's
+ * exponential throughput: n_blocks * 512 * iters * 8 / time. out is
+ * caller-owned device memory of n_blocks * 512 floats (a result that keeps
+ * the work live). Returns FA_ERR_INVALID_ARG for a null out or counts < 1.
+ */
+int fa_ex2_probe(float* out, int n_blocks, int iters, void* stream);
+
+/*
  * Diagnostic: number of CUDA kernels this library has launched in the
  * calling process (all devices, all entry points).
  */

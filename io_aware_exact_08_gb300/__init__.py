@@ -24,7 +24,7 @@ __all__ = [
     "FA_BF16", "FA_FP32", "FA_FP16", "FaError", "load_library", "library_path",
     "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
     "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
-    "fa_set_main_kernel_events", "fa_bwd_noalloc", "fa_fwd_fp8", "attention_fwd_fp8", "FA_BWD_NOALLOC_SCRATCH_BYTES", "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
+    "fa_set_main_kernel_events", "fa_bwd_noalloc", "fa_fwd_fp8", "attention_fwd_fp8", "fa_ex2_probe", "FA_BWD_NOALLOC_SCRATCH_BYTES", "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
 ]
 
 FA_BF16 = 0
@@ -39,7 +39,7 @@ _lock = threading.Lock()
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
             "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
             "fa_bwd_noalloc", "fa_test_wait_timeout", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size",
-            "fa_set_main_kernel_events", "fa_fwd_fp8")
+            "fa_set_main_kernel_events", "fa_fwd_fp8", "fa_ex2_probe")
 
 # Size of the fixed device array fa_bwd_noalloc takes its workspace from.
 FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -92,6 +92,8 @@ def load_library(build_if_missing: bool = True):
         lib.fa_bwd_noalloc.restype = I
         lib.fa_test_wait_timeout.argtypes = [U64, P]
         lib.fa_test_wait_timeout.restype = I
+        lib.fa_ex2_probe.argtypes = [P, I, I, P]
+        lib.fa_ex2_probe.restype = I
         lib.fa_set_main_kernel_events.argtypes = [P, P]
         lib.fa_set_main_kernel_events.restype = I
         lib.fa_launch_count.argtypes = []
@@ -174,6 +176,11 @@ def fa_test_wait_timeout(limit_ns, stream):
 
 def fa_launch_count():
     return int(load_library().fa_launch_count())
+
+
+def fa_ex2_probe(out, n_blocks, iters, stream):
+    """Launches the exponential-throughput probe (see include/fa.h)."""
+    return load_library().fa_ex2_probe(out, int(n_blocks), int(iters), stream)
 
 
 def fa_set_main_kernel_events(ev_start, ev_stop):

@@ -14,19 +14,22 @@ def test_flop_model_matches_formula():
 
 
 def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
-    rec = {"source_sha256": bench.kernel_source_hash(),
-           "kernels": {"gpt2_causal": {"bwd_tc_kernel": {"dram_bytes": 1234}}}}
+    rec = {"kernels": {"gpt2_causal": {"bwd_tc_kernel": {"dram_bytes": 1234,
+                                                         "source_sha256": bench.kernel_source_hash("bwd_tc_kernel")}}}}
     prof = tmp_path / "profiles"
     prof.mkdir()
     (prof / "dram_traffic.json").write_text(json.dumps(rec))
+    real_hash = bench.kernel_source_hash
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     # the hash is taken from the package sources under ROOT: point it back
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["source_sha256"])
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k=None: rec["kernels"]["gpt2_causal"]["bwd_tc_kernel"]
+                        ["source_sha256"] if k == "bwd_tc_kernel" else "x")
     assert bench.recorded_traffic("gpt2_causal", "bwd_tc_kernel") == 1234
     assert bench.recorded_traffic("gpt2_causal", "fwd_pp_kernel") is None
     assert bench.recorded_traffic("long_causal", "bwd_tc_kernel") is None
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 64)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k=None: "0" * 64)
     assert bench.recorded_traffic("gpt2_causal", "bwd_tc_kernel") is None
+    assert real_hash("bwd_tc_kernel") != real_hash("fwd_pp_kernel")
 
 
 def test_source_hash_tracks_kernel_files():
@@ -60,3 +63,17 @@ def test_main_kernel_names_and_bytes():
     bhnd, bhn = w.B * w.H * w.N * w.d, w.B * w.H * w.N
     assert bench.bwd_main_bytes(w) == 7 * bhnd * 2 + 8 * bhn
     assert bench.bwd_main_bytes(w) < bench.algorithmic_bytes(w)[1]
+
+
+def test_visible_pairs_closed_forms():
+    from workloads import Workload, make_inputs
+    w = Workload("t", 0, B=2, H=3, N=300, d=64, dtype="bf16", causal=True)
+    inp = make_inputs(w, with_grad_out=False)
+    assert bench.visible_pairs(w, inp) == 2 * 3 * 300 * 301 // 2
+    w2 = w.with_(causal=False, kv_len_range=(100, 200))
+    inp2 = make_inputs(w2, with_grad_out=False)
+    assert bench.visible_pairs(w2, inp2) == 3 * 300 * int(inp2["kv_len"].sum())
+    w3 = Workload("t", 0, B=1, H=2, N=16384, d=64, dtype="bf16", block_sparse=True)
+    inp3 = make_inputs(w3, with_grad_out=False)
+    dens = float(inp3["block_mask"].double().mean())
+    assert bench.visible_pairs(w3, inp3) == round(2 * 16384 * 16384 * dens)
