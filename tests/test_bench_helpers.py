@@ -19,7 +19,6 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     (prof / "dram_traffic.json").write_text(json.dumps(rec))
-    real_hash = bench.kernel_source_hash
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     # the hash is taken from the package sources under ROOT: point it back
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k=None: rec["kernels"]["gpt2_causal"]["bwd_tc_kernel"]
@@ -29,7 +28,11 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("long_causal", "bwd_tc_kernel") is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k=None: "0" * 64)
     assert bench.recorded_traffic("gpt2_causal", "bwd_tc_kernel") is None
-    assert real_hash("bwd_tc_kernel") != real_hash("fwd_pp_kernel")
+
+
+def test_each_kernel_hashes_its_own_sources():
+    assert bench.kernel_source_hash("bwd_tc_kernel") != bench.kernel_source_hash("fwd_pp_kernel")
+    assert bench.kernel_source_hash("fwd_pp_kernel") == bench.kernel_source_hash("fwd_d256_kernel")
 
 
 def test_source_hash_tracks_kernel_files():
