@@ -89,8 +89,8 @@ def visible_pairs(w, inp):
                 if w.causal:
                     total += int(np.clip(np.minimum(r + 1, hi) - lo, 0, None).sum())
                 else:
-                    total += (hi - lo) * len(r)
-    return total * w.H
+                    total += int(hi - lo) * len(r)
+    return int(total) * w.H
 
 
 def measure_ex2_rate(device):
@@ -126,7 +126,7 @@ def main_kernel_names(w, splits=1):
     of fa_set_main_kernel_events bracket them."""
     if w.dtype not in ("bf16", "fp16"):
         return "fwd_simt_kernel", "bwd_simt_kernels"
-    fwd = "fwd_d256_kernel" if w.d == 256 else "fwd_pp_kernel"
+    fwd = "fwd_d256_kernel" if w.d == 256 else "fwd_1t_kernel" if (w.d == 64 and splits == 1) else "fwd_pp_kernel"
     bwd = "bwd256_kernel (3 passes)" if w.d == 256 else "bwd_tc_kernel"
     return fwd, bwd
 

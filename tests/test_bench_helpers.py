@@ -61,6 +61,8 @@ def test_main_kernel_names_and_bytes():
     w = WORKLOADS["long_causal"]
     assert bench.main_kernel_names(w) == ("fwd_pp_kernel", "bwd_tc_kernel")
     assert bench.main_kernel_names(w.with_(d=256))[0] == "fwd_d256_kernel"
+    assert bench.main_kernel_names(w.with_(d=64))[0] == "fwd_1t_kernel"
+    assert bench.main_kernel_names(w.with_(d=64), splits=2)[0] == "fwd_pp_kernel"
     assert bench.main_kernel_names(WORKLOADS["single_head_fp32"])[0] == "fwd_simt_kernel"
     # the backward's main kernel reads Q, K, V, dO, LSE, delta and writes dQ, dK, dV
     bhnd, bhn = w.B * w.H * w.N * w.d, w.B * w.H * w.N
