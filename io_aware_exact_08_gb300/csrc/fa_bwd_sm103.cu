@@ -71,12 +71,17 @@ struct BwdCfg {
     static constexpr int kBoxes = D / 64;
     static constexpr int kStageBytes = 2 * kTileBytes;  // Q_i and dO_i
     static constexpr int kDsBytes = kTile * kTile * 2;  // dS^T, 128 x 128, 16-bit
+    // D = 64 runs the next step's S^T/dP^T products while the current step's
+    // dQ product still reads dS^T, so the tile is double-buffered by step
+    // parity there
+    static constexpr int kDsBuffers = (D == 64) ? 2 : 1;
     // (no alignment slack: the dynamic shared memory window starts 1024-byte
     // aligned, which the kernel checks)
     // block masks: this key tile's list of visible query tiles
     static constexpr int kListCap = (D == 128) ? kMaskListCapBwd128 : kMaskListCap;
     static constexpr int kSmemBase =
-        2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBytes + 2 * 2 * kTile * 4 /*lse, delta x2*/ + 256;
+        2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBuffers * kDsBytes + 2 * 2 * kTile * 4 /*lse, delta x2*/ +
+        256;
     static constexpr int smem(bool mask) { return kSmemBase + (mask ? kListCap * 2 : 0); }
     static constexpr uint32_t kColS = 0, kColDP = 128;
     // dQ accumulator. D = 128: dQ^T (lanes = head-dim rows, 128 query
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     uint8_t* sDS = sStages + Cfg::kStages * Cfg::kStageBytes;
     // -LSE (log2 units) and -delta of the step's 128 queries, double-buffered
     // by step parity: a warp may stage step it+1 while others still read it
-    float* sNegLse = reinterpret_cast<float*>(sDS + Cfg::kDsBytes);
+    float* sNegLse = reinterpret_cast<float*>(sDS + Cfg::kDsBuffers * Cfg::kDsBytes);
     float* sNegDelta = sNegLse + 2 * kTile;
     BwdShared* st = reinterpret_cast<BwdShared*>(sNegDelta + 2 * kTile);
     uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);
@@ -311,6 +316,93 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const uint64_t kd_mn2 = smem_desc_sw128(k_base, kTile * 128, 1024);    // K, MN-major (M = d)
             bool ok = mbar_wait_warp(&st->kv_full, 0, wctx, 110);
             tc_fence_after();
+            if constexpr (D == 64) {
+            // Software-pipelined order: the next step's S^T_0/dP^T_0 go right
+            // after this step's half-0 gradient products and its S^T_1/dP^T_1
+            // after the dQ product, so the compute warps of one half work on
+            // the next step while the tensor core finishes this one:
+            //   [dV_0 dK_0](t) [S_0 dP_0](t+1) [dV_1 dK_1 dQ](t) [S_1 dP_1](t+1)
+            // Each product that overwrites TMEM (S^T_h, dP^T_h) comes after
+            // the MMAs that read the old contents (in issue order) and after
+            // the compute warps released them (p_ready); dS^T alternates
+            // between two shared-memory tiles by step parity, because the dQ
+            // product of step t reads it after half 0 of step t + 1 may have
+            // started writing.
+            auto issue_sdp = [&](int t2, int h) {
+                const uint32_t qb = smem_u32(sStages + (t2 % Cfg::kStages) * Cfg::kStageBytes);
+                const uint64_t qk = smem_desc_sw128(qb, 16, 1024);
+                const uint64_t dk = smem_desc_sw128(qb + Cfg::kTileBytes, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss_warp(tmem + Cfg::kColS + 64 * h, desc_add(kd_k, kk * 32), desc_add(qk, kk * 32 + 8192 * h),
+                                id_sh, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss_warp(tmem + Cfg::kColDP + 64 * h, desc_add(vd_k, kk * 32), desc_add(dk, kk * 32 + 8192 * h),
+                                id_sh, kk > 0);
+                mma_commit_warp(&st->s_full[h]);
+            };
+            if (ok) ok = mbar_wait_warp(&st->st_full[0], 0, wctx, 111);
+            if (ok) {
+                tc_fence_after();
+                issue_sdp(0, 0);
+                issue_sdp(0, 1);
+            }
+            for (int it = 0; ok && it < n_active; ++it) {
+                const int s = it % Cfg::kStages;
+                const uint32_t q_base = smem_u32(sStages + s * Cfg::kStageBytes);
+                const uint32_t do_base = q_base + Cfg::kTileBytes;
+                const uint64_t qd_mn = smem_desc_sw128(q_base, Cfg::kBoxBytes, 1024);
+                const uint64_t dod_mn = smem_desc_sw128(do_base, Cfg::kBoxBytes, 1024);
+                const uint32_t dsb = (uint32_t)((it & 1) * Cfg::kDsBytes);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (!mbar_wait_warp(&st->p_ready[h], it & 1, wctx, 113)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t acc = (it > 0 || h > 0) ? 1u : 0u;
+                    // dV += P^T_h dO_h (A from TMEM), dK += dS^T_h Q_h
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ts_warp(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
+                                    desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss_warp(tmem + Cfg::kColDK, desc_add(dsd_k, dsb + h * (kTile * 128) + kk * 32),
+                                    desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
+                    if (h == 0) {
+                        if (it + 1 < n_active) {
+                            const int s1 = (it + 1) % Cfg::kStages;
+                            if (!mbar_wait_warp(&st->st_full[s1], ((it + 1) / Cfg::kStages) & 1, wctx, 111)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_sdp(it + 1, 0);
+                        }
+                    } else {
+                        mma_commit_warp(&st->st_empty[s]);  // Q_i, dO_i read
+                        // dQ = dS K_j over the whole tile, over the previous
+                        // step's dQ once it has been read out
+                        if (it > 0) {
+                            if (!mbar_wait_warp(&st->dq_free[0], (it - 1) & 1, wctx, 115)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ss_warp(tmem + Cfg::kColDQ, desc_add(dsd_mn, dsb + kk * 2048), desc_add(kd_mn, kk * 2048),
+                                        id_dq, kk > 0);
+                        mma_commit_warp(&st->dq_full[0]);
+                        if (it + 1 < n_active) issue_sdp(it + 1, 1);
+                    }
+                }
+            }
+            } else {
             for (int it = 0; ok && it < n_active; ++it) {
                 const int s = it % Cfg::kStages;
                 if (!mbar_wait_warp(&st->st_full[s], (it / Cfg::kStages) & 1, wctx, 111)) break;
@@ -413,6 +505,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     if (Cfg::kDqTransposed && h == 1) mma_commit_warp(&st->st_empty[s]);
                     if (with_dq) mma_commit_warp(&st->dq_full[Cfg::kDqTransposed ? h : 0]);
                 }
+            }
             }
             mma_commit_warp(&st->acc_done);
             mma_commit_warp(&st->teardown);
@@ -517,6 +610,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 ok = false;
                 break;
             }
+            // dropout keep bits of this row's 64 query columns, drawn before
+            // S^T arrives (bit x of keep_w[ch] is query column
+            // 64 half + 32 ch + x): lane (4a + w) draws the 4 keep bits of
+            // keys 4a..4a+3 for one query and the group exchanges them
+            uint32_t keep_w[2] = {0xffffffffu, 0xffffffffu};
+            if (p.dropout) {
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    const int cb = half * 64 + ch * 32;
+                    uint32_t keep = 0;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const int qi = i0 + cb + 4 * g + (lane & 3);
+                        const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, qi, jrow >> 2);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t v = __shfl_sync(0xffffffffu, bits, (lane & ~3) | q);
+                            keep |= ((v >> (lane & 3)) & 1u) << (4 * g + q);
+                        }
+                    }
+                    keep_w[ch] = keep;
+                }
+            }
             if (!mbar_wait_warp(&st->s_full[half], it & 1, wctx, 120)) {
                 ok = false;
                 break;
@@ -527,30 +643,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             if (p.causal) cmin = max(0, jrow - i0);
             const int cmax = key_ok ? min(kTile, p.N - i0) : 0;
 #pragma unroll
+            // at D = 64 both chunks of S^T and dP^T are loaded with one TMEM
+            // wait (the registers allow it there); at D = 128 one chunk at a
+            // time
+            constexpr bool kLoadBoth = (D == 64);
+            uint32_t sr2[2][32], dr2[2][32];
+            if constexpr (kLoadBoth) {
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    tmem_ld32(tmem + lane_base + Cfg::kColS + half * 64 + ch * 32, sr2[ch]);
+                    tmem_ld32(tmem + lane_base + Cfg::kColDP + half * 64 + ch * 32, dr2[ch]);
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    reg_fence(sr2[ch]);
+                    reg_fence(dr2[ch]);
+                }
+            }
+#pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
                 const int cb = half * 64 + ch * 32;  // first query column of this chunk
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_base + Cfg::kColS + cb, sr);
-                tmem_ld32(tmem + lane_base + Cfg::kColDP + cb, dr);
-                tmem_ld_wait();
-                reg_fence(sr);
-                reg_fence(dr);
-                uint32_t keep = 0xffffffffu;
-                if (p.dropout) {
-                    keep = 0;
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        // lane (4a + w) draws the 4 keep bits of keys 4a..4a+3
-                        // for query cb + 4g + w; the group exchanges them
-                        const int qi = i0 + cb + 4 * g + (lane & 3);
-                        const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, qi, jrow >> 2);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint32_t v = __shfl_sync(0xffffffffu, bits, (lane & ~3) | q);
-                            keep |= ((v >> (lane & 3)) & 1u) << (4 * g + q);
-                        }
-                    }
+                uint32_t(&sr)[32] = sr2[ch];
+                uint32_t(&dr)[32] = dr2[ch];
+                if constexpr (!kLoadBoth) {
+                    tmem_ld32(tmem + lane_base + Cfg::kColS + cb, sr);
+                    tmem_ld32(tmem + lane_base + Cfg::kColDP + cb, dr);
+                    tmem_ld_wait();
+                    reg_fence(sr);
+                    reg_fence(dr);
                 }
+                const uint32_t keep = keep_w[ch];
                 const bool edge = (cmin > cb) || (cmax < cb + 32);
                 uint32_t pk[16];
                 uint32_t dsk[16];
@@ -612,7 +735,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 // P^T into TMEM columns this warp has already read
                 tmem_st16(tmem + lane_base + Cfg::kColS + half * 64 + ch * 16, pk);
                 // dS^T row r, queries cb..cb+31: 4 swizzled 16-byte chunks
-                uint8_t* row = sDS + half * (kTile * 128) + r * 128;
+                uint8_t* row = sDS + (it & (Cfg::kDsBuffers - 1)) * Cfg::kDsBytes + half * (kTile * 128) + r * 128;
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const int chunk = ch * 4 + v;
