@@ -29,6 +29,7 @@
 // complete the third warpgroup), warps 12-15 dQ reduction (one per TMEM lane
 // quarter), so that the compute warps never wait for the dQ product or for
 // the reductions to drain into L2.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -103,6 +104,7 @@ struct BwdParams {
     const int32_t* kv_len;
     int* status;
     int H, N, nb;
+    int BH, nkt;  // heads x batch, key tiles: the work items are (bh, key tile)
     float scale;
     float scale_log2;
     float keep_scale;  // 1/(1-p)
@@ -121,6 +123,8 @@ struct BwdShared {
     uint64_t dq_full[2];   // dQ of half h (D = 128) / of the tile (D = 64, [0])
     uint64_t dq_free[2];   // that dQ read out of TMEM by the reduction warps
     uint64_t acc_done;
+    uint64_t acc_free;     // dK, dV of the item read out of TMEM by the compute warps
+    uint64_t kv_empty;     // K_j, V_j read by the item's last MMA
     uint64_t teardown;
     uint64_t lse_ready[2];
     uint32_t tmem_base;
@@ -183,6 +187,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
     using Cfg = BwdCfg<D>;
+    // the persistent grid (several items per CTA) is used at D = 128 without a
+    // block mask; otherwise every CTA runs exactly one item
+    constexpr bool kPersist = (D == 128) && !kMask;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0 && atomicCAS(p.status, 0, (int)FA_ERR_CUDA) == 0) atomicExch(p.status + 1, 130);
@@ -200,26 +207,43 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // grid (B*H, key tiles): dispatched x fastest, so under a causal mask the
-    // heaviest key tiles (lowest j) of every head go out first
-    const int bh = blockIdx.x;
-    const int b = bh / p.H, h = bh % p.H;
-    const int jt = blockIdx.y;
-    const int j0 = jt * kTile;
-
-    QSched<kMask> sched;
-    sched.jt = jt;
-    sched.nqt = (p.N + kTile - 1) / kTile;
-    sched.L = p.kv_len ? min(max(p.kv_len[b], 0), p.N) : p.N;
-    sched.causal = p.causal;
-    sched.list = sList;
-    sched.n_list = 0;
+    // Work items are (bh, key tile) pairs, item = bh + BH * key tile, so
+    // under a causal mask the heaviest key tiles (lowest j) of every head come
+    // first. At D = 128 without a block mask the grid is persistent (one CTA
+    // per SM), each CTA walking its items (item_of below); the barriers run on across
+    // items, counted by the global step gs + it and the item count gi, so the
+    // next item's loads and first products overlap the previous item's last
+    // products and its dK/dV stores. Otherwise each CTA takes one item (with
+    // a block mask, its list of query tiles is built once, below).
+    const int n_items = p.BH * p.nkt;
+    const int n_ctas = gridDim.x * gridDim.y;
+    const int cta = blockIdx.x + blockIdx.y * gridDim.x;
+    // the CTA's r-th item: items go out in rounds of n_ctas, left to right
+    // in even rounds and right to left in odd ones, so every CTA gets a mix
+    // of the heavy (early) and light (late) causal items
+    auto item_of = [&](int r) {
+        return r * n_ctas + ((r & 1) ? (n_ctas - 1 - cta) : cta);
+    };
+    const int item0 = item_of(0);
+    const int nqt = (p.N + kTile - 1) / kTile;
+    auto make_sched = [&](int item) {
+        QSched<kMask> q;
+        const int bh_ = item % p.BH;
+        q.jt = item / p.BH;
+        q.nqt = nqt;
+        q.L = p.kv_len ? min(max(p.kv_len[bh_ / p.H], 0), p.N) : p.N;
+        q.causal = p.causal;
+        q.list = sList;
+        q.n_list = 0;
+        return q;
+    };
     WaitCtx wctx{&st->abort_flag, p.status};
-    // block mask: warp 0 lists the query tiles whose mask block (i, j) is set
-    // (strided loads of one mask column, 32 at a time, and a ballot)
-    if (kMask && warp == 0) {
-        const int first = p.causal ? jt : 0;
-        const int cnt = warp_list_visible(p.block_mask + jt, (size_t)p.nb, first, sched.nqt, sList, lane);
+    // block mask (one item per CTA): warp 0 lists the query tiles whose mask
+    // block (i, j) is set (strided loads of one mask column and a ballot)
+    if (kMask && warp == 0 && item0 < n_items) {
+        const int jt0 = item0 / p.BH;
+        const int first = p.causal ? jt0 : 0;
+        const int cnt = warp_list_visible(p.block_mask + jt0, (size_t)p.nb, first, nqt, sList, lane);
         if (lane == 0) st->n_list = cnt;
     }
 
@@ -237,6 +261,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             mbar_init(&st->lse_ready[h], kComputeThreads / 64);
         }
         mbar_init(&st->acc_done, 1);
+        mbar_init(&st->acc_free, kComputeThreads / 32);
+        mbar_init(&st->kv_empty, 1);
         mbar_init(&st->teardown, 1);
         st->abort_flag = 0;
         fence_mbar_init();
@@ -249,8 +275,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = st->tmem_base;
-    if constexpr (kMask) sched.n_list = st->n_list;
-    const int n_active = sched.count();
+    // the item's query-step schedule and number of steps
+    auto item_sched = [&](int item, int& n_active) {
+        QSched<kMask> q = make_sched(item);
+        if constexpr (kMask) q.n_list = st->n_list;
+        n_active = q.count();
+        return q;
+    };
     // The next kernel (dq conversion) may start launching once every CTA is
     // here. Q, K, V, dO and LSE were complete before the preprocess kernel
     // ran, so the producer and MMA warps start at once; the compute and
@@ -260,39 +291,66 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (warp == 8) {
         // ------------------------------------------------------------ producer
         regs_dec<Cfg::kIssueRegs>();
-        if (lane == 0 && n_active > 0) {
+        if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
-            mbar_arrive_expect_tx(&st->kv_full, 2 * Cfg::kTileBytes);
-#pragma unroll
-            for (int x = 0; x < Cfg::kBoxes; ++x) {
-                tma_load_3d(sK + x * Cfg::kBoxBytes, &tm_k, &st->kv_full, x * 64, j0, bh);
-                tma_load_3d(sV + x * Cfg::kBoxBytes, &tm_v, &st->kv_full, x * 64, j0, bh);
-            }
             uint32_t issued_phase[Cfg::kStages];
             bool issued_any[Cfg::kStages];
             for (int s = 0; s < Cfg::kStages; ++s) issued_any[s] = false;
-            int t = 0;
-            for (int i = sched.first(); i < sched.nqt; i = sched.after(i, t), ++t) {
-                const int s = t % Cfg::kStages;
-                const uint32_t ph = (t / Cfg::kStages) & 1;
-                if (!mbar_wait(&st->st_empty[s], ph ^ 1, wctx, 101)) break;
-                mbar_arrive_expect_tx(&st->st_full[s], Cfg::kStageBytes);
-                uint8_t* dq = sStages + s * Cfg::kStageBytes;
-                uint8_t* ddo = dq + Cfg::kTileBytes;
+            bool okp = true;
+            int gs = 0, gi = 0;  // steps and items with work, so far
+            for (int rr = 0, item = item0; okp && item < n_items && (kPersist || rr == 0); item = item_of(++rr)) {
+                int n_active;
+                const QSched<kMask> sched = item_sched(item, n_active);
+                if (n_active == 0) continue;
+                const int bh = item % p.BH;
+                const int j0 = sched.jt * kTile;
+                // Q_i, dO_i of step t (global step gs + t) into its stage
+                auto load_step = [&](int i, int t) -> bool {
+                    const int g = gs + t;
+                    const int s = g % Cfg::kStages;
+                    const uint32_t ph = (g / Cfg::kStages) & 1;
+                    if (!mbar_wait(&st->st_empty[s], ph ^ 1, wctx, 101)) return false;
+                    mbar_arrive_expect_tx(&st->st_full[s], Cfg::kStageBytes);
+                    uint8_t* dq = sStages + s * Cfg::kStageBytes;
+                    uint8_t* ddo = dq + Cfg::kTileBytes;
+#pragma unroll
+                    for (int x = 0; x < Cfg::kBoxes; ++x) {
+                        tma_load_3d(dq + x * Cfg::kBoxBytes, &tm_q, &st->st_full[s], x * 64, i * kTile, bh);
+                        tma_load_3d(ddo + x * Cfg::kBoxBytes, &tm_do, &st->st_full[s], x * 64, i * kTile, bh);
+                    }
+                    issued_phase[s] = ph;
+                    issued_any[s] = true;
+                    return true;
+                };
+                // the item's first Q_i, dO_i go ahead of K_j, V_j: their stage
+                // frees before the previous item's last MMA has run
+                int i = sched.first();
+                if (!load_step(i, 0)) break;
+                i = sched.after(i, 0);
+                // K_j, V_j once the previous item's MMAs have read theirs
+                if (gi > 0 && !mbar_wait(&st->kv_empty, (gi - 1) & 1, wctx, 104)) break;
+                mbar_arrive_expect_tx(&st->kv_full, 2 * Cfg::kTileBytes);
 #pragma unroll
                 for (int x = 0; x < Cfg::kBoxes; ++x) {
-                    tma_load_3d(dq + x * Cfg::kBoxBytes, &tm_q, &st->st_full[s], x * 64, i * kTile, bh);
-                    tma_load_3d(ddo + x * Cfg::kBoxBytes, &tm_do, &st->st_full[s], x * 64, i * kTile, bh);
+                    tma_load_3d(sK + x * Cfg::kBoxBytes, &tm_k, &st->kv_full, x * 64, j0, bh);
+                    tma_load_3d(sV + x * Cfg::kBoxBytes, &tm_v, &st->kv_full, x * 64, j0, bh);
                 }
-                issued_phase[s] = ph;
-                issued_any[s] = true;
+                for (int t = 1; i < sched.nqt; i = sched.after(i, t), ++t) {
+                    if (!load_step(i, t)) {
+                        okp = false;
+                        break;
+                    }
+                }
+                gs += n_active;
+                ++gi;
             }
+            // drain: the last load issued into each stage, and the last K/V
             for (int s = 0; s < Cfg::kStages; ++s)
                 if (issued_any[s]) mbar_wait(&st->st_full[s], issued_phase[s], wctx, 102);
-            mbar_wait(&st->kv_full, 0, wctx, 103);
+            if (gi > 0) mbar_wait(&st->kv_full, (gi - 1) & 1, wctx, 103);
         }
     } else if (warp == 10 || warp == 11) {
         // idle: the rest of the producer / MMA warpgroup
@@ -301,7 +359,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         regs_dec<Cfg::kIssueRegs>();
         // the whole warp runs the issue loop; one elected lane issues
-        if (n_active > 0) {
+        {
             constexpr uint32_t id_sh = idesc_f32acc(Elem16<T>::kFmt, kTile, 64, 0, 0);      // S^T_h, dP^T_h (N = 64)
             constexpr uint32_t id_dv = idesc_f32acc(Elem16<T>::kFmt, kTile, D, 0, 1);      // dV (A tmem), dK (A K-major)
             constexpr uint32_t id_dqt_h = idesc_f32acc(Elem16<T>::kFmt, kTile, 64, 1, 1);   // dQ^T_h (A, B MN-major, N = 64)
@@ -314,7 +372,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const uint64_t dsd_mn = smem_desc_sw128(ds_base, kTile * 128, 1024);  // dS^T, MN-major
             const uint64_t kd_mn = smem_desc_sw128(k_base, Cfg::kBoxBytes, 1024);  // K, MN-major (N = d)
             const uint64_t kd_mn2 = smem_desc_sw128(k_base, kTile * 128, 1024);    // K, MN-major (M = d)
-            bool ok = mbar_wait_warp(&st->kv_full, 0, wctx, 110);
+            bool ok = true;
+            int gs = 0, gi = 0;  // steps and items with work, so far
+            for (int rr = 0, item = item0; ok && item < n_items && (kPersist || rr == 0); item = item_of(++rr)) {
+            int n_active;
+            (void)item_sched(item, n_active);
+            if (n_active == 0) continue;
+            if (!mbar_wait_warp(&st->kv_full, gi & 1, wctx, 110)) break;
             tc_fence_after();
             if constexpr (D == 64) {
             // Software-pipelined order: the next step's S^T_0/dP^T_0 go right
@@ -328,8 +392,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             // between two shared-memory tiles by step parity, because the dQ
             // product of step t reads it after half 0 of step t + 1 may have
             // started writing.
-            auto issue_sdp = [&](int t2, int h) {
-                const uint32_t qb = smem_u32(sStages + (t2 % Cfg::kStages) * Cfg::kStageBytes);
+            auto issue_sdp = [&](int g2, int h) {  // g2: global step
+                const uint32_t qb = smem_u32(sStages + (g2 % Cfg::kStages) * Cfg::kStageBytes);
                 const uint64_t qk = smem_desc_sw128(qb, 16, 1024);
                 const uint64_t dk = smem_desc_sw128(qb + Cfg::kTileBytes, 16, 1024);
 #pragma unroll
@@ -342,26 +406,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                                 id_sh, kk > 0);
                 mma_commit_warp(&st->s_full[h]);
             };
-            if (ok) ok = mbar_wait_warp(&st->st_full[0], 0, wctx, 111);
+            if (ok) ok = mbar_wait_warp(&st->st_full[gs % Cfg::kStages], (gs / Cfg::kStages) & 1, wctx, 111);
             if (ok) {
                 tc_fence_after();
-                issue_sdp(0, 0);
-                issue_sdp(0, 1);
+                issue_sdp(gs, 0);
+                issue_sdp(gs, 1);
             }
             for (int it = 0; ok && it < n_active; ++it) {
-                const int s = it % Cfg::kStages;
+                const int g = gs + it;
+                const int s = g % Cfg::kStages;
                 const uint32_t q_base = smem_u32(sStages + s * Cfg::kStageBytes);
                 const uint32_t do_base = q_base + Cfg::kTileBytes;
                 const uint64_t qd_mn = smem_desc_sw128(q_base, Cfg::kBoxBytes, 1024);
                 const uint64_t dod_mn = smem_desc_sw128(do_base, Cfg::kBoxBytes, 1024);
-                const uint32_t dsb = (uint32_t)((it & 1) * Cfg::kDsBytes);
+                const uint32_t dsb = (uint32_t)((g & 1) * Cfg::kDsBytes);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    if (!mbar_wait_warp(&st->p_ready[h], it & 1, wctx, 113)) {
+                    if (!mbar_wait_warp(&st->p_ready[h], g & 1, wctx, 113)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    // the item's first products overwrite dV, dK: the compute
+                    // warps must have read out the previous item's
+                    if (it == 0 && h == 0 && gi > 0) {
+                        if (!mbar_wait_warp(&st->acc_free, (gi - 1) & 1, wctx, 116)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
                     const uint32_t acc = (it > 0 || h > 0) ? 1u : 0u;
                     // dV += P^T_h dO_h (A from TMEM), dK += dS^T_h Q_h
 #pragma unroll
@@ -374,20 +448,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                                     desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
                     if (h == 0) {
                         if (it + 1 < n_active) {
-                            const int s1 = (it + 1) % Cfg::kStages;
-                            if (!mbar_wait_warp(&st->st_full[s1], ((it + 1) / Cfg::kStages) & 1, wctx, 111)) {
+                            const int s1 = (g + 1) % Cfg::kStages;
+                            if (!mbar_wait_warp(&st->st_full[s1], ((g + 1) / Cfg::kStages) & 1, wctx, 111)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            issue_sdp(it + 1, 0);
+                            issue_sdp(g + 1, 0);
                         }
                     } else {
                         mma_commit_warp(&st->st_empty[s]);  // Q_i, dO_i read
                         // dQ = dS K_j over the whole tile, over the previous
                         // step's dQ once it has been read out
-                        if (it > 0) {
-                            if (!mbar_wait_warp(&st->dq_free[0], (it - 1) & 1, wctx, 115)) {
+                        if (g > 0) {
+                            if (!mbar_wait_warp(&st->dq_free[0], (g - 1) & 1, wctx, 115)) {
                                 ok = false;
                                 break;
                             }
@@ -398,14 +472,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                             mma_ss_warp(tmem + Cfg::kColDQ, desc_add(dsd_mn, dsb + kk * 2048), desc_add(kd_mn, kk * 2048),
                                         id_dq, kk > 0);
                         mma_commit_warp(&st->dq_full[0]);
-                        if (it + 1 < n_active) issue_sdp(it + 1, 1);
+                        if (it + 1 < n_active) issue_sdp(g + 1, 1);
                     }
                 }
             }
             } else {
+            // D = 128: per 64-query half h, S^T_h = K_j Q_{i,h}^T and
+            // dP^T_h = V_j dO_{i,h}^T (N = 64); half 1's products run while
+            // the compute warps of half 0 work, and half 0's gradient MMAs
+            // while half 1's do. dP^T_h overwrites the previous step's dQ^T_h
+            // once the reduction warps have read it out.
             for (int it = 0; ok && it < n_active; ++it) {
-                const int s = it % Cfg::kStages;
-                if (!mbar_wait_warp(&st->st_full[s], (it / Cfg::kStages) & 1, wctx, 111)) break;
+                const int g = gs + it;
+                const int s = g % Cfg::kStages;
+                if (!mbar_wait_warp(&st->st_full[s], (g / Cfg::kStages) & 1, wctx, 111)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t q_base = smem_u32(sStages + s * Cfg::kStageBytes);
                 const uint32_t do_base = q_base + Cfg::kTileBytes;
@@ -413,10 +496,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 const uint64_t dod_k = smem_desc_sw128(do_base, 16, 1024);
                 const uint64_t qd_mn = smem_desc_sw128(q_base, Cfg::kBoxBytes, 1024);
                 const uint64_t dod_mn = smem_desc_sw128(do_base, Cfg::kBoxBytes, 1024);
-                // Per 64-query half h (h = 0, 1): S^T_h = K_j Q_{i,h}^T and
-                // dP^T_h = V_j dO_{i,h}^T (N = 64). Half 1's products run
-                // while the compute warps of half 0 work, and half 0's
-                // gradient MMAs while half 1's do.
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -425,9 +504,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         mma_ss_warp(tmem + Cfg::kColS + 64 * h, desc_add(kd_k, off), desc_add(qd_k, off + 8192 * h), id_sh,
                                kk > 0);
                     }
-                    // at D = 128, dP^T_h overwrites the previous tile's dQ^T_h
-                    if (D == 128 && it > 0) {
-                        if (!mbar_wait_warp(&st->dq_free[h], (it - 1) & 1, wctx, 112)) {
+                    if (g > 0) {
+                        if (!mbar_wait_warp(&st->dq_free[h], (g - 1) & 1, wctx, 112)) {
                             ok = false;
                             break;
                         }
@@ -444,72 +522,58 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 if (!ok) break;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    if (!mbar_wait_warp(&st->p_ready[h], it & 1, wctx, 113)) {
+                    if (!mbar_wait_warp(&st->p_ready[h], g & 1, wctx, 113)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // dV += P^T_h dO_h (P^T_h, 16-bit, in TMEM columns 64h..64h+31) and
-                    // dK += dS^T_h Q_h (dS^T half h is shared-memory box h),
-                    // at D = 128 interleaved with dQ so that consecutive MMAs
-                    // go to different accumulators:
-                    //   D = 128: dQ^T_h = K_j^T dS^T_h (M = head dim, N = 64
-                    //     queries: lane = head-dim index, so one reduction
-                    //     instruction covers 32 consecutive floats of a row);
-                    //   D = 64, with half 1: dQ = dS K_j over the whole tile
-                    //     (M = 128 queries, lane = query), over the previous
-                    //     tile's dQ once it has been read out.
-                    const uint32_t acc = (it > 0 || h > 0) ? 1u : 0u;
-                    const bool with_dq = Cfg::kDqTransposed || h == 1;
-                    if constexpr (Cfg::kDqTransposed) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            mma_ts_warp(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
-                                        desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int k2 = 2 * kk + e;
-                                mma_ss_warp(tmem + Cfg::kColDQ + 64 * h, desc_add(kd_mn2, k2 * 2048),
-                                            desc_add(dsd_mn, h * (kTile * 128) + k2 * 2048), id_dqt_h, k2 > 0);
-                                if (e == 0)
-                                    mma_ss_warp(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
-                                                desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
-                            }
+                    // the item's first products overwrite dV, dK: the compute
+                    // warps must have read out the previous item's
+                    if (it == 0 && h == 0 && gi > 0) {
+                        if (!mbar_wait_warp(&st->acc_free, (gi - 1) & 1, wctx, 116)) {
+                            ok = false;
+                            break;
                         }
-                    } else {
-                        // (at D = 64 the products go one after the other, which
-                        // measured faster there)
+                        tc_fence_after();
+                    }
+                    // dV += P^T_h dO_h (P^T_h, 16-bit, in TMEM columns
+                    // 64h..64h+31) and dK += dS^T_h Q_h (dS^T half h is
+                    // shared-memory box h), interleaved with
+                    // dQ^T_h = K_j^T dS^T_h (M = head dim, N = 64 queries:
+                    // lane = head-dim index, so one reduction instruction
+                    // covers 32 consecutive floats of a row) so that
+                    // consecutive MMAs go to different accumulators
+                    const uint32_t acc = (it > 0 || h > 0) ? 1u : 0u;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ts_warp(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
-                                        desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        mma_ts_warp(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
+                                    desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss_warp(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
-                                        desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
-                        if (h == 1) mma_commit_warp(&st->st_empty[s]);  // Q_i, dO_i read
-                        if (with_dq) {
-                            if (it > 0) {
-                                if (!mbar_wait_warp(&st->dq_free[0], (it - 1) & 1, wctx, 115)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                            }
-#pragma unroll
-                            for (int kk = 0; kk < kTile / 16; ++kk)
-                                mma_ss_warp(tmem + Cfg::kColDQ, desc_add(dsd_mn, kk * 2048), desc_add(kd_mn, kk * 2048),
-                                            id_dq, kk > 0);
+                        for (int e = 0; e < 2; ++e) {
+                            const int k2 = 2 * kk + e;
+                            mma_ss_warp(tmem + Cfg::kColDQ + 64 * h, desc_add(kd_mn2, k2 * 2048),
+                                        desc_add(dsd_mn, h * (kTile * 128) + k2 * 2048), id_dqt_h, k2 > 0);
+                            if (e == 0)
+                                mma_ss_warp(tmem + Cfg::kColDK, desc_add(dsd_k, h * (kTile * 128) + kk * 32),
+                                            desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
                         }
                     }
-                    if (Cfg::kDqTransposed && h == 1) mma_commit_warp(&st->st_empty[s]);
-                    if (with_dq) mma_commit_warp(&st->dq_full[Cfg::kDqTransposed ? h : 0]);
+                    if (h == 1) mma_commit_warp(&st->st_empty[s]);  // Q_i, dO_i read
+                    mma_commit_warp(&st->dq_full[h]);
                 }
             }
             }
+            // the item's K_j, V_j are read by every MMA issued so far; dK, dV
+            // are complete when these arrive
+            mma_commit_warp(&st->kv_empty);
             mma_commit_warp(&st->acc_done);
-            mma_commit_warp(&st->teardown);
-            mbar_wait_warp(&st->teardown, 0, wctx, 114);
+            gs += n_active;
+            ++gi;
+            }
+            if (gi > 0) {
+                mma_commit_warp(&st->teardown);
+                mbar_wait_warp(&st->teardown, 0, wctx, 114);
+            }
         }
     } else if (warp >= Cfg::kReduceWarp0) {
         // ------------------------------------------------------------ dQ reduction
@@ -520,15 +584,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int quarter = warp & 3;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const int r = quarter * 32 + lane;
-        bool ok = n_active > 0;
-        int it = 0;
+        bool ok = true;
+        int gs = 0;  // steps with work, so far
         pdl_wait();
+        for (int rr = 0, item = item0; ok && item < n_items && (kPersist || rr == 0); item = item_of(++rr)) {
+        int n_active;
+        const QSched<kMask> sched = item_sched(item, n_active);
+        if (n_active == 0) continue;
+        const int bh = item % p.BH;
+        int it = 0;
         for (int i = sched.first(); ok && i < sched.nqt; i = sched.after(i, it), ++it) {
+            const int g = gs + it;
             const int i0 = i * kTile;
             const int nvalid = min(kTile, p.N - i0);
 #pragma unroll
             for (int h = 0; h < (Cfg::kDqTransposed ? 2 : 1); ++h) {
-                if (!mbar_wait_warp(&st->dq_full[h], it & 1, wctx, 121)) {
+                if (!mbar_wait_warp(&st->dq_full[h], g & 1, wctx, 121)) {
                     ok = false;
                     break;
                 }
@@ -564,38 +635,60 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 }
             }
         }
+        gs += n_active;
+        }
     } else {
         // ------------------------------------------------------------ compute
         regs_inc<Cfg::kComputeRegs>();
         const int quarter = warp & 3;      // TMEM lane quarter
         const int half = warp >> 2;        // query columns [64*half, 64*half + 64)
         const int r = quarter * 32 + lane;  // key row within the tile
-        const int jrow = j0 + r;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const bool key_ok = jrow < sched.L;
-        bool ok = true;
-        int it = 0;
         // each warpgroup stages its own 64 query columns: row r < 64 the LSE
         // of column 64 half + r, row r >= 64 the delta of column
         // 64 half + r - 64; the value for the next tile is loaded early
         const int col = 64 * half + (r & 63);
         const bool stage_lse = r < 64;
-        const float* col_src = (stage_lse ? p.lse : p.delta) + (size_t)bh * p.N;
-        const int nqt = sched.nqt;
-        int i_cur = sched.first();
-        float col_val = 0.f;
+        bool ok = true;
+        int gs = 0, gi = 0;  // steps and items with work, so far
         pdl_wait();
-        if (n_active > 0) {
+        for (int rr = 0, item = item0; ok && item < n_items && (kPersist || rr == 0); item = item_of(++rr)) {
+        int n_active;
+        const QSched<kMask> sched = item_sched(item, n_active);
+        const int bh = item % p.BH;
+        const int b = bh / p.H, h = bh % p.H;
+        const int j0 = sched.jt * kTile;
+        const int jrow = j0 + r;
+        const bool key_ok = jrow < sched.L;
+        if (n_active == 0) {
+            // no query sees this key tile: dK = dV = 0 on its rows
+            if (jrow < p.N) {
+#pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    T* out = static_cast<T*>(which ? p.dv : p.dk) + ((size_t)bh * p.N + jrow) * D;
+                    uint4* dst = reinterpret_cast<uint4*>(out + half * (D / 2));
+#pragma unroll
+                    for (int v = 0; v < D / 16; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            continue;
+        }
+        const float* col_src = (stage_lse ? p.lse : p.delta) + (size_t)bh * p.N;
+        int it = 0;
+        int i_cur = sched.first();
+        float col_val;
+        {
             const int qi = i_cur * kTile + col;
             col_val = (qi < p.N) ? col_src[qi] : (stage_lse ? -INFINITY : 0.f);
         }
-        for (int i = i_cur; n_active > 0 && i < sched.nqt; ++it) {
+        for (int i = i_cur; i < sched.nqt; ++it) {
+            const int g = gs + it;
             const int i0 = i * kTile;
             const int i_next = sched.after(i, it);
             // per-query -LSE (log2 units; -inf for masked rows so P = 0) and
             // -delta, negated so that each pair of columns takes one paired
             // fma / add
-            const int lbuf = (it & 1) * kTile;
+            const int lbuf = (g & 1) * kTile;
             if (stage_lse)
                 sNegLse[lbuf + col] = (col_val == -INFINITY) ? -INFINITY : -(col_val * kLog2e);
             else
@@ -606,7 +699,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             }
             // (an mbarrier rather than a named barrier, so the wait is bounded)
             mbar_arrive_warp(&st->lse_ready[half]);
-            if (!mbar_wait_warp(&st->lse_ready[half], it & 1, wctx, 123)) {
+            if (!mbar_wait_warp(&st->lse_ready[half], g & 1, wctx, 123)) {
                 ok = false;
                 break;
             }
@@ -633,7 +726,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     keep_w[ch] = keep;
                 }
             }
-            if (!mbar_wait_warp(&st->s_full[half], it & 1, wctx, 120)) {
+            if (!mbar_wait_warp(&st->s_full[half], g & 1, wctx, 120)) {
                 ok = false;
                 break;
             }
@@ -642,7 +735,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             int cmin = 0;
             if (p.causal) cmin = max(0, jrow - i0);
             const int cmax = key_ok ? min(kTile, p.N - i0) : 0;
-#pragma unroll
             // at D = 64 both chunks of S^T and dP^T are loaded with one TMEM
             // wait (the registers allow it there); at D = 128 one chunk at a
             // time
@@ -735,7 +827,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 // P^T into TMEM columns this warp has already read
                 tmem_st16(tmem + lane_base + Cfg::kColS + half * 64 + ch * 16, pk);
                 // dS^T row r, queries cb..cb+31: 4 swizzled 16-byte chunks
-                uint8_t* row = sDS + (it & (Cfg::kDsBuffers - 1)) * Cfg::kDsBytes + half * (kTile * 128) + r * 128;
+                uint8_t* row = sDS + (g & (Cfg::kDsBuffers - 1)) * Cfg::kDsBytes + half * (kTile * 128) + r * 128;
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const int chunk = ch * 4 + v;
@@ -749,40 +841,54 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             mbar_arrive_warp(&st->p_ready[half]);
             i = i_next;
         }
-        // epilogue: dK = scale * acc, dV = acc, rows of this key tile
-        T* dK = static_cast<T*>(p.dk) + ((size_t)bh * p.N) * D;
-        T* dV = static_cast<T*>(p.dv) + ((size_t)bh * p.N) * D;
-        const bool have = ok && n_active > 0 && mbar_wait_warp(&st->acc_done, 0, wctx, 122);
-        if (have) tc_fence_after();
+        if (!ok) break;
+        // epilogue: dK = scale * acc, dV = acc, rows of this key tile. The
+        // accumulators are read out of TMEM and released (acc_free) before
+        // the stores, so the next item's products can start meanwhile.
+        if (!mbar_wait_warp(&st->acc_done, gi & 1, wctx, 122)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        uint32_t ar[2][D / 64][32];
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            T* out = which ? dV : dK;
-            const float mul = which ? 1.f : p.scale;
-            const uint32_t col0 = (which ? Cfg::kColDV : Cfg::kColDK) + half * (D / 2);
+        for (int which = 0; which < 2; ++which)
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t ar[32];
-                if (have) {
-                    tmem_ld32(tmem + lane_base + col0 + c * 32, ar);
-                    tmem_ld_wait();
-                    reg_fence(ar);
-                } else {
+            for (int c = 0; c < D / 64; ++c)
+                tmem_ld32(tmem + lane_base + (which ? Cfg::kColDV : Cfg::kColDK) + half * (D / 2) + c * 32, ar[which][c]);
+        tmem_ld_wait();
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) ar[x] = 0u;
-                }
-                if (jrow < p.N) {
+        for (int which = 0; which < 2; ++which)
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) reg_fence(ar[which][c]);
+        tc_fence_before();
+        mbar_arrive_warp(&st->acc_free);
+        if (jrow < p.N) {
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                T* out = static_cast<T*>(which ? p.dv : p.dk) + ((size_t)bh * p.N) * D;
+                const float mul = which ? 1.f : p.scale;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
                     uint4* dst = reinterpret_cast<uint4*>(out + (size_t)jrow * D + half * (D / 2) + c * 32);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         uint4 w4;
-                        w4.x = Elem16<T>::pack2(__uint_as_float(ar[8 * v + 0]) * mul, __uint_as_float(ar[8 * v + 1]) * mul);
-                        w4.y = Elem16<T>::pack2(__uint_as_float(ar[8 * v + 2]) * mul, __uint_as_float(ar[8 * v + 3]) * mul);
-                        w4.z = Elem16<T>::pack2(__uint_as_float(ar[8 * v + 4]) * mul, __uint_as_float(ar[8 * v + 5]) * mul);
-                        w4.w = Elem16<T>::pack2(__uint_as_float(ar[8 * v + 6]) * mul, __uint_as_float(ar[8 * v + 7]) * mul);
+                        w4.x = Elem16<T>::pack2(__uint_as_float(ar[which][c][8 * v + 0]) * mul,
+                                                __uint_as_float(ar[which][c][8 * v + 1]) * mul);
+                        w4.y = Elem16<T>::pack2(__uint_as_float(ar[which][c][8 * v + 2]) * mul,
+                                                __uint_as_float(ar[which][c][8 * v + 3]) * mul);
+                        w4.z = Elem16<T>::pack2(__uint_as_float(ar[which][c][8 * v + 4]) * mul,
+                                                __uint_as_float(ar[which][c][8 * v + 5]) * mul);
+                        w4.w = Elem16<T>::pack2(__uint_as_float(ar[which][c][8 * v + 6]) * mul,
+                                                __uint_as_float(ar[which][c][8 * v + 7]) * mul);
                         dst[v] = w4;
                     }
                 }
             }
+        }
+        gs += n_active;
+        ++gi;
         }
     }
 
@@ -880,6 +986,8 @@ int launch_bwd_tc_d(const Problem& pr) {
     p.H = pr.H;
     p.N = pr.N;
     p.nb = pr.nb;
+    p.BH = BH;
+    p.nkt = (pr.N + kTile - 1) / kTile;
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * kLog2e;
     p.keep_scale = 1.0f / (1.0f - pr.dropout_p);
@@ -908,7 +1016,21 @@ int launch_bwd_tc_d(const Problem& pr) {
         }
         attr_set = true;
     }
-    cfg.gridDim = dim3(BH, (pr.N + kTile - 1) / kTile);
+    // at D = 128 without a block mask the grid is persistent: one CTA per SM
+    // walking the (bh, key tile) items (long_causal 1.330 -> 1.285 ms); at
+    // D = 64, where a step is short and the items many, one CTA per item
+    // with the hardware's dispatch measured faster; with a block mask a CTA
+    // per item (its tile list is built once)
+    if (pr.block_mask || D != 128) {
+        cfg.gridDim = dim3(BH, p.nkt);
+    } else {
+        int dev = 0, nsm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1)
+            return FA_ERR_CUDA;
+        const long long n_items = (long long)BH * p.nkt;
+        cfg.gridDim = dim3((unsigned)std::min<long long>(n_items, nsm), 1);
+    }
     cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr);
     record_main_start(pr.stream);
