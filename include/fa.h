@@ -173,10 +173,11 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
  *              scaling; the caller chooses them, e.g. max|x| / 448).
  *   o          bf16 [B, H, N, 128]; lse fp32 [B, H, N] (natural log).
  *   causal, block_mask, kv_len as in fa_fwd; no dropout.
- * P is quantised to E4M3 for the P V product, scaled by 2^8 before
- * rounding (the running maximum is raised whenever a row's maximum exceeds
- * it by 1/2 in log2 units, so the scaled values stay below 2^8.5 < 448);
- * the row sum uses the unquantised values. The error this adds to O is that
+ * P is quantised to E4M3 for the P V product, scaled by 2^5 before
+ * rounding (the running maximum is raised when a row's maximum exceeds it
+ * by 3.5 in log2 units, so the scaled values stay below 2^8.5 < 448;
+ * probabilities below 2^-11 of the running maximum round as E4M3
+ * subnormals); the row sum uses the unquantised values. The error this adds to O is that
  * of rounding each P_ij to E4M3 (relative 2^-4): |dO_ic| is within a few
  * (2^-4/sqrt 3) sqrt(sum_j P_ij^2 V_jc^2) for independent roundings.
  * Returns FA_ERR_UNSUPPORTED for d != 128, N not a multiple of 16 (the rows

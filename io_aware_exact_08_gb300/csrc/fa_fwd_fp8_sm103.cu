@@ -18,13 +18,17 @@
 //    fp32 [B*H]): the real input is code * factor. The factors of Q and K
 //    fold into the softmax scale, V's into the final division by l;
 //  - P~ is quantised to E4M3 for the P V product. It is computed as
-//    2^(s - m + 8) in log2 units, i.e. shifted up by 2^8 so that the
+//    2^(s - m + 5) in log2 units, i.e. shifted up by 2^5 so that the
 //    probabilities that matter sit in E4M3's normal range (the smallest
-//    normal, 2^-6, stands for 2^-14 of the row maximum), and the running max
-//    is raised whenever the row max exceeds it by more than 1/2, so
+//    normal, 2^-6, stands for 2^-11 of the running maximum; smaller ones
+//    round as subnormals, to within 2^-15 of it), and the running max is
+//    raised when the row max exceeds it by more than 3.5, so
 //    P~ <= 2^8.5 < 448, the largest finite E4M3 value. l sums the fp32
 //    values before quantisation; the shift cancels in O = sum P V / l and is
-//    taken off LSE.
+//    taken off LSE. A raise rescales O in TMEM for the whole warp, so the
+//    threshold is as large as the E4M3 range allows (a threshold of 1/2
+//    with a 2^8 shift measured 1305 against 1698 TFLOP/s on a causal
+//    N = 8K, d = 128 problem).
 // One CTA computes two 128-row query tiles (ping-pong between two softmax
 // warpgroups, as in the 16-bit kernel); head dimension 128 only.
 #include <cmath>
@@ -51,8 +55,8 @@ constexpr int kSoftmaxThreads = 128;
 constexpr int kThreads = 384;
 constexpr int kSoftmaxRegs = 208, kIssueRegs = 80;
 static_assert(256 * kSoftmaxRegs + 128 * kIssueRegs <= kThreads * 168, "register budgets above the launch");
-constexpr float kRaise = 0.5f;   // raise the running max when the row max exceeds it by this (log2 units)
-constexpr float kPShift = 8.0f;  // P~ = 2^(s - m + 8)
+constexpr float kRaise = 3.5f;   // raise the running max when the row max exceeds it by this (log2 units)
+constexpr float kPShift = 5.0f;  // P~ = 2^(s - m + 5)
 constexpr int kStages = 8;
 constexpr int kTileBytes = kBlockN * kD;  // one 128 x 128 E4M3 tile: Q_t, K_j or Vt_j
 constexpr int kSmem = 1024 + 2 * kTileBytes + kStages * kTileBytes + 256 + 2 * kMaskListCap * 2;
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (raise) l *= alpha;
             }
             if (raise) m = mt;
-            // P~ = 2^(s - m + 8): at most 2^8.5 < 448
+            // P~ = 2^(s - m + 5): at most 2^8.5 < 448
             const float nmref = (m == -INFINITY) ? 0.f : kPShift - m;
             float ps[8];
 #pragma unroll
