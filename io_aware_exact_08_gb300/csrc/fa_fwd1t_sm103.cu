@@ -5,13 +5,16 @@
 // and Memory-Efficient Exact Attention with IO-Awareness", section "Metode",
 // steps 1-4; the division by l deferred to the end as in the FlashAttention-2
 // section of the "Flash Attention" guide), laid out so that two CTAs fit on
-// one SM: TMEM holds one S (128 columns, P written over it) and O (64
-// columns) in a 256-column allocation, and shared memory holds Q and a
-// five-stage K/V ring (about 100 KB). Within a CTA the S, softmax and P V of
-// consecutive key tiles run one after the other; the tensor core alternates
-// between the two CTAs of the SM, and one CTA's start (barriers, TMEM, the Q
-// and first K/V loads) and end (the O and LSE stores) overlap the other's
-// main loop. At head dimension 64 the per-CTA fixed costs are as large as a
+// one SM: TMEM holds S (128 columns), O (64) and P (64 columns of packed
+// 16-bit pairs) in a 256-column allocation, and shared memory holds Q and a
+// five-stage K/V ring (about 100 KB). P has columns of its own so that
+// S(u+1) = Q K_{u+1}^T is issued as soon as the softmax has read S(u) into
+// registers: the tensor core computes the next scores and P(u-1) V while the
+// softmax of tile u runs. The MMA order is S(0), S(1), P(0)V, S(2), P(1)V, ...
+// and the loads follow it (K0, K1, V0, K2, V1, ...). The tensor core also
+// alternates between the two CTAs of the SM, and one CTA's start (barriers,
+// TMEM, the Q and first K/V loads) and end (the O and LSE stores) overlap the
+// other's main loop. At head dimension 64 the per-CTA fixed costs are as large as a
 // few key tiles' work, which is what this layout hides; with one tile per
 // CTA the grid also has twice as many, smaller work units.
 // Roles (256 threads): warps 0-3 softmax (thread = query row), warp 4 TMA
@@ -49,7 +52,7 @@ constexpr int kStages = 5;
 constexpr int kTileBytes = kBlockN * kD * 2;  // one 128 x 64 16-bit tile (one 128-byte-wide box)
 constexpr int kSmem = 1024 + kTileBytes + kStages * kTileBytes + 256 + kMaskListCap * 2;
 static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
-constexpr uint32_t kColS = 0, kColO = 128, kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColO = 128, kColP = 192, kTmemCols = 256;
 
 struct Fwd1tParams {
     float* lse;
@@ -61,7 +64,6 @@ struct Fwd1tParams {
     float scale_log2;
     float out_scale;  // 1/(1-p)
     uint32_t drop_thr;
-    int dropout;
     int causal;
     uint64_t seed;
 };
@@ -70,8 +72,10 @@ struct Shared1t {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t q_full;
-    uint64_t s_full;
-    uint64_t p_full;
+    uint64_t s_full;   // S(u) in TMEM
+    uint64_t s_free;   // the softmax has read S(u): S(u+1) may be written
+    uint64_t p_full;   // P(u) in TMEM
+    uint64_t pv_done;  // P(u) V has completed: O may be rescaled, P overwritten
     uint64_t o_final;
     uint64_t teardown;
     uint32_t tmem_base;
@@ -80,7 +84,7 @@ struct Shared1t {
 };
 static_assert(sizeof(Shared1t) <= 256, "barrier block");
 
-template <typename T, bool kSplit>
+template <typename T, bool kSplit, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_1t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Fwd1tParams p) {
@@ -113,7 +117,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mbar_init(&st->q_full, 1);
         mbar_init(&st->s_full, 1);
+        mbar_init(&st->s_free, 4);
         mbar_init(&st->p_full, 4);
+        mbar_init(&st->pv_done, 1);
         mbar_init(&st->o_final, 1);
         mbar_init(&st->teardown, 1);
         st->abort_flag = 0;
@@ -138,23 +144,23 @@ __global__ void __launch_bounds__(kThreads, 2)
             prefetch_tmap(&tm_v);
             mbar_arrive_expect_tx(&st->q_full, kTileBytes);
             tma_load_3d(sQ, &tm_q, &st->q_full, 0, qt * kBlockM, bh);
-            // load 2u = K of key tile u, 2u + 1 = V of it
+            // loads in the order the MMA warp uses them: K(0), then for each
+            // u, K(u+1) (if any) and V(u)
             int t = 0;
             bool okp = true;
-            for (int u = 0; okp && u < n; ++u) {
+            for (int x = 0; okp && x < 2 * n; ++x) {
+                const bool is_v = x > 0 && ((x & 1) == 0 || x == 2 * n - 1);
+                const int u = is_v ? (x == 2 * n - 1 ? n - 1 : x / 2 - 1) : (x + 1) / 2;
                 const int j = kSplit ? (int)sList[u] : u;
-#pragma unroll
-                for (int which = 0; which < 2; ++which) {
-                    const int s = t % kStages;
-                    const uint32_t ph = (t / kStages) & 1;
-                    if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 361)) {
-                        okp = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&st->kv_full[s], kTileBytes);
-                    tma_load_3d(sKV + s * kTileBytes, which ? &tm_v : &tm_k, &st->kv_full[s], 0, j * kBlockN, bh);
-                    ++t;
+                const int s = t % kStages;
+                const uint32_t ph = (t / kStages) & 1;
+                if (!mbar_wait(&st->kv_empty[s], ph ^ 1, wctx, 361)) {
+                    okp = false;
+                    break;
                 }
+                mbar_arrive_expect_tx(&st->kv_full[s], kTileBytes);
+                tma_load_3d(sKV + s * kTileBytes, is_v ? &tm_v : &tm_k, &st->kv_full[s], 0, j * kBlockN, bh);
+                ++t;
             }
             // drain: the last load issued into each stage has landed
             for (int l = max(0, t - kStages); l < t; ++l)
@@ -177,8 +183,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             bool ok = mbar_wait_warp(&st->q_full, 0, wctx, 370);
             tc_fence_after();
             int ld = 0;  // next load to use
-            // S(u) = Q K_u^T over the S columns (P(u-1) there has been read:
-            // MMAs run in issue order)
+            // S(u) = Q K_u^T over the S columns (S(u-1) has been read)
             auto issue_s = [&]() -> bool {
                 const int s = ld % kStages;
                 if (!mbar_wait_warp(&st->kv_full[s], (ld / kStages) & 1, wctx, 371)) return false;
@@ -194,6 +199,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             };
             if (ok) ok = issue_s();
             for (int u = 0; ok && u < n; ++u) {
+                if (u + 1 < n) {
+                    if (!mbar_wait_warp(&st->s_free, u & 1, wctx, 375)) break;
+                    tc_fence_after();
+                    if (!issue_s()) break;
+                }
                 // O += P(u) V_u, A = P(u) from TMEM
                 if (!mbar_wait_warp(&st->p_full, u & 1, wctx, 372)) break;
                 tc_fence_after();
@@ -203,12 +213,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint64_t vd = kvd_v + (uint64_t)(s * kStageUnits);
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ts_warp(tmem + kColO, tmem + kColS + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
+                    mma_ts_warp(tmem + kColO, tmem + kColP + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
                                 (u > 0 || kk > 0) ? 1u : 0u);
                 mma_commit_warp(&st->kv_empty[s]);
+                mma_commit_warp(&st->pv_done);
                 ++ld;
                 if (u + 1 == n) mma_commit_warp(&st->o_final);
-                else ok = issue_s();
             }
             mma_commit_warp(&st->teardown);
             mbar_wait_warp(&st->teardown, 0, wctx, 373);
@@ -221,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const uint32_t sbase = tmem + lane_base + kColS;
         const uint32_t obase = tmem + lane_base + kColO;
+        const uint32_t pbase = tmem + lane_base + kColP;
         float m = -INFINITY;
         float l = 0.f;
         bool ok = true;
@@ -229,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // dropout keep bits of this row's 128 keys (bit x of keep[c] is
             // key 32c + x), drawn before S arrives
             uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-            if (p.dropout) {
+            if constexpr (kDrop) {
 #pragma unroll 8
                 for (int g = 0; g < 32; ++g) {
                     const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, i, ktile * (kBlockN / 4) + g);
@@ -245,7 +256,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 ok = false;
                 break;
             }
-            // S(u) was issued after P(u-1) V: O is complete here
             tc_fence_after();
             const int k0 = ktile * kBlockN;
             int lim = min(kBlockN, L - k0);
@@ -257,6 +267,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+            // S(u) is in registers: the S columns may take S(u+1)
+            tc_fence_before();
+            mbar_arrive_warp(&st->s_free);
+            // P(u-1) V must have completed before O is rescaled or P(u)
+            // written over P(u-1)
+            bool pv_waited = (u == 0);
             if (!full) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -280,6 +296,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             const float mt = pm[0] * p.scale_log2;
             const bool raise = mt > m + kRescaleThreshold;
             if (__any_sync(0xffffffffu, raise) && u > 0) {
+                if (!mbar_wait_warp(&st->pv_done, (u - 1) & 1, wctx, 382)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                pv_waited = true;
                 const float alpha = raise ? ex2_approx(m - mt) : 1.f;
 #pragma unroll 1
                 for (int c = 0; c < kD / 8; ++c) {
@@ -299,10 +321,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             float ps[8];
 #pragma unroll
             for (int x = 0; x < 8; ++x) ps[x] = 0.f;
-            // exponentials packed in place (P chunk c in columns 16c..16c+15,
-            // already read); the sum takes every exponential, the dropout
-            // mask only what goes to P
-            if (!p.dropout) {
+            // exponentials packed in place (P chunk c in sr[c][0..15], stored
+            // to P columns 16c..16c+15 once P(u-1) V is done); the sum takes
+            // every exponential, the dropout mask only what goes to P. Without
+            // dropout all four chunks are stored after the last exponential,
+            // so the wait for P(u-1) V comes as late as possible; with dropout
+            // (whose keep bits take longer than the products) the wait comes
+            // first and each chunk is stored as soon as it is packed, which
+            // keeps fewer registers live.
+            if constexpr (!kDrop) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -314,9 +341,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                         fadd2(ps[2 * k], ps[2 * k + 1], ps[2 * k], ps[2 * k + 1], e0, e1);
                         sr[c][x >> 1] = Elem16<T>::pack2(e0, e1);
                     }
-                    tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
                 }
             } else {
+                if (!pv_waited) {
+                    if (!mbar_wait_warp(&st->pv_done, (u - 1) & 1, wctx, 383)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    pv_waited = true;
+                }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -329,13 +363,25 @@ __global__ void __launch_bounds__(kThreads, 2)
                         sr[c][x >> 1] =
                             Elem16<T>::pack2(((keep[c] >> x) & 1u) ? e0 : 0.f, ((keep[c] >> (x + 1)) & 1u) ? e1 : 0.f);
                     }
-                    tmem_st16(sbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
+                    tmem_st16(pbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
                 }
             }
             fadd2(ps[0], ps[1], ps[0], ps[1], ps[4], ps[5]);
             fadd2(ps[2], ps[3], ps[2], ps[3], ps[6], ps[7]);
             fadd2(ps[0], ps[1], ps[0], ps[1], ps[2], ps[3]);
             l += ps[0] + ps[1];
+            if constexpr (!kDrop) {
+                if (!pv_waited) {
+                    if (!mbar_wait_warp(&st->pv_done, (u - 1) & 1, wctx, 383)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_st16(pbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
+            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive_warp(&st->p_full);
@@ -381,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, bool kSplit>
+template <typename T, bool kSplit, bool kDrop>
 int launch_1t(const Problem& pr) {
     constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
     CUtensorMap tq, tk, tv;
@@ -402,10 +448,9 @@ int launch_1t(const Problem& pr) {
     p.scale_log2 = pr.scale * kLog2e;
     p.out_scale = 1.0f / (1.0f - pr.dropout_p);
     p.drop_thr = pr.drop_threshold;
-    p.dropout = pr.dropout_p > 0.f;
     p.causal = pr.causal;
     p.seed = pr.seed;
-    auto kernel = fwd_1t_kernel<T, kSplit>;
+    auto kernel = fwd_1t_kernel<T, kSplit, kDrop>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
@@ -443,11 +488,18 @@ int launch_1t(const Problem& pr) {
     return FA_OK;
 }
 
+template <typename T>
+int launch_1t_for(const Problem& p) {
+    const bool drop = p.dropout_p > 0.f;
+    if (p.block_mask) return drop ? launch_1t<T, true, true>(p) : launch_1t<T, true, false>(p);
+    return drop ? launch_1t<T, false, true>(p) : launch_1t<T, false, false>(p);
+}
+
 }  // namespace
 
 int launch_fwd_1t(const Problem& p) {
-    if (p.dtype == FA_FP16) return p.block_mask ? launch_1t<__half, true>(p) : launch_1t<__half, false>(p);
-    if (p.dtype == FA_BF16) return p.block_mask ? launch_1t<__nv_bfloat16, true>(p) : launch_1t<__nv_bfloat16, false>(p);
+    if (p.dtype == FA_FP16) return launch_1t_for<__half>(p);
+    if (p.dtype == FA_BF16) return launch_1t_for<__nv_bfloat16>(p);
     return FA_ERR_UNSUPPORTED;
 }
 
