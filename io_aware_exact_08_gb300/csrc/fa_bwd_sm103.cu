@@ -45,6 +45,7 @@
 namespace fa {
 
 bool make_tmap16(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows, CUtensorMapDataType type);
+bool make_tmap_f32_acc(CUtensorMap* map, float* base, int BH, int N, int d);
 
 namespace {
 
@@ -76,13 +77,21 @@ struct BwdCfg {
     // dQ product still reads dS^T, so the tile is double-buffered by step
     // parity there
     static constexpr int kDsBuffers = (D == 64) ? 2 : 1;
+    // D = 64: dQ leaves through the TMA engine (bulk reduce-add of 32 x 32
+    // fp32 boxes staged in shared memory, 4 KB per reduction warp). Row-
+    // per-thread reductions there sent 32 scattered L2 requests per
+    // instruction through the load/store path, and the compute warps' shared
+    // memory accesses queued behind them.
+    static constexpr bool kDqBulk = (D == 64);
+    static constexpr int kDqStageBytes = kDqBulk ? 4 * 32 * 128 : 0;
     // (no alignment slack: the dynamic shared memory window starts 1024-byte
     // aligned, which the kernel checks)
     // block masks: this key tile's list of visible query tiles
     static constexpr int kListCap = (D == 128) ? kMaskListCapBwd128 : kMaskListCap;
     static constexpr int kSmemBase =
-        2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBuffers * kDsBytes + 2 * 2 * kTile * 4 /*lse, delta x2*/ +
-        256;
+        2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBuffers * kDsBytes + kDqStageBytes +
+        2 * 2 * kTile * 4 /*lse, delta x2*/ + 256;
+    static_assert(kSmemBase + kListCap * 2 <= 232448, "shared memory");
     static constexpr int smem(bool mask) { return kSmemBase + (mask ? kListCap * 2 : 0); }
     static constexpr uint32_t kColS = 0, kColDP = 128;
     // dQ accumulator. D = 128: dQ^T (lanes = head-dim rows, 128 query
@@ -169,12 +178,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// dst[0..3] += (a, b, c, d) (fp32, no return value, relaxed, L2).
-__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
 // *dst += a (fp32, no return value, relaxed, L2).
 __device__ __forceinline__ void red_add_f32(float* dst, float a) {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(a) : "memory");
@@ -185,7 +188,7 @@ template <typename T, int D, bool kMask>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using Cfg = BwdCfg<D>;
     // the persistent grid (several items per CTA) is used at D = 128 without a
     // block mask; otherwise every CTA runs exactly one item
@@ -201,7 +204,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     uint8_t* sDS = sStages + Cfg::kStages * Cfg::kStageBytes;
     // -LSE (log2 units) and -delta of the step's 128 queries, double-buffered
     // by step parity: a warp may stage step it+1 while others still read it
-    float* sNegLse = reinterpret_cast<float*>(sDS + Cfg::kDsBuffers * Cfg::kDsBytes);
+    uint8_t* sDQ = sDS + Cfg::kDsBuffers * Cfg::kDsBytes;  // D = 64: dQ staging, 4 KB per reduction warp
+    float* sNegLse = reinterpret_cast<float*>(sDQ + Cfg::kDqStageBytes);
     float* sNegDelta = sNegLse + 2 * kTile;
     BwdShared* st = reinterpret_cast<BwdShared*>(sNegDelta + 2 * kTile);
     uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);
@@ -381,17 +385,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             if (!mbar_wait_warp(&st->kv_full, gi & 1, wctx, 110)) break;
             tc_fence_after();
             if constexpr (D == 64) {
-            // Software-pipelined order: the next step's S^T_0/dP^T_0 go right
-            // after this step's half-0 gradient products and its S^T_1/dP^T_1
-            // after the dQ product, so the compute warps of one half work on
-            // the next step while the tensor core finishes this one:
-            //   [dV_0 dK_0](t) [S_0 dP_0](t+1) [dV_1 dK_1 dQ](t) [S_1 dP_1](t+1)
+            // Software-pipelined order: the next step's S^T_h/dP^T_h go right
+            // after this step's half-h gradient products, and the dQ product
+            // last, so the compute warps of one half work on the next step
+            // while the tensor core finishes this one, and neither half's
+            // chain (compute, gradient products, next scores) includes dQ:
+            //   [dV_0 dK_0](t) [S_0 dP_0](t+1) [dV_1 dK_1](t) [S_1 dP_1](t+1) [dQ](t)
             // Each product that overwrites TMEM (S^T_h, dP^T_h) comes after
             // the MMAs that read the old contents (in issue order) and after
-            // the compute warps released them (p_ready); dS^T alternates
-            // between two shared-memory tiles by step parity, because the dQ
-            // product of step t reads it after half 0 of step t + 1 may have
-            // started writing.
+            // the compute warps released them (p_ready). dS^T alternates
+            // between two shared-memory tiles by step parity: dQ of step t
+            // reads its tile while step t + 1 writes the other, and step t + 2
+            // writes it again only after S^T(t + 2), issued after dQ(t), is
+            // complete.
             auto issue_sdp = [&](int g2, int h) {  // g2: global step
                 const uint32_t qb = smem_u32(sStages + (g2 % Cfg::kStages) * Cfg::kStageBytes);
                 const uint64_t qk = smem_desc_sw128(qb, 16, 1024);
@@ -458,6 +464,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         }
                     } else {
                         mma_commit_warp(&st->st_empty[s]);  // Q_i, dO_i read
+                        if (it + 1 < n_active) issue_sdp(g + 1, 1);
                         // dQ = dS K_j over the whole tile, over the previous
                         // step's dQ once it has been read out
                         if (g > 0) {
@@ -472,7 +479,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                             mma_ss_warp(tmem + Cfg::kColDQ, desc_add(dsd_mn, dsb + kk * 2048), desc_add(kd_mn, kk * 2048),
                                         id_dq, kk > 0);
                         mma_commit_warp(&st->dq_full[0]);
-                        if (it + 1 < n_active) issue_sdp(g + 1, 1);
                     }
                 }
             }
@@ -580,12 +586,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         regs_dec<Cfg::kReduceRegs>();
         // D = 128: dQ^T, lane = head-dim index, so one reduction instruction
         // covers 32 consecutive floats of one query row. D = 64: dQ, lane =
-        // query row, 64 consecutive floats in 16-byte reductions.
+        // query row, added by bulk tensor reductions (below).
         const int quarter = warp & 3;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const int r = quarter * 32 + lane;
         bool ok = true;
         int gs = 0;  // steps with work, so far
+        uint8_t* dq_buf = sDQ + quarter * 4096;  // D = 64: this warp's 32 x 32 fp32 box
+        if (Cfg::kDqBulk && lane == 0) prefetch_tmap(&tm_dq);
         pdl_wait();
         for (int rr = 0, item = item0; ok && item < n_items && (kPersist || rr == 0); item = item_of(++rr)) {
         int n_active;
@@ -622,21 +630,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
                     for (int x = 0; x < 32; ++x)
                         if (h * 64 + 32 + x < nvalid) red_add_f32(dst + (size_t)(32 + x) * D, __uint_as_float(qb[x]));
-                } else if (r < nvalid) {
-                    float* dst = p.dq_acc + ((size_t)bh * p.N + i0 + r) * D;
+                } else if (Cfg::kDqBulk) {
+                    // this warp's 32 query rows in two boxes of 32 columns,
+                    // each staged with the 128-byte swizzle (16-byte chunk c
+                    // of row x at chunk position c ^ (x & 7)) and added into
+                    // the accumulator by the TMA engine; rows past N are
+                    // outside the tensor map and skipped
+                    if (quarter * 32 < nvalid) {
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        red_add_v4(dst + 4 * v, __uint_as_float(qa[4 * v]), __uint_as_float(qa[4 * v + 1]),
-                                   __uint_as_float(qa[4 * v + 2]), __uint_as_float(qa[4 * v + 3]));
+                        for (int c = 0; c < 2; ++c) {
+                            const uint32_t* q = c ? qb : qa;
+                            if (lane == 0) bulk_wait_read();  // the previous box has been read
+                            __syncwarp();
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        red_add_v4(dst + 32 + 4 * v, __uint_as_float(qb[4 * v]), __uint_as_float(qb[4 * v + 1]),
-                                   __uint_as_float(qb[4 * v + 2]), __uint_as_float(qb[4 * v + 3]));
+                            for (int v = 0; v < 8; ++v)
+                                *reinterpret_cast<uint4*>(dq_buf + lane * 128 + ((v ^ (lane & 7)) << 4)) =
+                                    make_uint4(q[4 * v], q[4 * v + 1], q[4 * v + 2], q[4 * v + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_reduce_add_3d(&tm_dq, dq_buf, 32 * c, i0 + quarter * 32, bh);
+                                bulk_commit_group();
+                            }
+                        }
+                    }
                 }
             }
         }
         gs += n_active;
         }
+        // the accumulator writes are complete before the CTA ends
+        if (Cfg::kDqBulk && lane == 0) bulk_wait_all();
     } else {
         // ------------------------------------------------------------ compute
         regs_inc<Cfg::kComputeRegs>();
@@ -740,6 +764,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             // time
             constexpr bool kLoadBoth = (D == 64);
             uint32_t sr2[2][32], dr2[2][32];
+            // D = 64: both chunks' P^T (TMEM) and dS^T (shared memory) are
+            // stored after the second chunk is computed, so that the second
+            // chunk's shared-memory reads of LSE and delta do not queue
+            // behind the first chunk's stores
+            uint32_t pk2[kLoadBoth ? 2 : 1][16];
+            uint32_t dsk2[kLoadBoth ? 2 : 1][16];
             if constexpr (kLoadBoth) {
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
@@ -767,8 +797,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 }
                 const uint32_t keep = keep_w[ch];
                 const bool edge = (cmin > cb) || (cmax < cb + 32);
-                uint32_t pk[16];
-                uint32_t dsk[16];
+                uint32_t(&pk)[16] = pk2[kLoadBoth ? ch : 0];
+                uint32_t(&dsk)[16] = dsk2[kLoadBoth ? ch : 0];
                 // columns outside [cmin, cmax) (causal diagonal, key padding,
                 // sequence end) are zeroed in S first, so the element loop
                 // below carries no per-element mask test
@@ -825,14 +855,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     }
                 }
                 // P^T into TMEM columns this warp has already read
-                tmem_st16(tmem + lane_base + Cfg::kColS + half * 64 + ch * 16, pk);
+                if constexpr (!kLoadBoth) tmem_st16(tmem + lane_base + Cfg::kColS + half * 64 + ch * 16, pk);
                 // dS^T row r, queries cb..cb+31: 4 swizzled 16-byte chunks
                 uint8_t* row = sDS + (g & (Cfg::kDsBuffers - 1)) * Cfg::kDsBytes + half * (kTile * 128) + r * 128;
+                if constexpr (!kLoadBoth) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const int chunk = ch * 4 + v;
-                    uint4 w4 = make_uint4(dsk[4 * v], dsk[4 * v + 1], dsk[4 * v + 2], dsk[4 * v + 3]);
-                    *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = w4;
+                    for (int v = 0; v < 4; ++v) {
+                        const int chunk = ch * 4 + v;
+                        uint4 w4 = make_uint4(dsk[4 * v], dsk[4 * v + 1], dsk[4 * v + 2], dsk[4 * v + 3]);
+                        *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = w4;
+                    }
+                }
+            }
+            if constexpr (kLoadBoth) {
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) tmem_st16(tmem + lane_base + Cfg::kColS + half * 64 + ch * 16, pk2[ch]);
+                uint8_t* row = sDS + (g & (Cfg::kDsBuffers - 1)) * Cfg::kDsBytes + half * (kTile * 128) + r * 128;
+#pragma unroll
+                for (int chunk = 0; chunk < 8; ++chunk) {
+                    const uint32_t* d4 = &dsk2[chunk >> 2][4 * (chunk & 3)];
+                    *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = make_uint4(d4[0], d4[1], d4[2], d4[3]);
                 }
             }
             tmem_st_wait();
@@ -952,9 +994,10 @@ int launch_bwd_tc_d(const Problem& pr) {
     using Cfg = BwdCfg<D>;
     constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
     const int BH = pr.B * pr.H;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_tmap16(&tq, pr.q, BH, pr.N, D, kTile, tt) || !make_tmap16(&tk, pr.k, BH, pr.N, D, kTile, tt) ||
-        !make_tmap16(&tv, pr.v, BH, pr.N, D, kTile, tt) || !make_tmap16(&tdo, pr.dO, BH, pr.N, D, kTile, tt))
+        !make_tmap16(&tv, pr.v, BH, pr.N, D, kTile, tt) || !make_tmap16(&tdo, pr.dO, BH, pr.N, D, kTile, tt) ||
+        !make_tmap_f32_acc(&tdq, pr.dq_acc, BH, pr.N, D))
         return FA_ERR_CUDA;
     const size_t rows = (size_t)BH * pr.N;
     // The three kernels are launched with programmatic stream serialization:
@@ -1034,8 +1077,8 @@ int launch_bwd_tc_d(const Problem& pr) {
     cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr);
     record_main_start(pr.stream);
-    cudaError_t e = pr.block_mask ? cudaLaunchKernelEx(&cfg, bwd_tc_kernel<T, D, true>, tq, tk, tv, tdo, p)
-                                  : cudaLaunchKernelEx(&cfg, bwd_tc_kernel<T, D, false>, tq, tk, tv, tdo, p);
+    cudaError_t e = pr.block_mask ? cudaLaunchKernelEx(&cfg, bwd_tc_kernel<T, D, true>, tq, tk, tv, tdo, tdq, p)
+                                  : cudaLaunchKernelEx(&cfg, bwd_tc_kernel<T, D, false>, tq, tk, tv, tdo, tdq, p);
     record_main_stop(pr.stream);
     note_launches(1);
     if (e != cudaSuccess) {

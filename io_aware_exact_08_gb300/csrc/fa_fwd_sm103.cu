@@ -1054,6 +1054,21 @@ bool make_tmap16(CUtensorMap* map, const void* base, int BH, int N, int d, int b
     return r == CUDA_SUCCESS;
 }
 
+// [B*H, N, d] fp32 (the backward's dQ accumulator) viewed as a 3-D tensor (d
+// fastest); boxes of 32 columns (128 bytes, 128-byte swizzle) x 32 rows.
+bool make_tmap_f32_acc(CUtensorMap* map, float* base, int BH, int N, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Merges the n_splits partial results of split-KV: with w_s = e^{LSE_s - M},
 // O = sum_s w_s O_s / sum_s w_s and LSE = M + log sum_s w_s (M = max_s LSE_s),
 // the combination of softmax partials over disjoint key blocks of the
