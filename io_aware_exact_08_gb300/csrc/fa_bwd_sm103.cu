@@ -184,15 +184,15 @@ __device__ __forceinline__ void red_add_f32(float* dst, float a) {
 }
 
 
-template <typename T, int D, bool kMask>
+template <typename T, int D, bool kMask, bool kPersist>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using Cfg = BwdCfg<D>;
-    // the persistent grid (several items per CTA) is used at D = 128 without a
-    // block mask; otherwise every CTA runs exactly one item
-    constexpr bool kPersist = (D == 128) && !kMask;
+    // kPersist: a CTA walks several items (persistent grid, never with a
+    // block mask); otherwise every CTA runs exactly one item
+    static_assert(!(kPersist && kMask), "a block mask's tile list is built for one item");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0 && atomicCAS(p.status, 0, (int)FA_ERR_CUDA) == 0) atomicExch(p.status + 1, 130);
@@ -1038,33 +1038,38 @@ int launch_bwd_tc_d(const Problem& pr) {
     p.dropout = pr.dropout_p > 0.f;
     p.causal = pr.causal;
     p.seed = pr.seed;
+    // without a block mask or per-sequence lengths the grid is persistent: one
+    // CTA per SM walking the (bh, key tile) items in a fixed order, so that
+    // one item's last products and dK/dV stores overlap the next one's loads
+    // and first products (gpt2_causal backward 377 -> 394 TFLOP/s). Key
+    // padding leaves items of very different length, which the hardware's
+    // dispatch of one CTA per item balances better (bert_pad_dropout 315
+    // against 298 persistent); with a block mask a CTA per item (its tile
+    // list is built once)
+    const bool persist = !pr.block_mask && !pr.kv_len;
+    auto kernel = pr.block_mask ? bwd_tc_kernel<T, D, true, false>
+                                : (persist ? bwd_tc_kernel<T, D, false, true> : bwd_tc_kernel<T, D, false, false>);
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(bwd_tc_kernel<T, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::smem(false)) != cudaSuccess ||
-            cudaFuncSetAttribute(bwd_tc_kernel<T, D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::smem(true)) != cudaSuccess)
-            return FA_ERR_CUDA;
         // setmaxnreg.inc takes registers from what the CTA was launched with
         // and waits (without bound) until they are free: refuse to launch
         // unless the budgets fit in that allocation
-        cudaFuncAttributes a0{}, a1{};
-        if (cudaFuncGetAttributes(&a0, bwd_tc_kernel<T, D, false>) != cudaSuccess ||
-            cudaFuncGetAttributes(&a1, bwd_tc_kernel<T, D, true>) != cudaSuccess ||
-            a0.numRegs * Cfg::kThreads < Cfg::kRegBudget || a1.numRegs * Cfg::kThreads < Cfg::kRegBudget) {
-            if (std::getenv("FA_DEBUG"))
-                std::fprintf(stderr, "fa: bwd register budget %d exceeds the launch allocation (%d, %d regs)\n",
-                             Cfg::kRegBudget, a0.numRegs, a1.numRegs);
-            return FA_ERR_CUDA;
+        decltype(kernel) all[3] = {bwd_tc_kernel<T, D, true, false>, bwd_tc_kernel<T, D, false, true>,
+                                   bwd_tc_kernel<T, D, false, false>};
+        for (int x = 0; x < 3; ++x) {
+            cudaFuncAttributes a{};
+            if (cudaFuncSetAttribute(all[x], cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::smem(x == 0)) !=
+                    cudaSuccess ||
+                cudaFuncGetAttributes(&a, all[x]) != cudaSuccess || a.numRegs * Cfg::kThreads < Cfg::kRegBudget) {
+                if (std::getenv("FA_DEBUG"))
+                    std::fprintf(stderr, "fa: bwd register budget %d exceeds the launch allocation (%d regs)\n",
+                                 Cfg::kRegBudget, a.numRegs);
+                return FA_ERR_CUDA;
+            }
         }
         attr_set = true;
     }
-    // at D = 128 without a block mask the grid is persistent: one CTA per SM
-    // walking the (bh, key tile) items (long_causal 1.330 -> 1.285 ms); at
-    // D = 64, where a step is short and the items many, one CTA per item
-    // with the hardware's dispatch measured faster; with a block mask a CTA
-    // per item (its tile list is built once)
-    if (pr.block_mask || D != 128) {
+    if (!persist) {
         cfg.gridDim = dim3(BH, p.nkt);
     } else {
         int dev = 0, nsm = 0;
@@ -1077,8 +1082,7 @@ int launch_bwd_tc_d(const Problem& pr) {
     cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr);
     record_main_start(pr.stream);
-    cudaError_t e = pr.block_mask ? cudaLaunchKernelEx(&cfg, bwd_tc_kernel<T, D, true>, tq, tk, tv, tdo, tdq, p)
-                                  : cudaLaunchKernelEx(&cfg, bwd_tc_kernel<T, D, false>, tq, tk, tv, tdo, tdq, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, tdq, p);
     record_main_stop(pr.stream);
     note_launches(1);
     if (e != cudaSuccess) {
