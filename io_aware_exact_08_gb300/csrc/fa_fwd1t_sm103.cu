@@ -1,8 +1,8 @@
 // Forward attention at head dimension 64, one 128-row query tile per CTA,
 // two CTAs per SM.
 //
-// The same per-block update as the two-tile kernel ("FlashAttention: Fast
-// and Memory-Efficient Exact Attention with IO-Awareness", section "Metode",
+// The same per-block update as the two-tile kernel ("FlashAttention: Fast and
+// Memory-Efficient Exact Attention with IO-Awareness", section "Metode",
 // steps 1-4; the division by l deferred to the end as in the FlashAttention-2
 // section of the "Flash Attention" guide), laid out so that two CTAs fit on
 // one SM: TMEM holds S (128 columns), O (64) and P (64 columns of packed
@@ -11,16 +11,17 @@
 // S(u+1) = Q K_{u+1}^T is issued as soon as the softmax has read S(u) into
 // registers: the tensor core computes the next scores and P(u-1) V while the
 // softmax of tile u runs. The MMA order is S(0), S(1), P(0)V, S(2), P(1)V, ...
-// and the loads follow it (K0, K1, V0, K2, V1, ...). The tensor core also
+// and the loads follow it (K0, K1, V0, K2, V1, ...). Each query row is shared
+// by two softmax threads, one per 64-key half of the tile, which halves the
+// per-thread chain (TMEM load, exponentials, P store) that bounds a CTA's
+// pace; the halves exchange their maxima once per tile. The tensor core
 // alternates between the two CTAs of the SM, and one CTA's start (barriers,
 // TMEM, the Q and first K/V loads) and end (the O and LSE stores) overlap the
-// other's main loop. At head dimension 64 the per-CTA fixed costs are as large as a
-// few key tiles' work, which is what this layout hides; with one tile per
-// CTA the grid also has twice as many, smaller work units.
-// Roles (256 threads): warps 0-3 softmax (thread = query row), warp 4 TMA
-// producer, warp 5 MMA issuer (all 32 lanes run its loop, one elected lane
-// issues), warps 6-7 idle. setmaxnreg gives the softmax warpgroup 208
-// registers a thread and the other 48 (launched at 128).
+// other's main loop.
+// Roles (384 threads): warps 0-7 softmax (thread = query row, column half),
+// warp 8 TMA producer, warp 9 MMA issuer (all 32 lanes run its loop, one
+// elected lane issues), warps 10-11 idle. setmaxnreg gives the softmax
+// warpgroups 96 registers a thread and the other 48 (launched at 80).
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -44,13 +45,32 @@ using namespace sm103;
 constexpr int kD = 64;
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-constexpr int kThreads = 256;
-constexpr int kSoftRegs = 208, kIssueRegs = 48;
-static_assert(128 * kSoftRegs + 128 * kIssueRegs <= kThreads * 128, "register budgets above the launch");
+// Thread layout, chosen by whether dropout applies. With dropout the keep
+// bits (one Philox4x32-10 call per four keys) dominate a tile, and two
+// threads per query row (one per 64-key half) halve them per thread
+// (bert_pad_dropout forward 192 -> 239 TFLOP/s). Without dropout the
+// exchange of the halves' maxima costs more than the shorter chain saves
+// (block_sparse forward 650 against 563 TFLOP/s), so one thread takes a row.
+template <bool kDrop>
+struct Layout1t {
+    static constexpr int kHalves = kDrop ? 2 : 1;           // softmax threads per query row
+    static constexpr int kSoftWarps = 4 * kHalves;
+    static constexpr int kThreads = 32 * kSoftWarps + 128;  // + producer, MMA issuer, two idle warps
+    // two CTAs per SM; setmaxnreg moves registers to the softmax warps
+    static constexpr int kLaunchRegs = 65536 / (2 * kThreads) / 8 * 8;
+    static constexpr int kSoftRegs = kDrop ? 96 : 208, kIssueRegs = 48;
+    static constexpr int kBudget = 32 * kSoftWarps * kSoftRegs + 128 * kIssueRegs;
+    static_assert(kBudget <= kThreads * kLaunchRegs, "register budgets above the launch");
+    static constexpr int kCols = kBlockN / kHalves;  // keys of a tile per thread
+    static constexpr int kChunks = kCols / 32;
+    static constexpr int kOCols = kD / kHalves;      // columns of O per thread
+};
 constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in the two-tile kernel
 constexpr int kStages = 5;
 constexpr int kTileBytes = kBlockN * kD * 2;  // one 128 x 64 16-bit tile (one 128-byte-wide box)
-constexpr int kSmem = 1024 + kTileBytes + kStages * kTileBytes + 256 + kMaskListCap * 2;
+// barrier block, the two column halves' row maxima (double-buffered by tile
+// parity) and row-sum shares, the block-mask tile list
+constexpr int kSmem = 1024 + kTileBytes + kStages * kTileBytes + 256 + (2 * 2 * 128 + 2 * 128) * 4 + kMaskListCap * 2;
 static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t kColS = 0, kColO = 128, kColP = 192, kTmemCols = 256;
 
@@ -76,6 +96,8 @@ struct Shared1t {
     uint64_t s_free;   // the softmax has read S(u): S(u+1) may be written
     uint64_t p_full;   // P(u) in TMEM
     uint64_t pv_done;  // P(u) V has completed: O may be rescaled, P overwritten
+    uint64_t mx_ready[2];  // both column halves' maxima of tile u (buffer u & 1) written
+    uint64_t l_ready;      // both halves' row-sum shares written
     uint64_t o_final;
     uint64_t teardown;
     uint32_t tmem_base;
@@ -85,7 +107,7 @@ struct Shared1t {
 static_assert(sizeof(Shared1t) <= 256, "barrier block");
 
 template <typename T, bool kSplit, bool kDrop>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(Layout1t<kDrop>::kThreads, 2)
     fwd_1t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Fwd1tParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -93,8 +115,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t* sQ = smem;
     uint8_t* sKV = smem + kTileBytes;
     Shared1t* st = reinterpret_cast<Shared1t*>(sKV + kStages * kTileBytes);
-    uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);  // [kMaskListCap]
+    float* sMax = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(st) + 256);  // [2 parities][2 halves][128 rows]
+    float* sL = sMax + 2 * 2 * 128;                                                // [2 halves][128 rows]
+    uint16_t* sList = reinterpret_cast<uint16_t*>(sL + 2 * 128);                   // [kMaskListCap]
 
+    using Lay = Layout1t<kDrop>;
+    constexpr int kProdWarp = Lay::kSoftWarps, kMmaWarp = Lay::kSoftWarps + 1;
     pdl_wait();
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -110,22 +136,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int cnt = warp_list_visible(p.block_mask + (size_t)qt * p.nb, 1, 0, n, sList, lane);
         if (lane == 0) st->n_list = cnt;
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kProdWarp && lane == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&st->kv_full[s], 1);
             mbar_init(&st->kv_empty[s], 1);
         }
         mbar_init(&st->q_full, 1);
         mbar_init(&st->s_full, 1);
-        mbar_init(&st->s_free, 4);
-        mbar_init(&st->p_full, 4);
+        mbar_init(&st->s_free, Lay::kSoftWarps);
+        mbar_init(&st->p_full, Lay::kSoftWarps);
         mbar_init(&st->pv_done, 1);
+        mbar_init(&st->mx_ready[0], Lay::kSoftWarps);
+        mbar_init(&st->mx_ready[1], Lay::kSoftWarps);
+        mbar_init(&st->l_ready, Lay::kSoftWarps);
         mbar_init(&st->o_final, 1);
         mbar_init(&st->teardown, 1);
         st->abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&st->tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -135,9 +164,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t tmem = st->tmem_base;
     if constexpr (kSplit) n = st->n_list;
 
-    if (warp == 4) {
+    if (warp == kProdWarp) {
         // ------------------------------------------------------------ producer
-        regs_dec<kIssueRegs>();
+        regs_dec<Lay::kIssueRegs>();
         if (lane == 0 && n > 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
@@ -167,11 +196,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 mbar_wait(&st->kv_full[l % kStages], (l / kStages) & 1, wctx, 362);
             mbar_wait(&st->q_full, 0, wctx, 363);
         }
-    } else if (warp == 6 || warp == 7) {
-        regs_dec<kIssueRegs>();  // idle: the rest of the producer / MMA warpgroup
-    } else if (warp == 5) {
+    } else if (warp > kMmaWarp) {
+        regs_dec<Lay::kIssueRegs>();  // idle: the rest of the producer / MMA warpgroup
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        regs_dec<kIssueRegs>();
+        regs_dec<Lay::kIssueRegs>();
         if (n > 0) {
             constexpr uint32_t idesc_s = idesc_f32acc(Elem16<T>::kFmt, kBlockM, kBlockN, 0, 0);
             constexpr uint32_t idesc_o = idesc_f32acc(Elem16<T>::kFmt, kBlockM, kD, 0, 1);
@@ -225,31 +254,42 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // ------------------------------------------------------------ softmax
-        regs_inc<kSoftRegs>();
-        const int r = tid;  // 0..127
+        // warp w reads TMEM lane quarter w & 3 (query rows 32 (w & 3) .. + 31)
+        // and column part w >> 2 of every score tile. With two parts (the
+        // dropout layout) a row is shared by two threads, one per 64-key half:
+        // both take the tile's row maximum from the two halves' maxima
+        // (exchanged through shared memory), so they keep the same running
+        // maximum m and make the same rescaling decisions; each rescales and
+        // stores its columns of O and keeps its share of the row sum l, and
+        // the shares are added at the end.
+        regs_inc<Lay::kSoftRegs>();
+        constexpr int kCols = Lay::kCols, kChunks = Lay::kChunks, kOCols = Lay::kOCols;
+        const int quarter = warp & 3;
+        const int half = warp >> 2;  // column part (0 in the one-part layout)
+        const int r = quarter * 32 + lane;  // query row within the tile
         const int i = qt * kBlockM + r;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const uint32_t sbase = tmem + lane_base + kColS;
-        const uint32_t obase = tmem + lane_base + kColO;
-        const uint32_t pbase = tmem + lane_base + kColP;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t sbase = tmem + lane_base + kColS + kCols * half;
+        const uint32_t obase = tmem + lane_base + kColO + kOCols * half;
+        const uint32_t pbase = tmem + lane_base + kColP + (kCols / 2) * half;
         float m = -INFINITY;
         float l = 0.f;
         bool ok = true;
         for (int u = 0; u < n; ++u) {
             const int ktile = kSplit ? (int)sList[u] : u;
-            // dropout keep bits of this row's 128 keys (bit x of keep[c] is
-            // key 32c + x), drawn before S arrives
-            uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+            // dropout keep bits of this thread's keys (bit x of keep[c] is
+            // key kCols half + 32 c + x of the tile), drawn before S arrives
+            uint32_t keep[kChunks];
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) keep[c] = 0xffffffffu;
             if constexpr (kDrop) {
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) keep[c] = 0;
 #pragma unroll 8
-                for (int g = 0; g < 32; ++g) {
-                    const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, i, ktile * (kBlockN / 4) + g);
-                    if (g == 0) keep[0] = keep[1] = keep[2] = keep[3] = 0;
-                    const uint32_t sh = bits << (4 * (g & 7));
-                    if ((g >> 3) == 0) keep[0] |= sh;
-                    else if ((g >> 3) == 1) keep[1] |= sh;
-                    else if ((g >> 3) == 2) keep[2] |= sh;
-                    else keep[3] |= sh;
+                for (int g = 0; g < kCols / 4; ++g) {
+                    const uint32_t bits =
+                        keep_bits4(p.seed, p.drop_thr, b, h, i, ktile * (kBlockN / 4) + (kCols / 4) * half + g);
+                    keep[g >> 3] |= bits << (4 * (g & 7));
                 }
             }
             if (!mbar_wait_warp(&st->s_full, u & 1, wctx, 380)) {
@@ -257,25 +297,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             }
             tc_fence_after();
-            const int k0 = ktile * kBlockN;
-            int lim = min(kBlockN, L - k0);
+            const int k0 = ktile * kBlockN + kCols * half;  // first key of this thread's part
+            int lim = min(kCols, L - k0);
             if (p.causal) lim = min(lim, i - k0 + 1);
-            const bool full = lim >= kBlockN;
-            uint32_t sr[4][32];
+            uint32_t sr[kChunks][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(sbase + c * 32, sr[c]);
+            for (int c = 0; c < kChunks; ++c) tmem_ld32(sbase + c * 32, sr[c]);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+            for (int c = 0; c < kChunks; ++c) reg_fence(sr[c]);
             // S(u) is in registers: the S columns may take S(u+1)
             tc_fence_before();
             mbar_arrive_warp(&st->s_free);
-            // P(u-1) V must have completed before O is rescaled or P(u)
-            // written over P(u-1)
-            bool pv_waited = (u == 0);
-            if (!full) {
+            if (lim < kCols) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < kChunks; ++c)
 #pragma unroll
                     for (int x = 0; x < 32; ++x)
                         if (c * 32 + x >= lim) sr[c][x] = __float_as_uint(-INFINITY);
@@ -284,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int x = 0; x < 8; ++x) pm[x] = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < kChunks; ++c)
 #pragma unroll
                 for (int x = 0; x < 32; x += 2)
                     pm[(x >> 1) & 7] =
@@ -293,8 +329,24 @@ __global__ void __launch_bounds__(kThreads, 2)
             pm[3] = fmax3(pm[3], pm[4], pm[5]);
             pm[6] = fmaxf(pm[6], pm[7]);
             pm[0] = fmax3(pm[0], pm[3], pm[6]);
+            if constexpr (Lay::kHalves == 2) {
+                // the row maximum of the tile from both halves (buffer u & 1:
+                // a half writes it again at u + 2 only after both halves have
+                // passed the exchange of u + 1, so after this one's reads)
+                float* mx = sMax + (u & 1) * 256;
+                mx[half * 128 + r] = pm[0];
+                mbar_arrive_warp(&st->mx_ready[u & 1]);
+                if (!mbar_wait_warp(&st->mx_ready[u & 1], (u >> 1) & 1, wctx, 384)) {
+                    ok = false;
+                    break;
+                }
+                pm[0] = fmaxf(pm[0], mx[(half ^ 1) * 128 + r]);
+            }
             const float mt = pm[0] * p.scale_log2;
             const bool raise = mt > m + kRescaleThreshold;
+            // P(u-1) V must have completed before O is rescaled or P(u)
+            // written over P(u-1)
+            bool pv_waited = (u == 0);
             if (__any_sync(0xffffffffu, raise) && u > 0) {
                 if (!mbar_wait_warp(&st->pv_done, (u - 1) & 1, wctx, 382)) {
                     ok = false;
@@ -304,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 pv_waited = true;
                 const float alpha = raise ? ex2_approx(m - mt) : 1.f;
 #pragma unroll 1
-                for (int c = 0; c < kD / 8; ++c) {
+                for (int c = 0; c < kOCols / 8; ++c) {
                     uint32_t orr[8];
                     tmem_ld8(obase + c * 8, orr);
                     tmem_ld_wait();
@@ -321,17 +373,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             float ps[8];
 #pragma unroll
             for (int x = 0; x < 8; ++x) ps[x] = 0.f;
-            // exponentials packed in place (P chunk c in sr[c][0..15], stored
-            // to P columns 16c..16c+15 once P(u-1) V is done); the sum takes
-            // every exponential, the dropout mask only what goes to P. Without
-            // dropout all four chunks are stored after the last exponential,
-            // so the wait for P(u-1) V comes as late as possible; with dropout
-            // (whose keep bits take longer than the products) the wait comes
-            // first and each chunk is stored as soon as it is packed, which
-            // keeps fewer registers live.
+            // exponentials packed in place (P chunk c in sr[c][0..15], this
+            // thread's P columns 16c..16c+15); the sum takes every
+            // exponential, the dropout mask only what goes to P. Without
+            // dropout all chunks are stored after the last exponential, so the
+            // wait for P(u-1) V comes as late as possible; with dropout the
+            // wait comes first and each chunk is stored as soon as it is
+            // packed, which keeps fewer registers live.
             if constexpr (!kDrop) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
                     for (int x = 0; x < 32; x += 2) {
                         float a0, a1;
@@ -352,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     pv_waited = true;
                 }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
                     for (int x = 0; x < 32; x += 2) {
                         float a0, a1;
@@ -379,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tc_fence_after();
                 }
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < kChunks; ++c)
                     tmem_st16(pbase + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&sr[c][0]));
             }
             tmem_st_wait();
@@ -388,17 +439,26 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         T* O = static_cast<T*>(p.o) + ((size_t)bh * p.N) * kD;
         if (ok && n > 0) {
-            if (mbar_wait_warp(&st->o_final, 0, wctx, 381)) {
+            bool ready = true;
+            float lt = l;
+            if constexpr (Lay::kHalves == 2) {
+                // the row sum is the two halves' shares
+                sL[half * 128 + r] = l;
+                mbar_arrive_warp(&st->l_ready);
+                ready = mbar_wait_warp(&st->l_ready, 0, wctx, 385);
+                if (ready) lt += sL[(half ^ 1) * 128 + r];
+            }
+            if (ready && mbar_wait_warp(&st->o_final, 0, wctx, 381)) {
                 tc_fence_after();
-                const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+                const float inv = (lt > 0.f) ? p.out_scale / lt : 0.f;
 #pragma unroll
-                for (int c = 0; c < kD / 32; ++c) {
+                for (int c = 0; c < kOCols / 32; ++c) {
                     uint32_t orr[32];
                     tmem_ld32(obase + c * 32, orr);
                     tmem_ld_wait();
                     reg_fence(orr);
                     if (i < p.N) {
-                        uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * kD + c * 32);
+                        uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * kD + kOCols * half + c * 32);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint4 w4;
@@ -410,21 +470,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                         }
                     }
                 }
-                if (i < p.N) p.lse[(size_t)bh * p.N + i] = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+                if (half == 0 && i < p.N) p.lse[(size_t)bh * p.N + i] = (lt > 0.f) ? (m + __log2f(lt)) * kLn2 : -INFINITY;
             }
         } else if (n == 0 && i < p.N) {
             const uint4 z = make_uint4(0, 0, 0, 0);
-            uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * kD);
+            uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * kD + kOCols * half);
 #pragma unroll
-            for (int v = 0; v < kD / 8; ++v) dst[v] = z;
-            p.lse[(size_t)bh * p.N + i] = -INFINITY;
+            for (int v = 0; v < kOCols / 8; ++v) dst[v] = z;
+            if (half == 0) p.lse[(size_t)bh * p.N + i] = -INFINITY;
         }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <typename T, bool kSplit, bool kDrop>
@@ -459,7 +519,7 @@ int launch_1t(const Problem& pr) {
         // launched with, or the softmax warps would wait forever
         cudaFuncAttributes a{};
         if (cudaFuncGetAttributes(&a, kernel) != cudaSuccess ||
-            a.numRegs * kThreads < 128 * kSoftRegs + 128 * kIssueRegs) {
+            a.numRegs * Layout1t<kDrop>::kThreads < Layout1t<kDrop>::kBudget) {
             if (std::getenv("FA_DEBUG"))
                 std::fprintf(stderr, "fa: fwd_1t register budget exceeds the launch allocation (%d regs)\n", a.numRegs);
             return FA_ERR_CUDA;
@@ -472,7 +532,7 @@ int launch_1t(const Problem& pr) {
     cudaLaunchConfig_t cfg = {};
     if (p.n_qtiles > 65535) return FA_ERR_UNSUPPORTED;
     cfg.gridDim = dim3(BH, p.n_qtiles);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Layout1t<kDrop>::kThreads);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = pr.stream;
     cfg.attrs = pdl;
