@@ -100,8 +100,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * output gradient dO, writes dq, dk, dv (dtype, [B,H,N,d]). S and P are
  * recomputed tile by tile from lse; the same masks, scale and dropout
  * (seed, p) as the forward must be passed. workspace is caller-owned device
- * memory of at least fa_bwd_workspace_size(B,H,N,d) bytes, 256-byte aligned;
- * its contents on entry do not matter and on exit are unspecified.
+ * memory of at least fa_bwd_workspace_size(B,H,N,d) bytes, 256-byte aligned
+ * (rowsum(dO o O), the fp32 dQ accumulator and a work counter: about
+ * B*H*N*(d+1)*4 + 256 bytes); its contents on entry do not matter and on
+ * exit are unspecified.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dO, void* dq, void* dk, void* dv,
@@ -195,8 +197,9 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int n_splits);
 
 /*
  * Bytes of backward workspace: rowsum(dO o O) (fp32 [B,H,N]) plus the fp32
- * dQ accumulator ([B,H,N,d]), each rounded up to 256 bytes. O(B*H*N*d): the
- * backward keeps no N x N state. Returns 0 for invalid sizes.
+ * dQ accumulator ([B,H,N,d]), each rounded up to 256 bytes, plus 256 bytes
+ * for the counter through which the backward's CTAs claim work. O(B*H*N*d):
+ * the backward keeps no N x N state. Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 

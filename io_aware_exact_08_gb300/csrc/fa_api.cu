@@ -229,7 +229,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 0 || (d != 64 && d != 128 && d != 256)) return 0;
     const size_t rows = (size_t)B * H * N;
-    return round256(rows * sizeof(float)) + round256(rows * (size_t)d * sizeof(float));
+    // rowsum(dO o O), the fp32 dQ accumulator, the backward's work counter
+    return round256(rows * sizeof(float)) + round256(rows * (size_t)d * sizeof(float)) + 256;
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
@@ -259,6 +260,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     const size_t rows = (size_t)B * H * N;
     p.delta = static_cast<float*>(workspace);
     p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)));
+    p.item_ctr = reinterpret_cast<int*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)) +
+                                        round256(rows * (size_t)d * sizeof(float)));
     bool tc = false;
     rc = pick_path(p, true, &tc);
     if (rc != FA_OK) return rc;

@@ -92,7 +92,9 @@ struct BwdCfg {
         2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBuffers * kDsBytes + kDqStageBytes +
         2 * 2 * kTile * 4 /*lse, delta x2*/ + 256;
     static_assert(kSmemBase + kListCap * 2 <= 232448, "shared memory");
-    static constexpr int smem(bool mask) { return kSmemBase + (mask ? kListCap * 2 : 0); }
+    // a persistent CTA with a block mask keeps two item lists (D = 64 only)
+    static_assert(D != 64 || kSmemBase + kListCap * 4 <= 232448, "shared memory");
+    static constexpr int smem(bool mask, bool ring) { return kSmemBase + (mask ? kListCap * 2 * (ring ? 2 : 1) : 0); }
     static constexpr uint32_t kColS = 0, kColDP = 128;
     // dQ accumulator. D = 128: dQ^T (lanes = head-dim rows, 128 query
     // columns), aliasing dP^T. D = 64: dQ (lanes = query rows, 64 columns).
@@ -114,6 +116,7 @@ struct BwdParams {
     int* status;
     int H, N, nb;
     int BH, nkt;  // heads x batch, key tiles: the work items are (bh, key tile)
+    int* item_ctr;  // persistent grid: items claimed past each CTA's first (zeroed by the preprocess kernel)
     float scale;
     float scale_log2;
     float keep_scale;  // 1/(1-p)
@@ -136,10 +139,14 @@ struct BwdShared {
     uint64_t kv_empty;     // K_j, V_j read by the item's last MMA
     uint64_t teardown;
     uint64_t lse_ready[2];
+    uint64_t list_full[2];  // block mask, persistent: item list of buffer b built
+    uint64_t list_free[2];  // ... and released by every warp that reads it
     uint32_t tmem_base;
     int abort_flag;
-    int n_list;  // block mask: visible query tiles of this key tile
+    int n_list[2];  // block mask: visible query tiles of the item's key tile (per list buffer)
+    int ring_item[2];  // persistent grid: the item of ring buffer b (n_items: no more work)
 };
+static_assert(sizeof(BwdShared) <= 256, "barrier block");
 
 // Query tiles that see key tile j, in increasing order: without a block
 // mask (kMask false) the suffix [first, nqt) (first = j when causal), with
@@ -190,9 +197,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using Cfg = BwdCfg<D>;
-    // kPersist: a CTA walks several items (persistent grid, never with a
-    // block mask); otherwise every CTA runs exactly one item
-    static_assert(!(kPersist && kMask), "a block mask's tile list is built for one item");
+    // kPersist: a CTA walks several items (persistent grid); otherwise every
+    // CTA runs exactly one item. With a block mask and a persistent grid
+    // (kRing) each item's list of query tiles goes into one of two buffers
+    constexpr bool kRing = kMask && kPersist;
+    static_assert(!kRing || D == 64, "two item lists fit in shared memory at D = 64 only");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & 1023u) {  // swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0 && atomicCAS(p.status, 0, (int)FA_ERR_CUDA) == 0) atomicExch(p.status + 1, 130);
@@ -213,42 +222,40 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Work items are (bh, key tile) pairs, item = bh + BH * key tile, so
     // under a causal mask the heaviest key tiles (lowest j) of every head come
-    // first. At D = 128 without a block mask the grid is persistent (one CTA
-    // per SM), each CTA walking its items (item_of below); the barriers run on across
-    // items, counted by the global step gs + it and the item count gi, so the
-    // next item's loads and first products overlap the previous item's last
-    // products and its dK/dV stores. Otherwise each CTA takes one item (with
-    // a block mask, its list of query tiles is built once, below).
+    // first. A CTA of the one-item grid takes item = its index. In the
+    // persistent grid (one CTA per SM) a CTA's first item is its index too
+    // and warp 10 claims each further one from a counter in the workspace, so
+    // items go out in order to whichever CTA is free (the balance of the
+    // hardware's dispatch, without the CTA set-up between items), and
+    // publishes it, with its list of query tiles under a block mask, in one of
+    // two alternating buffers that every other role reads before the item;
+    // the barriers run on across items, counted by the global step gs + it
+    // and the item count gi, so the next item's loads and first products
+    // overlap the previous item's last products and its dK/dV stores.
     const int n_items = p.BH * p.nkt;
     const int n_ctas = gridDim.x * gridDim.y;
     const int cta = blockIdx.x + blockIdx.y * gridDim.x;
-    // the CTA's r-th item: items go out in rounds of n_ctas, left to right
-    // in even rounds and right to left in odd ones, so every CTA gets a mix
-    // of the heavy (early) and light (late) causal items
-    auto item_of = [&](int r) {
-        return r * n_ctas + ((r & 1) ? (n_ctas - 1 - cta) : cta);
-    };
-    const int item0 = item_of(0);
+    const int item0 = cta;
     const int nqt = (p.N + kTile - 1) / kTile;
-    auto make_sched = [&](int item) {
+    auto make_sched = [&](int item, int rr) {
         QSched<kMask> q;
         const int bh_ = item % p.BH;
         q.jt = item / p.BH;
         q.nqt = nqt;
         q.L = p.kv_len ? min(max(p.kv_len[bh_ / p.H], 0), p.N) : p.N;
         q.causal = p.causal;
-        q.list = sList;
+        q.list = sList + (kRing ? (rr & 1) * Cfg::kListCap : 0);
         q.n_list = 0;
         return q;
     };
     WaitCtx wctx{&st->abort_flag, p.status};
     // block mask (one item per CTA): warp 0 lists the query tiles whose mask
     // block (i, j) is set (strided loads of one mask column and a ballot)
-    if (kMask && warp == 0 && item0 < n_items) {
+    if (kMask && !kRing && warp == 0 && item0 < n_items) {
         const int jt0 = item0 / p.BH;
         const int first = p.causal ? jt0 : 0;
         const int cnt = warp_list_visible(p.block_mask + jt0, (size_t)p.nb, first, nqt, sList, lane);
-        if (lane == 0) st->n_list = cnt;
+        if (lane == 0) st->n_list[0] = cnt;
     }
 
     if (tid == 0) {
@@ -268,6 +275,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_init(&st->acc_free, kComputeThreads / 32);
         mbar_init(&st->kv_empty, 1);
         mbar_init(&st->teardown, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&st->list_full[b], 1);
+            mbar_init(&st->list_free[b], 14);  // producer, MMA, 8 compute and 4 reduction warps
+        }
         st->abort_flag = 0;
         fence_mbar_init();
     }
@@ -280,11 +291,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = st->tmem_base;
     // the item's query-step schedule and number of steps
-    auto item_sched = [&](int item, int& n_active) {
-        QSched<kMask> q = make_sched(item);
-        if constexpr (kMask) q.n_list = st->n_list;
+    auto item_sched = [&](int item, int rr, int& n_active) {
+        QSched<kMask> q = make_sched(item, rr);
+        if constexpr (kMask) q.n_list = st->n_list[kRing ? (rr & 1) : 0];
         n_active = q.count();
         return q;
+    };
+    // persistent grid: before its rr-th item a reading warp releases ring
+    // buffer (rr - 1) & 1 and waits until buffer rr & 1 holds the next item
+    // (one thread per warp arrives; the producer's loop runs on one lane)
+    auto list_acquire = [&](int rr, bool warp_wide) -> bool {
+        if constexpr (!kPersist) return true;
+        if (rr > 0) {
+            if (warp_wide) mbar_arrive_warp(&st->list_free[(rr - 1) & 1]);
+            else mbar_arrive(&st->list_free[(rr - 1) & 1]);
+        }
+        return warp_wide ? mbar_wait_warp(&st->list_full[rr & 1], (rr >> 1) & 1, wctx, 140)
+                         : mbar_wait(&st->list_full[rr & 1], (rr >> 1) & 1, wctx, 140);
     };
     // The next kernel (dq conversion) may start launching once every CTA is
     // here. Q, K, V, dO and LSE were complete before the preprocess kernel
@@ -305,9 +328,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             for (int s = 0; s < Cfg::kStages; ++s) issued_any[s] = false;
             bool okp = true;
             int gs = 0, gi = 0;  // steps and items with work, so far
-            for (int rr = 0, item = item0; okp && item < n_items && (kPersist || rr == 0); item = item_of(++rr)) {
+            for (int rr = 0; okp && (kPersist || rr == 0); ++rr) {
+                if (!list_acquire(rr, false)) break;
+                const int item = kPersist ? st->ring_item[rr & 1] : item0;
+                if (item >= n_items) break;
                 int n_active;
-                const QSched<kMask> sched = item_sched(item, n_active);
+                const QSched<kMask> sched = item_sched(item, rr, n_active);
                 if (n_active == 0) continue;
                 const int bh = item % p.BH;
                 const int j0 = sched.jt * kTile;
@@ -357,8 +383,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             if (gi > 0) mbar_wait(&st->kv_full, (gi - 1) & 1, wctx, 103);
         }
     } else if (warp == 10 || warp == 11) {
-        // idle: the rest of the producer / MMA warpgroup
+        // the rest of the producer / MMA warpgroup. In the persistent grid
+        // warp 10 fills the item ring: buffer rr & 1, once every reader has
+        // released the item before it there (rr - 2), gets the CTA's rr-th
+        // item (its index for rr = 0, then claimed from the counter, n_items
+        // once none is left) and, with a block mask, the item's query tiles.
+        // Warp 11 is idle.
         regs_dec<Cfg::kIssueRegs>();
+        if constexpr (kPersist) {
+            if (warp == 10) {
+                for (int rr = 0;; ++rr) {
+                    if (rr >= 2 && !mbar_wait_warp(&st->list_free[rr & 1], ((rr - 2) >> 1) & 1, wctx, 141)) break;
+                    int item = item0;
+                    if (rr > 0) {
+                        if (rr == 1) pdl_wait();  // the counter is zeroed by the preprocess kernel
+                        int claimed = 0;
+                        if (lane == 0) claimed = atomicAdd(p.item_ctr, 1);
+                        item = n_ctas + __shfl_sync(0xffffffffu, claimed, 0);
+                    }
+                    item = min(item, n_items);
+                    if (kMask && item < n_items) {
+                        const int jt = item / p.BH;
+                        const int cnt = warp_list_visible(p.block_mask + jt, (size_t)p.nb, p.causal ? jt : 0, nqt,
+                                                          sList + (rr & 1) * Cfg::kListCap, lane);
+                        if (lane == 0) st->n_list[rr & 1] = cnt;
+                    }
+                    if (lane == 0) st->ring_item[rr & 1] = item;
+                    mbar_arrive_warp(&st->list_full[rr & 1]);
+                    if (item >= n_items) break;
+                }
+            }
+        }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         regs_dec<Cfg::kIssueRegs>();
@@ -378,9 +433,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const uint64_t kd_mn2 = smem_desc_sw128(k_base, kTile * 128, 1024);    // K, MN-major (M = d)
             bool ok = true;
             int gs = 0, gi = 0;  // steps and items with work, so far
-            for (int rr = 0, item = item0; ok && item < n_items && (kPersist || rr == 0); item = item_of(++rr)) {
+            for (int rr = 0; ok && (kPersist || rr == 0); ++rr) {
+            if (!list_acquire(rr, true)) break;
+            const int item = kPersist ? st->ring_item[rr & 1] : item0;
+            if (item >= n_items) break;
             int n_active;
-            (void)item_sched(item, n_active);
+            (void)item_sched(item, rr, n_active);
             if (n_active == 0) continue;
             if (!mbar_wait_warp(&st->kv_full, gi & 1, wctx, 110)) break;
             tc_fence_after();
@@ -595,9 +653,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         uint8_t* dq_buf = sDQ + quarter * 4096;  // D = 64: this warp's 32 x 32 fp32 box
         if (Cfg::kDqBulk && lane == 0) prefetch_tmap(&tm_dq);
         pdl_wait();
-        for (int rr = 0, item = item0; ok && item < n_items && (kPersist || rr == 0); item = item_of(++rr)) {
+        for (int rr = 0; ok && (kPersist || rr == 0); ++rr) {
+        if (!list_acquire(rr, true)) break;
+        const int item = kPersist ? st->ring_item[rr & 1] : item0;
+        if (item >= n_items) break;
         int n_active;
-        const QSched<kMask> sched = item_sched(item, n_active);
+        const QSched<kMask> sched = item_sched(item, rr, n_active);
         if (n_active == 0) continue;
         const int bh = item % p.BH;
         int it = 0;
@@ -676,9 +737,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         bool ok = true;
         int gs = 0, gi = 0;  // steps and items with work, so far
         pdl_wait();
-        for (int rr = 0, item = item0; ok && item < n_items && (kPersist || rr == 0); item = item_of(++rr)) {
+        for (int rr = 0; ok && (kPersist || rr == 0); ++rr) {
+        if (!list_acquire(rr, true)) {
+            ok = false;
+            break;
+        }
+        const int item = kPersist ? st->ring_item[rr & 1] : item0;
+        if (item >= n_items) break;
         int n_active;
-        const QSched<kMask> sched = item_sched(item, n_active);
+        const QSched<kMask> sched = item_sched(item, rr, n_active);
         const int bh = item % p.BH;
         const int b = bh / p.H, h = bh % p.H;
         const int j0 = sched.jt * kTile;
@@ -945,10 +1012,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_pre_tc_kernel(const T* __restrict__ O, const T* __restrict__ dO,
                                                          float* __restrict__ delta, float* __restrict__ dq_acc,
-                                                         size_t rows) {
+                                                         int* __restrict__ item_ctr, size_t rows) {
     constexpr int TPR = D / 8;  // threads per row (8 or 16)
     pdl_wait();               // O comes from the forward kernel
     pdl_trigger();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *item_ctr = 0;  // the main kernel's work counter
     const size_t row = ((size_t)blockIdx.x * 256 + threadIdx.x) / TPR;
     const int t = threadIdx.x % TPR;
     // every lane takes part in the shuffles below; past the last row it
@@ -1013,7 +1081,7 @@ int launch_bwd_tc_d(const Problem& pr) {
     cfg.blockDim = dim3(256);
     cfg.gridDim = dim3((unsigned)((rows * (D / 8) + 255) / 256));
     if (cudaLaunchKernelEx(&cfg, bwd_pre_tc_kernel<T, D>, static_cast<const T*>(pr.o), static_cast<const T*>(pr.dO),
-                           pr.delta, pr.dq_acc, rows) != cudaSuccess)
+                           pr.delta, pr.dq_acc, pr.item_ctr, rows) != cudaSuccess)
         return FA_ERR_CUDA;
     note_launches(1);
 
@@ -1031,6 +1099,7 @@ int launch_bwd_tc_d(const Problem& pr) {
     p.nb = pr.nb;
     p.BH = BH;
     p.nkt = (pr.N + kTile - 1) / kTile;
+    p.item_ctr = pr.item_ctr;
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * kLog2e;
     p.keep_scale = 1.0f / (1.0f - pr.dropout_p);
@@ -1038,28 +1107,29 @@ int launch_bwd_tc_d(const Problem& pr) {
     p.dropout = pr.dropout_p > 0.f;
     p.causal = pr.causal;
     p.seed = pr.seed;
-    // without a block mask or per-sequence lengths the grid is persistent: one
-    // CTA per SM walking the (bh, key tile) items in a fixed order, so that
-    // one item's last products and dK/dV stores overlap the next one's loads
-    // and first products (gpt2_causal backward 377 -> 394 TFLOP/s). Key
-    // padding leaves items of very different length, which the hardware's
-    // dispatch of one CTA per item balances better (bert_pad_dropout 315
-    // against 298 persistent); with a block mask a CTA per item (its tile
-    // list is built once)
-    const bool persist = !pr.block_mask && !pr.kv_len;
-    auto kernel = pr.block_mask ? bwd_tc_kernel<T, D, true, false>
-                                : (persist ? bwd_tc_kernel<T, D, false, true> : bwd_tc_kernel<T, D, false, false>);
+    // The grid is persistent (one CTA per SM claiming items in order from the
+    // workspace counter), so that one item's last products and dK/dV stores
+    // overlap the next one's loads and first products; with a block mask the
+    // persistent CTA needs two item lists in shared memory, which fit at
+    // D = 64 only, and D = 128 keeps one CTA per item.
+    const bool persist = !pr.block_mask || D == 64;
+    using KernelFn = decltype(&bwd_tc_kernel<T, D, false, false>);
+    KernelFn kernel = nullptr;
+    KernelFn all[4] = {bwd_tc_kernel<T, D, false, false>, bwd_tc_kernel<T, D, false, true>,
+                       bwd_tc_kernel<T, D, true, false>, nullptr};
+    if constexpr (D == 64) all[3] = bwd_tc_kernel<T, D, true, true>;
+    kernel = all[(pr.block_mask ? 2 : 0) + (persist ? 1 : 0)];
+    if (!kernel) return FA_ERR_UNSUPPORTED;
     static bool attr_set = false;
     if (!attr_set) {
         // setmaxnreg.inc takes registers from what the CTA was launched with
         // and waits (without bound) until they are free: refuse to launch
         // unless the budgets fit in that allocation
-        decltype(kernel) all[3] = {bwd_tc_kernel<T, D, true, false>, bwd_tc_kernel<T, D, false, true>,
-                                   bwd_tc_kernel<T, D, false, false>};
-        for (int x = 0; x < 3; ++x) {
+        for (int x = 0; x < 4; ++x) {
+            if (!all[x]) continue;
             cudaFuncAttributes a{};
-            if (cudaFuncSetAttribute(all[x], cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::smem(x == 0)) !=
-                    cudaSuccess ||
+            if (cudaFuncSetAttribute(all[x], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg::smem(x >= 2, x == 3)) != cudaSuccess ||
                 cudaFuncGetAttributes(&a, all[x]) != cudaSuccess || a.numRegs * Cfg::kThreads < Cfg::kRegBudget) {
                 if (std::getenv("FA_DEBUG"))
                     std::fprintf(stderr, "fa: bwd register budget %d exceeds the launch allocation (%d regs)\n",
@@ -1080,7 +1150,7 @@ int launch_bwd_tc_d(const Problem& pr) {
         cfg.gridDim = dim3((unsigned)std::min<long long>(n_items, nsm), 1);
     }
     cfg.blockDim = dim3(Cfg::kThreads);
-    cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr);
+    cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr, pr.block_mask != nullptr && persist);
     record_main_start(pr.stream);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, tdq, p);
     record_main_stop(pr.stream);

@@ -34,6 +34,7 @@ struct Problem {
     const int32_t* kv_len;      // [B] or nullptr
     float* delta;               // workspace: rowsum(dO o O), fp32 [B,H,N]
     float* dq_acc;              // workspace: fp32 [B,H,N,d]
+    int* item_ctr = nullptr;    // workspace: the backward's work counter (zeroed by its first kernel)
     int* status;                // device status word (timeouts)
     cudaStream_t stream;
     // split-KV forward: n_splits key-tile ranges per pair of query tiles,
