@@ -157,17 +157,15 @@ struct QSched {
     const uint16_t* list;
     int n_list;
     __device__ bool key_tile_live() const { return jt * kTile < L; }
-    __device__ bool active(int i) const { return !(causal && i * kTile + kTile - 1 < jt * kTile); }
-    __device__ int next(int i) const {
-        while (i < nqt && !active(i)) ++i;
-        return i;
-    }
+    // without a block mask the query tiles that see key tile j are the range
+    // [j, nqt) under a causal mask (tile i holds a query at or after key
+    // 128 j exactly when i >= j) and [0, nqt) otherwise
+    __device__ int lo() const { return causal ? jt : 0; }
+    __device__ int next(int i) const { return min(max(i, lo()), nqt); }
     __device__ int count() const {
         if (!key_tile_live()) return 0;
         if constexpr (kMask) return n_list;
-        int c = 0;
-        for (int i = next(0); i < nqt; i = next(i + 1)) ++c;
-        return c;
+        return max(nqt - lo(), 0);
     }
     // the first query tile, and the one after i, the k-th (k from 0); nqt
     // past the last
