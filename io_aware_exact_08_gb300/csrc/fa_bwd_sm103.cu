@@ -9,23 +9,29 @@
 //   dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three launches:
-//   1. preprocess: delta_i = sum_c dO_ic O_ic (fp32) and dQacc = 0;
-//   2. main: one CTA per (128-key tile K_j/V_j, batch*head), looping over the
-//      query tiles i that see it. Per tile, on tensor cores:
+//   1. preprocess: delta_i = sum_c dO_ic O_ic (fp32), dQacc = 0 and the work
+//      counter = 0;
+//   2. main: work items are (128-key tile K_j/V_j, batch*head) pairs, each
+//      looping over the query tiles i that see it; one CTA per item, or (the
+//      persistent grid) one CTA per SM claiming items in order. Per tile, on
+//      tensor cores:
 //        S^T = K_j Q_i^T,  dP^T = V_j dO_i^T          (TMEM, fp32)
 //      eight compute warps (thread = key row, half of the 128 query columns
 //      each) rebuild P^T = exp(S^T - LSE), apply masks and dropout, and form
 //      dS^T = P^T o (dP^T - delta); P^T (16-bit) goes back into TMEM and dS^T
 //      (16-bit) into a swizzled shared-memory tile, then
 //        dV_j += P^T dO_i  (A from TMEM),  dK_j += dS^T Q_i,
-//        dQ_i^T = K_j^T dS^T (both operands read MN-major)
+//        dQ_i = dS K_j (both operands read MN-major)
 //      (at D = 128 computed transposed, dQ_i^T = K_j^T dS^T, so that a
-//      warp's reduction covers 32 consecutive floats of one row) and the
-//      reduction warps add it into the fp32 accumulator in global memory.
-//      dK_j, dV_j stay in TMEM until the end.
+//      warp's reduction covers 32 consecutive floats of one row), and the
+//      reduction warps add it into the fp32 accumulator in global memory
+//      (D = 128: red.global.add; D = 64: TMA bulk tensor reduce-adds of
+//      32 x 32 boxes staged in shared memory). dK_j, dV_j stay in TMEM until
+//      the item's end.
 //   3. convert: dq = dtype(scale * dQacc).
 // Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer (all 32
-// lanes run its loop, one elected lane issues), warps 10-11 idle (they
+// lanes run its loop, one elected lane issues), warp 10 claims the persistent
+// grid's items and builds their block-mask tile lists, warp 11 idle (they
 // complete the third warpgroup), warps 12-15 dQ reduction (one per TMEM lane
 // quarter), so that the compute warps never wait for the dQ product or for
 // the reductions to drain into L2.
