@@ -122,7 +122,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
  * every GPU it is loaded on until exit; nothing is allocated per call.
  *  - Returns FA_ERR_WORKSPACE, without launching, when
  *    fa_bwd_workspace_size(B,H,N,d) exceeds that size (about
- *    B*H*N*(d+1)*4 bytes).
+ *    B*H*N*(d+2)*4 bytes).
  *  - Calls share the array: calls whose kernels may overlap on the GPU
  *    (unordered streams) race and give wrong results. Each call clears the
  *    parts that must start at zero.
@@ -196,10 +196,12 @@ int fa_fwd_fp8(const void* q, const void* k, const void* vt,
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int n_splits);
 
 /*
- * Bytes of backward workspace: rowsum(dO o O) (fp32 [B,H,N]) plus the fp32
- * dQ accumulator ([B,H,N,d]), each rounded up to 256 bytes, plus 256 bytes
- * for the counter through which the backward's CTAs claim work. O(B*H*N*d):
- * the backward keeps no N x N state. Returns 0 for invalid sizes.
+ * Bytes of backward workspace: the per-row statistics (1 KB per 128-row tile
+ * of each head: -LSE and -rowsum(dO o O) of the tile's rows, padded past N)
+ * plus the fp32 dQ accumulator ([B,H,N,d]), each rounded up to 256 bytes,
+ * plus 256 bytes for the counter through which the backward's CTAs claim
+ * work. O(B*H*N*d): the backward keeps no N x N state. Returns 0 for invalid
+ * sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 

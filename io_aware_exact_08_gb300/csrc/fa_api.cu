@@ -26,6 +26,12 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Backward workspace for the per-row statistics: kColTableFloats floats per
+// (b*h, 128-row query tile), which also holds the plain [B,H,N] row sums.
+size_t stats_bytes(int B, int H, int N) {
+    return (size_t)B * H * ((N + kMaskBlock - 1) / kMaskBlock) * kColTableFloats * sizeof(float);
+}
+
 uint32_t keep_threshold(float p) {
     const double t = std::floor((double)p * 4294967296.0);
     if (t <= 0.0) return 0u;
@@ -229,8 +235,10 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 0 || (d != 64 && d != 128 && d != 256)) return 0;
     const size_t rows = (size_t)B * H * N;
-    // rowsum(dO o O), the fp32 dQ accumulator, the backward's work counter
-    return round256(rows * sizeof(float)) + round256(rows * (size_t)d * sizeof(float)) + 256;
+    // the per-row statistics (1 KB per 128-row tile: -LSE and -rowsum(dO o O)
+    // of the tile's rows, or the plain row sums), the fp32 dQ accumulator,
+    // the backward's work counter
+    return round256(stats_bytes(B, H, N)) + round256(rows * (size_t)d * sizeof(float)) + 256;
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
@@ -258,10 +266,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     p.dk = dk;
     p.dv = dv;
     const size_t rows = (size_t)B * H * N;
+    const size_t stats = round256(stats_bytes(B, H, N));
     p.delta = static_cast<float*>(workspace);
-    p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)));
-    p.item_ctr = reinterpret_cast<int*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)) +
-                                        round256(rows * (size_t)d * sizeof(float)));
+    p.col_table = static_cast<float*>(workspace);
+    p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + stats);
+    p.item_ctr = reinterpret_cast<int*>(static_cast<char*>(workspace) + stats + round256(rows * (size_t)d * sizeof(float)));
     bool tc = false;
     rc = pick_path(p, true, &tc);
     if (rc != FA_OK) return rc;

@@ -9,15 +9,18 @@
 //   dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three launches:
-//   1. preprocess: delta_i = sum_c dO_ic O_ic (fp32), dQacc = 0 and the work
-//      counter = 0;
+//   1. preprocess: per 128-row query tile a column table of -LSE_i log2(e)
+//      and -delta_i, delta_i = sum_c dO_ic O_ic (fp32, rows past N padded),
+//      dQacc = 0 and the work counter = 0;
 //   2. main: work items are (128-key tile K_j/V_j, batch*head) pairs, each
 //      looping over the query tiles i that see it; one CTA per item, or (the
-//      persistent grid) one CTA per SM claiming items in order. Per tile, on
-//      tensor cores:
+//      persistent grid) one CTA per SM claiming items in order. The TMA
+//      engine loads each step's Q_i, dO_i and column table into one stage.
+//      Per tile, on tensor cores:
 //        S^T = K_j Q_i^T,  dP^T = V_j dO_i^T          (TMEM, fp32)
-//      eight compute warps (thread = key row, half of the 128 query columns
-//      each) rebuild P^T = exp(S^T - LSE), apply masks and dropout, and form
+//      (D = 64: over all 128 queries; D = 128: per 64-query half), eight
+//      compute warps (thread = key row, half of the 128 query columns each)
+//      rebuild P^T = exp(S^T - LSE), apply masks and dropout, and form
 //      dS^T = P^T o (dP^T - delta); P^T (16-bit) goes back into TMEM and dS^T
 //      (16-bit) into a swizzled shared-memory tile, then
 //        dV_j += P^T dO_i  (A from TMEM),  dK_j += dS^T Q_i,
@@ -77,7 +80,11 @@ struct BwdCfg {
     static constexpr int kTileBytes = kTile * D * 2;  // one 128 x D 16-bit tile
     static constexpr int kBoxBytes = kTile * 128;     // 128 rows x 64 columns
     static constexpr int kBoxes = D / 64;
-    static constexpr int kStageBytes = 2 * kTileBytes;  // Q_i and dO_i
+    // a step's stage: Q_i, dO_i and the column table of its 128 queries
+    // (-LSE in log2 units, then -delta), loaded together by the TMA engine
+    static constexpr int kColBytes = kColTableFloats * 4;
+    static constexpr int kStageBytes = 2 * kTileBytes + kColBytes;
+    static_assert(kStageBytes % 1024 == 0, "stages keep the swizzled tiles 1024-byte aligned");
     static constexpr int kDsBytes = kTile * kTile * 2;  // dS^T, 128 x 128, 16-bit
     // D = 64 runs the next step's S^T/dP^T products while the current step's
     // dQ product still reads dS^T, so the tile is double-buffered by step
@@ -95,8 +102,7 @@ struct BwdCfg {
     // block masks: this key tile's list of visible query tiles
     static constexpr int kListCap = (D == 128) ? kMaskListCapBwd128 : kMaskListCap;
     static constexpr int kSmemBase =
-        2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBuffers * kDsBytes + kDqStageBytes +
-        2 * 2 * kTile * 4 /*lse, delta x2*/ + 256;
+        2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBuffers * kDsBytes + kDqStageBytes + 256;
     static_assert(kSmemBase + kListCap * 2 <= 232448, "shared memory");
     // a persistent CTA with a block mask keeps two item lists (D = 64 only)
     static_assert(D != 64 || kSmemBase + kListCap * 4 <= 232448, "shared memory");
@@ -108,12 +114,14 @@ struct BwdCfg {
     static constexpr uint32_t kColDQ = (D == 128) ? 128 : 256;
     static constexpr uint32_t kColDV = (D == 128) ? 256 : 320;
     static constexpr uint32_t kColDK = 384;
+    // D = 64: P^T (16-bit pairs, 128 keys x 128 queries) in columns of its
+    // own, so the next step's S^T may be written while dV still reads P^T
+    static constexpr uint32_t kColP = 448;
 };
 
 
 struct BwdParams {
-    const float* lse;
-    const float* delta;
+    const float* col_table;  // per (bh, query tile): -LSE log2(e), -delta of its 128 rows
     float* dq_acc;
     void* dk;
     void* dv;
@@ -136,15 +144,16 @@ struct BwdShared {
     uint64_t kv_full;
     uint64_t st_full[3];
     uint64_t st_empty[3];
-    uint64_t s_full[2];    // per 64-query half h: S^T_h and dP^T_h in TMEM
-    uint64_t p_ready[2];   // P^T_h in TMEM and dS^T_h in shared memory
+    uint64_t s_full[2];    // D = 128: per 64-query half h, S^T_h and dP^T_h in TMEM; D = 64: [0], the whole tile
+    uint64_t p_ready[2];   // P^T_h in TMEM and dS^T_h in shared memory (D = 64: [0], both halves)
+    uint64_t s_free;       // D = 64: S^T, dP^T read into the compute warps' registers
+    uint64_t p_free;       // D = 64: P^T read by the dV product
     uint64_t dq_full[2];   // dQ of half h (D = 128) / of the tile (D = 64, [0])
     uint64_t dq_free[2];   // that dQ read out of TMEM by the reduction warps
     uint64_t acc_done;
     uint64_t acc_free;     // dK, dV of the item read out of TMEM by the compute warps
     uint64_t kv_empty;     // K_j, V_j read by the item's last MMA
     uint64_t teardown;
-    uint64_t lse_ready[2];
     uint64_t list_full[2];  // block mask, persistent: item list of buffer b built
     uint64_t list_free[2];  // ... and released by every warp that reads it
     uint32_t tmem_base;
@@ -215,12 +224,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     uint8_t* sV = sK + Cfg::kTileBytes;
     uint8_t* sStages = sV + Cfg::kTileBytes;
     uint8_t* sDS = sStages + Cfg::kStages * Cfg::kStageBytes;
-    // -LSE (log2 units) and -delta of the step's 128 queries, double-buffered
-    // by step parity: a warp may stage step it+1 while others still read it
     uint8_t* sDQ = sDS + Cfg::kDsBuffers * Cfg::kDsBytes;  // D = 64: dQ staging, 4 KB per reduction warp
-    float* sNegLse = reinterpret_cast<float*>(sDQ + Cfg::kDqStageBytes);
-    float* sNegDelta = sNegLse + 2 * kTile;
-    BwdShared* st = reinterpret_cast<BwdShared*>(sNegDelta + 2 * kTile);
+    BwdShared* st = reinterpret_cast<BwdShared*>(sDQ + Cfg::kDqStageBytes);
     uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -270,11 +275,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(&st->s_full[h], 1);
-            mbar_init(&st->p_ready[h], kComputeThreads / 64);
+            mbar_init(&st->p_ready[h], kComputeThreads / (D == 64 ? 32 : 64));
             mbar_init(&st->dq_full[h], 1);
             mbar_init(&st->dq_free[h], kComputeThreads / 64);
-            mbar_init(&st->lse_ready[h], kComputeThreads / 64);
         }
+        mbar_init(&st->s_free, kComputeThreads / 32);
+        mbar_init(&st->p_free, 1);
         mbar_init(&st->acc_done, 1);
         mbar_init(&st->acc_free, kComputeThreads / 32);
         mbar_init(&st->kv_empty, 1);
@@ -331,6 +337,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             bool issued_any[Cfg::kStages];
             for (int s = 0; s < Cfg::kStages; ++s) issued_any[s] = false;
             bool okp = true;
+            bool pre_done = false;  // the preprocess kernel's column table is visible
             int gs = 0, gi = 0;  // steps and items with work, so far
             for (int rr = 0; okp && (kPersist || rr == 0); ++rr) {
                 if (!list_acquire(rr, false)) break;
@@ -341,7 +348,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 if (n_active == 0) continue;
                 const int bh = item % p.BH;
                 const int j0 = sched.jt * kTile;
-                // Q_i, dO_i of step t (global step gs + t) into its stage
+                // Q_i, dO_i and the column table of query tile i, step t
+                // (global step gs + t), into its stage
                 auto load_step = [&](int i, int t) -> bool {
                     const int g = gs + t;
                     const int s = g % Cfg::kStages;
@@ -355,6 +363,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         tma_load_3d(dq + x * Cfg::kBoxBytes, &tm_q, &st->st_full[s], x * 64, i * kTile, bh);
                         tma_load_3d(ddo + x * Cfg::kBoxBytes, &tm_do, &st->st_full[s], x * 64, i * kTile, bh);
                     }
+                    // the table is written by the preprocess kernel: the first
+                    // copy waits for it (Q_i, dO_i are already on their way)
+                    if (!pre_done) {
+                        pdl_wait();
+                        pre_done = true;
+                    }
+                    bulk_load_1d(dq + 2 * Cfg::kTileBytes, p.col_table + ((size_t)bh * nqt + i) * kColTableFloats,
+                                 Cfg::kColBytes, &st->st_full[s]);
                     issued_phase[s] = ph;
                     issued_any[s] = true;
                     return true;
@@ -447,38 +463,35 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             if (!mbar_wait_warp(&st->kv_full, gi & 1, wctx, 110)) break;
             tc_fence_after();
             if constexpr (D == 64) {
-            // Software-pipelined order: the next step's S^T_h/dP^T_h go right
-            // after this step's half-h gradient products, and the dQ product
-            // last, so the compute warps of one half work on the next step
-            // while the tensor core finishes this one, and neither half's
-            // chain (compute, gradient products, next scores) includes dQ:
-            //   [dV_0 dK_0](t) [S_0 dP_0](t+1) [dV_1 dK_1](t) [S_1 dP_1](t+1) [dQ](t)
-            // Each product that overwrites TMEM (S^T_h, dP^T_h) comes after
-            // the MMAs that read the old contents (in issue order) and after
-            // the compute warps released them (p_ready). dS^T alternates
-            // between two shared-memory tiles by step parity: dQ of step t
-            // reads its tile while step t + 1 writes the other, and step t + 2
-            // writes it again only after S^T(t + 2), issued after dQ(t), is
-            // complete.
-            auto issue_sdp = [&](int g2, int h) {  // g2: global step
+            // Software-pipelined order: the next step's S^T, dP^T (over all
+            // 128 queries, N = 128) are issued as soon as the compute warps
+            // have read this step's into registers (s_free), ahead of this
+            // step's gradient products, so the compute warps work on step
+            // t + 1 while the tensor core runs dV, dK, dQ of step t:
+            //   [S dP](t+1) [dV dK dQ](t) [S dP](t+2) [dV dK dQ](t+1) ...
+            // P^T has TMEM columns of its own; the compute warps write P^T of
+            // step t + 1 once dV(t) has read P^T(t) (p_free). dS^T alternates
+            // between two shared-memory tiles by step parity: dK, dQ of step t
+            // read their tile while step t + 1 writes the other, and step
+            // t + 2 writes it again only after S^T(t + 2), issued after dQ(t),
+            // is complete.
+            constexpr uint32_t id_s = idesc_f32acc(Elem16<T>::kFmt, kTile, kTile, 0, 0);  // S^T, dP^T (N = 128)
+            auto issue_sdp = [&](int g2) {  // g2: global step
                 const uint32_t qb = smem_u32(sStages + (g2 % Cfg::kStages) * Cfg::kStageBytes);
                 const uint64_t qk = smem_desc_sw128(qb, 16, 1024);
                 const uint64_t dk = smem_desc_sw128(qb + Cfg::kTileBytes, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss_warp(tmem + Cfg::kColS + 64 * h, desc_add(kd_k, kk * 32), desc_add(qk, kk * 32 + 8192 * h),
-                                id_sh, kk > 0);
+                    mma_ss_warp(tmem + Cfg::kColS, desc_add(kd_k, kk * 32), desc_add(qk, kk * 32), id_s, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss_warp(tmem + Cfg::kColDP + 64 * h, desc_add(vd_k, kk * 32), desc_add(dk, kk * 32 + 8192 * h),
-                                id_sh, kk > 0);
-                mma_commit_warp(&st->s_full[h]);
+                    mma_ss_warp(tmem + Cfg::kColDP, desc_add(vd_k, kk * 32), desc_add(dk, kk * 32), id_s, kk > 0);
+                mma_commit_warp(&st->s_full[0]);
             };
             if (ok) ok = mbar_wait_warp(&st->st_full[gs % Cfg::kStages], (gs / Cfg::kStages) & 1, wctx, 111);
             if (ok) {
                 tc_fence_after();
-                issue_sdp(gs, 0);
-                issue_sdp(gs, 1);
+                issue_sdp(gs);
             }
             for (int it = 0; ok && it < n_active; ++it) {
                 const int g = gs + it;
@@ -488,61 +501,58 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 const uint64_t qd_mn = smem_desc_sw128(q_base, Cfg::kBoxBytes, 1024);
                 const uint64_t dod_mn = smem_desc_sw128(do_base, Cfg::kBoxBytes, 1024);
                 const uint32_t dsb = (uint32_t)((g & 1) * Cfg::kDsBytes);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (!mbar_wait_warp(&st->p_ready[h], g & 1, wctx, 113)) {
+                if (it + 1 < n_active) {
+                    const int s1 = (g + 1) % Cfg::kStages;
+                    if (!mbar_wait_warp(&st->s_free, g & 1, wctx, 117) ||
+                        !mbar_wait_warp(&st->st_full[s1], ((g + 1) / Cfg::kStages) & 1, wctx, 111)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // the item's first products overwrite dV, dK: the compute
-                    // warps must have read out the previous item's
-                    if (it == 0 && h == 0 && gi > 0) {
-                        if (!mbar_wait_warp(&st->acc_free, (gi - 1) & 1, wctx, 116)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                    }
-                    const uint32_t acc = (it > 0 || h > 0) ? 1u : 0u;
-                    // dV += P^T_h dO_h (A from TMEM), dK += dS^T_h Q_h
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ts_warp(tmem + Cfg::kColDV, tmem + Cfg::kColS + 64 * h + kk * 8,
-                                    desc_add(dod_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss_warp(tmem + Cfg::kColDK, desc_add(dsd_k, dsb + h * (kTile * 128) + kk * 32),
-                                    desc_add(qd_mn, 8192 * h + kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
-                    if (h == 0) {
-                        if (it + 1 < n_active) {
-                            const int s1 = (g + 1) % Cfg::kStages;
-                            if (!mbar_wait_warp(&st->st_full[s1], ((g + 1) / Cfg::kStages) & 1, wctx, 111)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            issue_sdp(g + 1, 0);
-                        }
-                    } else {
-                        mma_commit_warp(&st->st_empty[s]);  // Q_i, dO_i read
-                        if (it + 1 < n_active) issue_sdp(g + 1, 1);
-                        // dQ = dS K_j over the whole tile, over the previous
-                        // step's dQ once it has been read out
-                        if (g > 0) {
-                            if (!mbar_wait_warp(&st->dq_free[0], (g - 1) & 1, wctx, 115)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                        }
-#pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ss_warp(tmem + Cfg::kColDQ, desc_add(dsd_mn, dsb + kk * 2048), desc_add(kd_mn, kk * 2048),
-                                        id_dq, kk > 0);
-                        mma_commit_warp(&st->dq_full[0]);
-                    }
+                    issue_sdp(g + 1);
                 }
+                if (!mbar_wait_warp(&st->p_ready[0], g & 1, wctx, 113)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // the item's first products overwrite dV, dK: the compute
+                // warps must have read out the previous item's
+                if (it == 0 && gi > 0) {
+                    if (!mbar_wait_warp(&st->acc_free, (gi - 1) & 1, wctx, 116)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                const uint32_t acc = (it > 0) ? 1u : 0u;
+                // dV += P^T dO (A from TMEM: query columns 16 kk.. of P^T in
+                // packed columns 8 kk..), then dK += dS^T Q (dS^T query half
+                // kk / 4 is shared-memory box kk / 4)
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ts_warp(tmem + Cfg::kColDV, tmem + Cfg::kColP + kk * 8, desc_add(dod_mn, kk * 2048), id_dv,
+                                (acc || kk > 0) ? 1u : 0u);
+                mma_commit_warp(&st->p_free);
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ss_warp(tmem + Cfg::kColDK, desc_add(dsd_k, dsb + (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
+                                desc_add(qd_mn, kk * 2048), id_dv, (acc || kk > 0) ? 1u : 0u);
+                mma_commit_warp(&st->st_empty[s]);  // Q_i, dO_i read
+                // dQ = dS K_j over the whole tile, over the previous step's dQ
+                // once it has been read out
+                if (g > 0) {
+                    if (!mbar_wait_warp(&st->dq_free[0], (g - 1) & 1, wctx, 115)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ss_warp(tmem + Cfg::kColDQ, desc_add(dsd_mn, dsb + kk * 2048), desc_add(kd_mn, kk * 2048), id_dq,
+                                kk > 0);
+                mma_commit_warp(&st->dq_full[0]);
             }
             } else {
             // D = 128: per 64-query half h, S^T_h = K_j Q_{i,h}^T and
@@ -733,14 +743,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int half = warp >> 2;        // query columns [64*half, 64*half + 64)
         const int r = quarter * 32 + lane;  // key row within the tile
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        // each warpgroup stages its own 64 query columns: row r < 64 the LSE
-        // of column 64 half + r, row r >= 64 the delta of column
-        // 64 half + r - 64; the value for the next tile is loaded early
-        const int col = 64 * half + (r & 63);
-        const bool stage_lse = r < 64;
         bool ok = true;
         int gs = 0, gi = 0;  // steps and items with work, so far
-        pdl_wait();
         for (int rr = 0; ok && (kPersist || rr == 0); ++rr) {
         if (!list_acquire(rr, true)) {
             ok = false;
@@ -768,36 +772,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             }
             continue;
         }
-        const float* col_src = (stage_lse ? p.lse : p.delta) + (size_t)bh * p.N;
         int it = 0;
-        int i_cur = sched.first();
-        float col_val;
-        {
-            const int qi = i_cur * kTile + col;
-            col_val = (qi < p.N) ? col_src[qi] : (stage_lse ? -INFINITY : 0.f);
-        }
-        for (int i = i_cur; i < sched.nqt; ++it) {
+        for (int i = sched.first(); i < sched.nqt; ++it) {
             const int g = gs + it;
             const int i0 = i * kTile;
             const int i_next = sched.after(i, it);
-            // per-query -LSE (log2 units; -inf for masked rows so P = 0) and
-            // -delta, negated so that each pair of columns takes one paired
-            // fma / add
-            const int lbuf = (g & 1) * kTile;
-            if (stage_lse)
-                sNegLse[lbuf + col] = (col_val == -INFINITY) ? -INFINITY : -(col_val * kLog2e);
-            else
-                sNegDelta[lbuf + col] = -col_val;
-            {
-                const int qi = i_next * kTile + col;
-                col_val = (i_next < nqt && qi < p.N) ? col_src[qi] : (stage_lse ? -INFINITY : 0.f);
-            }
-            // (an mbarrier rather than a named barrier, so the wait is bounded)
-            mbar_arrive_warp(&st->lse_ready[half]);
-            if (!mbar_wait_warp(&st->lse_ready[half], g & 1, wctx, 123)) {
-                ok = false;
-                break;
-            }
+            // per-query -LSE (log2 units; -inf for masked rows and rows past
+            // N, so P = 0) and -delta, negated so that each pair of columns
+            // takes one paired fma / add: the column table in the step's
+            // stage, loaded with Q_i and dO_i
+            const int sidx = g % Cfg::kStages;
+            const float* colt = reinterpret_cast<const float*>(sStages + sidx * Cfg::kStageBytes + 2 * Cfg::kTileBytes);
             // dropout keep bits of this row's 64 query columns, drawn before
             // S^T arrives (bit x of keep_w[ch] is query column
             // 64 half + 32 ch + x): lane (4a + w) draws the 4 keep bits of
@@ -821,7 +806,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     keep_w[ch] = keep;
                 }
             }
-            if (!mbar_wait_warp(&st->s_full[half], g & 1, wctx, 120)) {
+            if (!mbar_wait_warp(&st->s_full[D == 64 ? 0 : half], g & 1, wctx, 120) ||
+                !mbar_wait_warp(&st->st_full[sidx], (g / Cfg::kStages) & 1, wctx, 123)) {
                 ok = false;
                 break;
             }
@@ -838,9 +824,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             // D = 64: both chunks' P^T (TMEM) and dS^T (shared memory) are
             // stored after the second chunk is computed, so that the second
             // chunk's shared-memory reads of LSE and delta do not queue
-            // behind the first chunk's stores
-            uint32_t pk2[kLoadBoth ? 2 : 1][16];
-            uint32_t dsk2[kLoadBoth ? 2 : 1][16];
+            // behind the first chunk's stores; the 16-bit results are packed
+            // in place over the scores they came from (P^T pairs into S^T's
+            // registers, dS^T pairs into dP^T's: pair x/2 is written once
+            // elements x..x+3 are read), which leaves the compiler the
+            // registers to load LSE and delta ahead of their use. D = 128
+            // packs one chunk at a time into separate arrays.
+            uint32_t pk2[1][16];
+            uint32_t dsk2[1][16];
             if constexpr (kLoadBoth) {
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
@@ -853,6 +844,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     reg_fence(sr2[ch]);
                     reg_fence(dr2[ch]);
                 }
+                // S^T, dP^T are in registers: the next step's may be written
+                tc_fence_before();
+                mbar_arrive_warp(&st->s_free);
             }
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
@@ -868,8 +862,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 }
                 const uint32_t keep = keep_w[ch];
                 const bool edge = (cmin > cb) || (cmax < cb + 32);
-                uint32_t(&pk)[16] = pk2[kLoadBoth ? ch : 0];
-                uint32_t(&dsk)[16] = dsk2[kLoadBoth ? ch : 0];
+                uint32_t(&pk)[16] = pk2[0];
+                uint32_t(&dsk)[16] = dsk2[0];
+                auto put = [&](int idx, uint32_t pv, uint32_t dv) {
+                    if constexpr (kLoadBoth) {
+                        sr[idx] = pv;
+                        dr[idx] = dv;
+                    } else {
+                        pk[idx] = pv;
+                        dsk[idx] = dv;
+                    }
+                };
                 // columns outside [cmin, cmax) (causal diagonal, key padding,
                 // sequence end) are zeroed in S first, so the element loop
                 // below carries no per-element mask test
@@ -882,8 +885,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 if (!p.dropout) {
 #pragma unroll
                     for (int x = 0; x < 32; x += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4*>(sNegLse + lbuf + cb + x);
-                        const float4 d4 = *reinterpret_cast<const float4*>(sNegDelta + lbuf + cb + x);
+                        const float4 l4 = *reinterpret_cast<const float4*>(colt + cb + x);
+                        const float4 d4 = *reinterpret_cast<const float4*>(colt + kTile + cb + x);
                         float a[4], e[4], t[4], g[4];
                         ffma2(a[0], a[1], __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), sl2, sl2, l4.x, l4.y);
                         ffma2(a[2], a[3], __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]), sl2, sl2, l4.z, l4.w);
@@ -894,16 +897,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         fadd2(t[2], t[3], __uint_as_float(dr[x + 2]), __uint_as_float(dr[x + 3]), d4.z, d4.w);
                         fmul2(g[0], g[1], e[0], e[1], t[0], t[1]);
                         fmul2(g[2], g[3], e[2], e[3], t[2], t[3]);
-                        pk[x / 2] = Elem16<T>::pack2(e[0], e[1]);
-                        pk[x / 2 + 1] = Elem16<T>::pack2(e[2], e[3]);
-                        dsk[x / 2] = Elem16<T>::pack2(g[0], g[1]);
-                        dsk[x / 2 + 1] = Elem16<T>::pack2(g[2], g[3]);
+                        put(x / 2, Elem16<T>::pack2(e[0], e[1]), Elem16<T>::pack2(g[0], g[1]));
+                        put(x / 2 + 1, Elem16<T>::pack2(e[2], e[3]), Elem16<T>::pack2(g[2], g[3]));
                     }
                 } else {
 #pragma unroll
                     for (int x = 0; x < 32; x += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4*>(sNegLse + lbuf + cb + x);
-                        const float4 d4 = *reinterpret_cast<const float4*>(sNegDelta + lbuf + cb + x);
+                        const float4 l4 = *reinterpret_cast<const float4*>(colt + cb + x);
+                        const float4 d4 = *reinterpret_cast<const float4*>(colt + kTile + cb + x);
                         float a[4], e[4], z[4], t[4], g[4], pv[4];
                         ffma2(a[0], a[1], __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), sl2, sl2, l4.x, l4.y);
                         ffma2(a[2], a[3], __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]), sl2, sl2, l4.z, l4.w);
@@ -919,10 +920,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         ffma2(t[2], t[3], __uint_as_float(dr[x + 2]), __uint_as_float(dr[x + 3]), z[2], z[3], d4.z, d4.w);
                         fmul2(g[0], g[1], e[0], e[1], t[0], t[1]);
                         fmul2(g[2], g[3], e[2], e[3], t[2], t[3]);
-                        pk[x / 2] = Elem16<T>::pack2(pv[0], pv[1]);
-                        pk[x / 2 + 1] = Elem16<T>::pack2(pv[2], pv[3]);
-                        dsk[x / 2] = Elem16<T>::pack2(g[0], g[1]);
-                        dsk[x / 2 + 1] = Elem16<T>::pack2(g[2], g[3]);
+                        put(x / 2, Elem16<T>::pack2(pv[0], pv[1]), Elem16<T>::pack2(g[0], g[1]));
+                        put(x / 2 + 1, Elem16<T>::pack2(pv[2], pv[3]), Elem16<T>::pack2(g[2], g[3]));
                     }
                 }
                 // P^T into TMEM columns this warp has already read
@@ -939,19 +938,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 }
             }
             if constexpr (kLoadBoth) {
+                // P^T (own columns: query column c in packed column c / 2)
+                // once the previous step's dV product has read it
+                if (g > 0) {
+                    if (!mbar_wait_warp(&st->p_free, (g - 1) & 1, wctx, 124)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
 #pragma unroll
-                for (int ch = 0; ch < 2; ++ch) tmem_st16(tmem + lane_base + Cfg::kColS + half * 64 + ch * 16, pk2[ch]);
+                for (int ch = 0; ch < 2; ++ch)
+                    tmem_st16(tmem + lane_base + Cfg::kColP + half * 32 + ch * 16,
+                              *reinterpret_cast<const uint32_t(*)[16]>(&sr2[ch][0]));
                 uint8_t* row = sDS + (g & (Cfg::kDsBuffers - 1)) * Cfg::kDsBytes + half * (kTile * 128) + r * 128;
 #pragma unroll
                 for (int chunk = 0; chunk < 8; ++chunk) {
-                    const uint32_t* d4 = &dsk2[chunk >> 2][4 * (chunk & 3)];
+                    const uint32_t* d4 = &dr2[chunk >> 2][4 * (chunk & 3)];
                     *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = make_uint4(d4[0], d4[1], d4[2], d4[3]);
                 }
             }
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive_warp(&st->p_ready[half]);
+            mbar_arrive_warp(&st->p_ready[D == 64 ? 0 : half]);
             i = i_next;
         }
         if (!ok) break;
@@ -1011,21 +1021,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
-// delta_i = sum_c dO_ic O_ic and dQacc = 0 (16-bit inputs): D/8 threads per
-// row, 16-byte loads and stores, the row sum reduced across those threads.
+// The column table and dQacc = 0 (16-bit inputs). Rows are padded to whole
+// 128-row tiles per head (Np = 128 nqt); for row i of head bh the table entry
+// of query tile i / 128 gets -LSE_i log2(e) (-inf where LSE_i = -inf, so
+// P = 0) and -delta_i, delta_i = sum_c dO_ic O_ic, and rows past N get -inf
+// and 0. D/8 threads per row, 16-byte loads and stores, the row sum reduced
+// across those threads.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_pre_tc_kernel(const T* __restrict__ O, const T* __restrict__ dO,
-                                                         float* __restrict__ delta, float* __restrict__ dq_acc,
-                                                         int* __restrict__ item_ctr, size_t rows) {
+                                                         const float* __restrict__ lse, float* __restrict__ col_table,
+                                                         float* __restrict__ dq_acc, int* __restrict__ item_ctr, int N,
+                                                         int nqt, size_t padded_rows) {
     constexpr int TPR = D / 8;  // threads per row (8 or 16)
-    pdl_wait();               // O comes from the forward kernel
+    pdl_wait();               // O and LSE come from the forward kernel
     pdl_trigger();
     if (blockIdx.x == 0 && threadIdx.x == 0) *item_ctr = 0;  // the main kernel's work counter
-    const size_t row = ((size_t)blockIdx.x * 256 + threadIdx.x) / TPR;
+    const size_t prow = ((size_t)blockIdx.x * 256 + threadIdx.x) / TPR;
     const int t = threadIdx.x % TPR;
-    // every lane takes part in the shuffles below; past the last row it
-    // contributes zeros and stores nothing
-    const bool valid = row < rows;
+    const size_t np = (size_t)nqt * kTile;
+    const size_t bh = prow / np;
+    const int i = (int)(prow - bh * np);
+    // every lane takes part in the shuffles below; rows past N or past the
+    // last head contribute zeros and load nothing
+    const bool in_range = prow < padded_rows;
+    const bool valid = in_range && i < N;
+    const size_t row = bh * (size_t)N + (size_t)i;
     const uint4 zero4 = make_uint4(0, 0, 0, 0);
     const uint4 o4 = valid ? reinterpret_cast<const uint4*>(O + row * D)[t] : zero4;
     const uint4 g4 = valid ? reinterpret_cast<const uint4*>(dO + row * D)[t] : zero4;
@@ -1040,8 +1060,19 @@ __global__ void __launch_bounds__(256) bwd_pre_tc_kernel(const T* __restrict__ O
     }
 #pragma unroll
     for (int w = TPR / 2; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+    if (!in_range) return;
+    if (t == 0) {
+        float* ent = col_table + (bh * nqt + (size_t)(i / kTile)) * kColTableFloats + (i % kTile);
+        float nl = -INFINITY, nd = 0.f;
+        if (valid) {
+            const float l = lse[row];
+            nl = (l == -INFINITY) ? -INFINITY : -(l * kLog2e);
+            nd = -s;
+        }
+        ent[0] = nl;
+        ent[kTile] = nd;
+    }
     if (!valid) return;
-    if (t == 0) delta[row] = s;
     float4* acc = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * t;
     acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1072,6 +1103,8 @@ int launch_bwd_tc_d(const Problem& pr) {
         !make_tmap_f32_acc(&tdq, pr.dq_acc, BH, pr.N, D))
         return FA_ERR_CUDA;
     const size_t rows = (size_t)BH * pr.N;
+    const int nqt = (pr.N + kTile - 1) / kTile;
+    const size_t padded_rows = (size_t)BH * nqt * kTile;
     // The three kernels are launched with programmatic stream serialization:
     // each may start while the previous one drains and waits (pdl_wait) only
     // where it reads what that one wrote.
@@ -1083,15 +1116,15 @@ int launch_bwd_tc_d(const Problem& pr) {
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     cfg.blockDim = dim3(256);
-    cfg.gridDim = dim3((unsigned)((rows * (D / 8) + 255) / 256));
+    cfg.gridDim = dim3((unsigned)((padded_rows * (D / 8) + 255) / 256));
     if (cudaLaunchKernelEx(&cfg, bwd_pre_tc_kernel<T, D>, static_cast<const T*>(pr.o), static_cast<const T*>(pr.dO),
-                           pr.delta, pr.dq_acc, pr.item_ctr, rows) != cudaSuccess)
+                           static_cast<const float*>(pr.lse), pr.col_table, pr.dq_acc, pr.item_ctr, pr.N, nqt,
+                           padded_rows) != cudaSuccess)
         return FA_ERR_CUDA;
     note_launches(1);
 
     BwdParams p{};
-    p.lse = pr.lse;
-    p.delta = pr.delta;
+    p.col_table = pr.col_table;
     p.dq_acc = pr.dq_acc;
     p.dk = pr.dk;
     p.dv = pr.dv;

@@ -32,7 +32,12 @@ struct Problem {
     uint64_t seed;
     fa_dtype dtype;
     const int32_t* kv_len;      // [B] or nullptr
-    float* delta;               // workspace: rowsum(dO o O), fp32 [B,H,N]
+    float* delta;               // workspace: rowsum(dO o O), fp32 [B,H,N] (d = 256 and CUDA-core backward)
+    // workspace, the same bytes as delta (tensor-core backward at d = 64, 128):
+    // per (b*h, 128-row query tile) 128 floats -LSE*log2(e) then 128 floats
+    // -rowsum(dO o O), rows past N padded with -inf and 0 (kColTableFloats
+    // floats a tile)
+    float* col_table;
     float* dq_acc;              // workspace: fp32 [B,H,N,d]
     int* item_ctr = nullptr;    // workspace: the backward's work counter (zeroed by its first kernel)
     int* status;                // device status word (timeouts)
@@ -45,6 +50,8 @@ struct Problem {
 };
 
 constexpr int kMaxSplits = 64;
+
+constexpr int kColTableFloats = 256;
 
 constexpr int kMaskBlock = 128;
 // With a block mask the tensor-core kernels keep each CTA's list of visible

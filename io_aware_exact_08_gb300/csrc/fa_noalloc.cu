@@ -1,8 +1,8 @@
 // fa_bwd_noalloc: the backward pass for callers that cannot allocate device
 // memory themselves.
 //
-// fa_bwd needs a workspace (the per-row rowsum(dO o O) and the fp32 dQ
-// accumulator). Some callers have no way to provide one: a host framework
+// fa_bwd needs a workspace (the per-row statistics -LSE and rowsum(dO o O)
+// and the fp32 dQ accumulator). Some callers have no way to provide one: a host framework
 // whose caching allocator has already reserved the device's memory, a
 // latency-bound serving path where cudaMalloc (which can synchronise the
 // device and take unbounded time) is not allowed, or a plugin that is handed
