@@ -34,10 +34,12 @@
 //   3. convert: dq = dtype(scale * dQacc).
 // Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer (all 32
 // lanes run its loop, one elected lane issues), warp 10 claims the persistent
-// grid's items and builds their block-mask tile lists, warp 11 idle (they
-// complete the third warpgroup), warps 12-15 dQ reduction (one per TMEM lane
+// grid's items and builds their block-mask tile lists, warp 11 stores dK and
+// dV at D = 64 (TMA stores of tiles the compute warps stage in the item's K/V
+// buffer; idle at D = 128), warps 12-15 dQ reduction (one per TMEM lane
 // quarter), so that the compute warps never wait for the dQ product or for
-// the reductions to drain into L2.
+// the reductions to drain into L2. At D = 64 K_j, V_j alternate between two
+// buffers by item, so the next item's tiles load during this one.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -76,8 +78,13 @@ struct BwdCfg {
     static constexpr int kReduceRegs = 96;
     static constexpr int kRegBudget = 256 * kComputeRegs + 128 * kIssueRegs + 128 * kReduceRegs;
     static_assert(kRegBudget <= kThreads * 128, "register budgets above the launch allocation");
-    static constexpr int kStages = (D == 128) ? 2 : 3;
+    static constexpr int kStages = 2;
     static constexpr int kTileBytes = kTile * D * 2;  // one 128 x D 16-bit tile
+    // D = 64: K_j, V_j in two buffers alternating by item, so the next
+    // item's tiles load while this one runs (D = 128: one, shared memory is
+    // full)
+    static constexpr int kKvBuffers = (D == 64) ? 2 : 1;
+    static constexpr int kKvBytes = 2 * kTileBytes;  // K_j then V_j
     static constexpr int kBoxBytes = kTile * 128;     // 128 rows x 64 columns
     static constexpr int kBoxes = D / 64;
     // a step's stage: Q_i, dO_i and the column table of its 128 queries
@@ -97,12 +104,19 @@ struct BwdCfg {
     // memory accesses queued behind them.
     static constexpr bool kDqBulk = (D == 64);
     static constexpr int kDqStageBytes = kDqBulk ? 4 * 32 * 128 : 0;
+    // D = 64: dK, dV leave through TMA stores (issued by warp 11) of two
+    // 128 x 64 tiles staged in the item's own K/V buffer, whose products have
+    // completed when the accumulators are read; the buffer takes the next
+    // K/V tiles once the stores have read it. D = 128 stores rows from the
+    // compute warps.
+    static constexpr bool kTmaOut = (D == 64);
     // (no alignment slack: the dynamic shared memory window starts 1024-byte
     // aligned, which the kernel checks)
     // block masks: this key tile's list of visible query tiles
     static constexpr int kListCap = (D == 128) ? kMaskListCapBwd128 : kMaskListCap;
+    static constexpr int kBarBytes = 512;
     static constexpr int kSmemBase =
-        2 * kTileBytes /*K, V*/ + kStages * kStageBytes + kDsBuffers * kDsBytes + kDqStageBytes + 256;
+        kKvBuffers * kKvBytes + kStages * kStageBytes + kDsBuffers * kDsBytes + kDqStageBytes + kBarBytes;
     static_assert(kSmemBase + kListCap * 2 <= 232448, "shared memory");
     // a persistent CTA with a block mask keeps two item lists (D = 64 only)
     static_assert(D != 64 || kSmemBase + kListCap * 4 <= 232448, "shared memory");
@@ -141,9 +155,9 @@ struct BwdParams {
 };
 
 struct BwdShared {
-    uint64_t kv_full;
-    uint64_t st_full[3];
-    uint64_t st_empty[3];
+    uint64_t kv_full[2];   // K_j, V_j of the item in buffer b loaded
+    uint64_t st_full[2];
+    uint64_t st_empty[2];
     uint64_t s_full[2];    // D = 128: per 64-query half h, S^T_h and dP^T_h in TMEM; D = 64: [0], the whole tile
     uint64_t p_ready[2];   // P^T_h in TMEM and dS^T_h in shared memory (D = 64: [0], both halves)
     uint64_t s_free;       // D = 64: S^T, dP^T read into the compute warps' registers
@@ -152,7 +166,8 @@ struct BwdShared {
     uint64_t dq_free[2];   // that dQ read out of TMEM by the reduction warps
     uint64_t acc_done;
     uint64_t acc_free;     // dK, dV of the item read out of TMEM by the compute warps
-    uint64_t kv_empty;     // K_j, V_j read by the item's last MMA
+    uint64_t kv_empty[2];  // buffer b free: its K_j, V_j read by the item's MMAs (D = 64: and its dK, dV stored)
+    uint64_t out_staged[2];  // D = 64: the item's dK, dV tiles staged in K/V buffer b (8 compute warps)
     uint64_t teardown;
     uint64_t list_full[2];  // block mask, persistent: item list of buffer b built
     uint64_t list_free[2];  // ... and released by every warp that reads it
@@ -161,7 +176,7 @@ struct BwdShared {
     int n_list[2];  // block mask: visible query tiles of the item's key tile (per list buffer)
     int ring_item[2];  // persistent grid: the item of ring buffer b (n_items: no more work)
 };
-static_assert(sizeof(BwdShared) <= 256, "barrier block");
+static_assert(sizeof(BwdShared) <= 512, "barrier block");
 
 // Query tiles that see key tile j, in increasing order: without a block
 // mask (kMask false) the suffix [first, nqt) (first = j when causal), with
@@ -208,7 +223,8 @@ template <typename T, int D, bool kMask, bool kPersist>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                  const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
     using Cfg = BwdCfg<D>;
     // kPersist: a CTA walks several items (persistent grid); otherwise every
     // CTA runs exactly one item. With a block mask and a persistent grid
@@ -220,13 +236,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (threadIdx.x == 0 && atomicCAS(p.status, 0, (int)FA_ERR_CUDA) == 0) atomicExch(p.status + 1, 130);
         return;
     }
-    uint8_t* sK = smem_raw;
-    uint8_t* sV = sK + Cfg::kTileBytes;
-    uint8_t* sStages = sV + Cfg::kTileBytes;
+    uint8_t* sK = smem_raw;  // K/V buffer b: K at sK + b kKvBytes, V kTileBytes after it
+    uint8_t* sStages = sK + Cfg::kKvBuffers * Cfg::kKvBytes;
     uint8_t* sDS = sStages + Cfg::kStages * Cfg::kStageBytes;
     uint8_t* sDQ = sDS + Cfg::kDsBuffers * Cfg::kDsBytes;  // D = 64: dQ staging, 4 KB per reduction warp
     BwdShared* st = reinterpret_cast<BwdShared*>(sDQ + Cfg::kDqStageBytes);
-    uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + 256);
+    uint16_t* sList = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(st) + Cfg::kBarBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Work items are (bh, key tile) pairs, item = bh + BH * key tile, so
@@ -268,7 +283,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
 
     if (tid == 0) {
-        mbar_init(&st->kv_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&st->kv_full[b], 1);
+            mbar_init(&st->kv_empty[b], Cfg::kTmaOut ? 2 : 1);  // the MMA commit (+ warp 11 after the stores)
+            mbar_init(&st->out_staged[b], kComputeThreads / 32);
+        }
         for (int s = 0; s < Cfg::kStages; ++s) {
             mbar_init(&st->st_full[s], 1);
             mbar_init(&st->st_empty[s], 1);
@@ -283,11 +302,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_init(&st->p_free, 1);
         mbar_init(&st->acc_done, 1);
         mbar_init(&st->acc_free, kComputeThreads / 32);
-        mbar_init(&st->kv_empty, 1);
         mbar_init(&st->teardown, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&st->list_full[b], 1);
-            mbar_init(&st->list_free[b], 14);  // producer, MMA, 8 compute and 4 reduction warps
+            // producer, MMA, 8 compute and 4 reduction warps (+ warp 11, the
+            // dK/dV store warp at D = 64)
+            mbar_init(&st->list_free[b], Cfg::kTmaOut ? 15 : 14);
         }
         st->abort_flag = 0;
         fence_mbar_init();
@@ -333,9 +353,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
-            uint32_t issued_phase[Cfg::kStages];
-            bool issued_any[Cfg::kStages];
-            for (int s = 0; s < Cfg::kStages; ++s) issued_any[s] = false;
+            // bit s: a load was issued into stage s / the phase of its last one
+            uint32_t issued_any = 0, issued_phase = 0;
             bool okp = true;
             bool pre_done = false;  // the preprocess kernel's column table is visible
             int gs = 0, gi = 0;  // steps and items with work, so far
@@ -371,24 +390,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     }
                     bulk_load_1d(dq + 2 * Cfg::kTileBytes, p.col_table + ((size_t)bh * nqt + i) * kColTableFloats,
                                  Cfg::kColBytes, &st->st_full[s]);
-                    issued_phase[s] = ph;
-                    issued_any[s] = true;
+                    issued_phase = (issued_phase & ~(1u << s)) | (ph << s);
+                    issued_any |= 1u << s;
                     return true;
                 };
-                // the item's first Q_i, dO_i go ahead of K_j, V_j: their stage
-                // frees before the previous item's last MMA has run
+                // With one K/V buffer the item's first Q_i, dO_i go ahead of
+                // K_j, V_j (their stage frees before the previous item's last
+                // MMA has run); with two, K_j and V_j go first, into buffer
+                // gi % 2, which the item before the previous one has released
+                // long before.
                 int i = sched.first();
-                if (!load_step(i, 0)) break;
-                i = sched.after(i, 0);
-                // K_j, V_j once the previous item's MMAs have read theirs
-                if (gi > 0 && !mbar_wait(&st->kv_empty, (gi - 1) & 1, wctx, 104)) break;
-                mbar_arrive_expect_tx(&st->kv_full, 2 * Cfg::kTileBytes);
+                int t0 = 0;
+                if constexpr (Cfg::kKvBuffers == 1) {
+                    if (!load_step(i, 0)) break;
+                    i = sched.after(i, 0);
+                    t0 = 1;
+                }
+                const int kb = gi % Cfg::kKvBuffers;
+                const int g_prev = gi - Cfg::kKvBuffers;  // the item that last used buffer kb
+                if (g_prev >= 0 && !mbar_wait(&st->kv_empty[kb], (g_prev / Cfg::kKvBuffers) & 1, wctx, 104)) break;
+                mbar_arrive_expect_tx(&st->kv_full[kb], Cfg::kKvBytes);
+                uint8_t* kv = sK + kb * Cfg::kKvBytes;
 #pragma unroll
                 for (int x = 0; x < Cfg::kBoxes; ++x) {
-                    tma_load_3d(sK + x * Cfg::kBoxBytes, &tm_k, &st->kv_full, x * 64, j0, bh);
-                    tma_load_3d(sV + x * Cfg::kBoxBytes, &tm_v, &st->kv_full, x * 64, j0, bh);
+                    tma_load_3d(kv + x * Cfg::kBoxBytes, &tm_k, &st->kv_full[kb], x * 64, j0, bh);
+                    tma_load_3d(kv + Cfg::kTileBytes + x * Cfg::kBoxBytes, &tm_v, &st->kv_full[kb], x * 64, j0, bh);
                 }
-                for (int t = 1; i < sched.nqt; i = sched.after(i, t), ++t) {
+                for (int t = t0; i < sched.nqt; i = sched.after(i, t), ++t) {
                     if (!load_step(i, t)) {
                         okp = false;
                         break;
@@ -399,8 +427,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             }
             // drain: the last load issued into each stage, and the last K/V
             for (int s = 0; s < Cfg::kStages; ++s)
-                if (issued_any[s]) mbar_wait(&st->st_full[s], issued_phase[s], wctx, 102);
-            if (gi > 0) mbar_wait(&st->kv_full, (gi - 1) & 1, wctx, 103);
+                if ((issued_any >> s) & 1u) mbar_wait(&st->st_full[s], (issued_phase >> s) & 1u, wctx, 102);
+            if (gi > 0) mbar_wait(&st->kv_full[(gi - 1) % Cfg::kKvBuffers], ((gi - 1) / Cfg::kKvBuffers) & 1, wctx, 103);
         }
     } else if (warp == 10 || warp == 11) {
         // the rest of the producer / MMA warpgroup. In the persistent grid
@@ -434,6 +462,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 }
             }
         }
+        if constexpr (Cfg::kTmaOut) {
+            if (warp == 11) {
+                // dK/dV stores: per item with work, once the compute warps have
+                // staged the tiles in the item's K/V buffer, two TMA stores
+                // (rows past N are outside the tensor and not written); the
+                // buffer is released to the producer when they have read it
+                if (lane == 0) {
+                    prefetch_tmap(&tm_dk);
+                    prefetch_tmap(&tm_dv);
+                }
+                int gi = 0;  // items with work, so far
+                for (int rr = 0; kPersist || rr == 0; ++rr) {
+                    if (!list_acquire(rr, true)) break;
+                    const int item = kPersist ? st->ring_item[rr & 1] : item0;
+                    if (item >= n_items) break;
+                    int n_active;
+                    const QSched<kMask> sched = item_sched(item, rr, n_active);
+                    if (n_active == 0) continue;
+                    const int kb = gi % Cfg::kKvBuffers;
+                    if (!mbar_wait_warp(&st->out_staged[kb], (gi / Cfg::kKvBuffers) & 1, wctx, 127)) break;
+                    if (lane == 0) {
+                        uint8_t* kv = sK + kb * Cfg::kKvBytes;
+                        tma_store_3d(&tm_dk, kv, 0, sched.jt * kTile, item % p.BH);
+                        tma_store_3d(&tm_dv, kv + Cfg::kTileBytes, 0, sched.jt * kTile, item % p.BH);
+                        bulk_commit_group();
+                        bulk_wait_read();
+                    }
+                    __syncwarp();
+                    mbar_arrive_warp(&st->kv_empty[kb]);
+                    ++gi;
+                }
+                // the stores have completed before the CTA ends
+                if (lane == 0) bulk_wait_all();
+            }
+        }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         regs_dec<Cfg::kIssueRegs>();
@@ -443,14 +506,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             constexpr uint32_t id_dv = idesc_f32acc(Elem16<T>::kFmt, kTile, D, 0, 1);      // dV (A tmem), dK (A K-major)
             constexpr uint32_t id_dqt_h = idesc_f32acc(Elem16<T>::kFmt, kTile, 64, 1, 1);   // dQ^T_h (A, B MN-major, N = 64)
             constexpr uint32_t id_dq = idesc_f32acc(Elem16<T>::kFmt, kTile, D, 1, 1);       // dQ (A, B MN-major)
-            const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
-            // descriptors built once, advanced by constants per MMA
-            const uint64_t kd_k = smem_desc_sw128(k_base, 16, 1024);         // K, K-major
-            const uint64_t vd_k = smem_desc_sw128(v_base, 16, 1024);         // V, K-major
+            const uint32_t ds_base = smem_u32(sDS);
+            // descriptors built once (K and V per item, from the item's
+            // buffer), advanced by constants per MMA
             const uint64_t dsd_k = smem_desc_sw128(ds_base, 16, 1024);       // dS^T, K-major
             const uint64_t dsd_mn = smem_desc_sw128(ds_base, kTile * 128, 1024);  // dS^T, MN-major
-            const uint64_t kd_mn = smem_desc_sw128(k_base, Cfg::kBoxBytes, 1024);  // K, MN-major (N = d)
-            const uint64_t kd_mn2 = smem_desc_sw128(k_base, kTile * 128, 1024);    // K, MN-major (M = d)
             bool ok = true;
             int gs = 0, gi = 0;  // steps and items with work, so far
             for (int rr = 0; ok && (kPersist || rr == 0); ++rr) {
@@ -460,8 +520,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             int n_active;
             (void)item_sched(item, rr, n_active);
             if (n_active == 0) continue;
-            if (!mbar_wait_warp(&st->kv_full, gi & 1, wctx, 110)) break;
+            const int kb = gi % Cfg::kKvBuffers;
+            if (!mbar_wait_warp(&st->kv_full[kb], (gi / Cfg::kKvBuffers) & 1, wctx, 110)) break;
             tc_fence_after();
+            const uint32_t k_base = smem_u32(sK + kb * Cfg::kKvBytes), v_base = k_base + Cfg::kTileBytes;
+            const uint64_t kd_k = smem_desc_sw128(k_base, 16, 1024);               // K, K-major
+            const uint64_t vd_k = smem_desc_sw128(v_base, 16, 1024);               // V, K-major
+            const uint64_t kd_mn = smem_desc_sw128(k_base, Cfg::kBoxBytes, 1024);  // K, MN-major (N = d)
+            const uint64_t kd_mn2 = smem_desc_sw128(k_base, kTile * 128, 1024);    // K, MN-major (M = d)
             if constexpr (D == 64) {
             // Software-pipelined order: the next step's S^T, dP^T (over all
             // 128 queries, N = 128) are issued as soon as the compute warps
@@ -643,7 +709,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             }
             // the item's K_j, V_j are read by every MMA issued so far; dK, dV
             // are complete when these arrive
-            mma_commit_warp(&st->kv_empty);
+            mma_commit_warp(&st->kv_empty[kb]);
             mma_commit_warp(&st->acc_done);
             gs += n_active;
             ++gi;
@@ -938,8 +1004,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 }
             }
             if constexpr (kLoadBoth) {
-                // P^T (own columns: query column c in packed column c / 2)
-                // once the previous step's dV product has read it
+                // dS^T first (its buffer is free since S^T of this step
+                // completed), then P^T (own columns: query column c in packed
+                // column c / 2) once the previous step's dV product has read it
+                uint8_t* row = sDS + (g & (Cfg::kDsBuffers - 1)) * Cfg::kDsBytes + half * (kTile * 128) + r * 128;
+#pragma unroll
+                for (int chunk = 0; chunk < 8; ++chunk) {
+                    const uint32_t* d4 = &dr2[chunk >> 2][4 * (chunk & 3)];
+                    *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = make_uint4(d4[0], d4[1], d4[2], d4[3]);
+                }
                 if (g > 0) {
                     if (!mbar_wait_warp(&st->p_free, (g - 1) & 1, wctx, 124)) {
                         ok = false;
@@ -951,12 +1024,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 for (int ch = 0; ch < 2; ++ch)
                     tmem_st16(tmem + lane_base + Cfg::kColP + half * 32 + ch * 16,
                               *reinterpret_cast<const uint32_t(*)[16]>(&sr2[ch][0]));
-                uint8_t* row = sDS + (g & (Cfg::kDsBuffers - 1)) * Cfg::kDsBytes + half * (kTile * 128) + r * 128;
-#pragma unroll
-                for (int chunk = 0; chunk < 8; ++chunk) {
-                    const uint32_t* d4 = &dr2[chunk >> 2][4 * (chunk & 3)];
-                    *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = make_uint4(d4[0], d4[1], d4[2], d4[3]);
-                }
             }
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -986,7 +1053,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             for (int c = 0; c < D / 64; ++c) reg_fence(ar[which][c]);
         tc_fence_before();
         mbar_arrive_warp(&st->acc_free);
-        if (jrow < p.N) {
+        if constexpr (Cfg::kTmaOut) {
+            // dK (scaled) and dV as two 128 x 64 tiles, 128-byte swizzled, over
+            // the item's K_j and V_j (every product of the item has completed:
+            // acc_done); warp 11 stores them
+            uint8_t* tile = sK + (gi % Cfg::kKvBuffers) * Cfg::kKvBytes;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const float mul = which ? 1.f : p.scale;
+                uint8_t* row = tile + which * Cfg::kTileBytes + r * 128;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint32_t* a = &ar[which][0][8 * v];
+                    uint4 w4;
+                    w4.x = Elem16<T>::pack2(__uint_as_float(a[0]) * mul, __uint_as_float(a[1]) * mul);
+                    w4.y = Elem16<T>::pack2(__uint_as_float(a[2]) * mul, __uint_as_float(a[3]) * mul);
+                    w4.z = Elem16<T>::pack2(__uint_as_float(a[4]) * mul, __uint_as_float(a[5]) * mul);
+                    w4.w = Elem16<T>::pack2(__uint_as_float(a[6]) * mul, __uint_as_float(a[7]) * mul);
+                    const int chunk = half * 4 + v;  // 16-byte chunk of the 128-byte row
+                    *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = w4;
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive_warp(&st->out_staged[gi % Cfg::kKvBuffers]);
+        } else if (jrow < p.N) {
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 T* out = static_cast<T*>(which ? p.dv : p.dk) + ((size_t)bh * p.N) * D;
@@ -1097,10 +1187,11 @@ int launch_bwd_tc_d(const Problem& pr) {
     using Cfg = BwdCfg<D>;
     constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
     const int BH = pr.B * pr.H;
-    CUtensorMap tq, tk, tv, tdo, tdq;
+    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
     if (!make_tmap16(&tq, pr.q, BH, pr.N, D, kTile, tt) || !make_tmap16(&tk, pr.k, BH, pr.N, D, kTile, tt) ||
         !make_tmap16(&tv, pr.v, BH, pr.N, D, kTile, tt) || !make_tmap16(&tdo, pr.dO, BH, pr.N, D, kTile, tt) ||
-        !make_tmap_f32_acc(&tdq, pr.dq_acc, BH, pr.N, D))
+        !make_tmap_f32_acc(&tdq, pr.dq_acc, BH, pr.N, D) || !make_tmap16(&tdk, pr.dk, BH, pr.N, D, kTile, tt) ||
+        !make_tmap16(&tdv, pr.dv, BH, pr.N, D, kTile, tt))
         return FA_ERR_CUDA;
     const size_t rows = (size_t)BH * pr.N;
     const int nqt = (pr.N + kTile - 1) / kTile;
@@ -1189,7 +1280,7 @@ int launch_bwd_tc_d(const Problem& pr) {
     cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::smem(pr.block_mask != nullptr, pr.block_mask != nullptr && persist);
     record_main_start(pr.stream);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, tdq, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, tdq, tdk, tdv, p);
     record_main_stop(pr.stream);
     note_launches(1);
     if (e != cudaSuccess) {

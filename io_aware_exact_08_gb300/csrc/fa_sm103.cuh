@@ -170,6 +170,16 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const 
         : "memory");
 }
 
+// Store of a shared-memory box into global memory by the TMA engine (rows or
+// columns outside the tensor are not written); bulk-group completion as for
+// tma_reduce_add_3d.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
