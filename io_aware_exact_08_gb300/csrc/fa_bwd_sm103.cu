@@ -209,10 +209,6 @@ struct QSched {
     }
 };
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // *dst += a (fp32, no return value, relaxed, L2).
 __device__ __forceinline__ void red_add_f32(float* dst, float a) {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(a) : "memory");

@@ -99,6 +99,7 @@ struct Shared1t {
     uint64_t mx_ready[2];  // both column halves' maxima of tile u (buffer u & 1) written
     uint64_t l_ready;      // both halves' row-sum shares written
     uint64_t o_final;
+    uint64_t o_staged;  // every softmax warp has written its rows of O over Q
     uint64_t teardown;
     uint32_t tmem_base;
     int abort_flag;
@@ -109,7 +110,8 @@ static_assert(sizeof(Shared1t) <= 256, "barrier block");
 template <typename T, bool kSplit, bool kDrop>
 __global__ void __launch_bounds__(Layout1t<kDrop>::kThreads, 2)
     fwd_1t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const Fwd1tParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const Fwd1tParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
@@ -150,6 +152,7 @@ __global__ void __launch_bounds__(Layout1t<kDrop>::kThreads, 2)
         mbar_init(&st->mx_ready[1], Lay::kSoftWarps);
         mbar_init(&st->l_ready, Lay::kSoftWarps);
         mbar_init(&st->o_final, 1);
+        mbar_init(&st->o_staged, Lay::kSoftWarps);
         mbar_init(&st->teardown, 1);
         st->abort_flag = 0;
         fence_mbar_init();
@@ -450,6 +453,11 @@ __global__ void __launch_bounds__(Layout1t<kDrop>::kThreads, 2)
             }
             if (ready && mbar_wait_warp(&st->o_final, 0, wctx, 381)) {
                 tc_fence_after();
+                // O = acc / l in 16 bits, written over Q (every product has
+                // completed, the last S before the last P V) as one 128 x 64
+                // tile, 128-byte swizzled (16-byte chunk c of row r at chunk
+                // position c ^ (r & 7)), then stored by the TMA engine: rows
+                // past N are outside the tensor and not written
                 const float inv = (lt > 0.f) ? p.out_scale / lt : 0.f;
 #pragma unroll
                 for (int c = 0; c < kOCols / 32; ++c) {
@@ -457,20 +465,25 @@ __global__ void __launch_bounds__(Layout1t<kDrop>::kThreads, 2)
                     tmem_ld32(obase + c * 32, orr);
                     tmem_ld_wait();
                     reg_fence(orr);
-                    if (i < p.N) {
-                        uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * kD + kOCols * half + c * 32);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 w4;
-                            w4.x = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
-                            w4.y = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
-                            w4.z = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
-                            w4.w = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
-                            dst[v] = w4;
-                        }
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w4;
+                        w4.x = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
+                        w4.y = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
+                        w4.z = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
+                        w4.w = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
+                        const int chunk = (kOCols * half + c * 32) / 8 + v;
+                        *reinterpret_cast<uint4*>(sQ + r * 128 + ((chunk ^ (r & 7)) << 4)) = w4;
                     }
                 }
                 if (half == 0 && i < p.N) p.lse[(size_t)bh * p.N + i] = (lt > 0.f) ? (m + __log2f(lt)) * kLn2 : -INFINITY;
+                fence_proxy_async_smem();
+                mbar_arrive_warp(&st->o_staged);
+                if (warp == 0 && mbar_wait_warp(&st->o_staged, 0, wctx, 386) && lane == 0) {
+                    tma_store_3d(&tm_o, sQ, 0, qt * kBlockM, bh);
+                    bulk_commit_group();
+                    bulk_wait_all();  // complete before the CTA ends
+                }
             }
         } else if (n == 0 && i < p.N) {
             const uint4 z = make_uint4(0, 0, 0, 0);
@@ -490,10 +503,10 @@ __global__ void __launch_bounds__(Layout1t<kDrop>::kThreads, 2)
 template <typename T, bool kSplit, bool kDrop>
 int launch_1t(const Problem& pr) {
     constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const int BH = pr.B * pr.H;
     if (!make_tmap16(&tq, pr.q, BH, pr.N, kD, kBlockM, tt) || !make_tmap16(&tk, pr.k, BH, pr.N, kD, kBlockN, tt) ||
-        !make_tmap16(&tv, pr.v, BH, pr.N, kD, kBlockN, tt))
+        !make_tmap16(&tv, pr.v, BH, pr.N, kD, kBlockN, tt) || !make_tmap16(&to, pr.o, BH, pr.N, kD, kBlockM, tt))
         return FA_ERR_CUDA;
     Fwd1tParams p{};
     p.lse = pr.lse;
@@ -538,7 +551,7 @@ int launch_1t(const Problem& pr) {
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     record_main_start(pr.stream);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, p);
     record_main_stop(pr.stream);
     note_launches(1);
     if (e != cudaSuccess) {

@@ -170,6 +170,12 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const 
         : "memory");
 }
 
+// Makes this thread's shared-memory writes visible to the async proxy (the
+// TMA engine) before a bulk copy reads them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Store of a shared-memory box into global memory by the TMA engine (rows or
 // columns outside the tensor are not written); bulk-group completion as for
 // tma_reduce_add_3d.
