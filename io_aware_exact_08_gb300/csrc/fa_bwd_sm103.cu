@@ -847,23 +847,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const float* colt = reinterpret_cast<const float*>(sStages + sidx * Cfg::kStageBytes + 2 * Cfg::kTileBytes);
             // dropout keep bits of this row's 64 query columns, drawn before
             // S^T arrives (bit x of keep_w[ch] is query column
-            // 64 half + 32 ch + x): lane (4a + w) draws the 4 keep bits of
-            // keys 4a..4a+3 for one query and the group exchanges them
+            // 64 half + 32 ch + x). Lane (4a + w) draws, for the 8 queries
+            // 4g + w of each 32-column chunk, the 4 keep bits of keys
+            // 4a..4a+3 and packs them into one word (bits 4g..4g+3); the key
+            // of lane 4a + w for query 4g + q is then bit 4g + w of lane
+            // 4a + q's word, so one shuffle per group mate moves all of them
             uint32_t keep_w[2] = {0xffffffffu, 0xffffffffu};
             if (p.dropout) {
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
                     const int cb = half * 64 + ch * 32;
-                    uint32_t keep = 0;
+                    uint32_t word = 0;
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
                         const int qi = i0 + cb + 4 * g + (lane & 3);
-                        const uint32_t bits = keep_bits4(p.seed, p.drop_thr, b, h, qi, jrow >> 2);
+                        word |= keep_bits4(p.seed, p.drop_thr, b, h, qi, jrow >> 2) << (4 * g);
+                    }
+                    uint32_t keep = 0;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint32_t v = __shfl_sync(0xffffffffu, bits, (lane & ~3) | q);
-                            keep |= ((v >> (lane & 3)) & 1u) << (4 * g + q);
-                        }
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t v = __shfl_sync(0xffffffffu, word, (lane & ~3) | q);
+                        keep |= ((v >> (lane & 3)) & 0x11111111u) << q;
                     }
                     keep_w[ch] = keep;
                 }
