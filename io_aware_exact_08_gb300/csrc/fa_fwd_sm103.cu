@@ -103,16 +103,19 @@ struct SharedPP {
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t o_final[2];
+    uint64_t o_staged[2];  // every softmax warp of tile t has written its rows of O over Q_t
     uint64_t teardown;
     uint32_t tmem_base;
     int abort_flag;
     int n_list[2];  // kSplit: visible key tiles of each query tile
 };
+static_assert(sizeof(SharedPP) <= 256, "barrier block");
 
 template <typename T, int D, bool kSplit, bool kPartial>
 __global__ void __launch_bounds__(kThreadsPP, 1)
     fwd_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdParams p) {
     using Cfg = FwdPPCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -183,6 +186,7 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             mbar_init(&st->s_full[t], 1);
             mbar_init(&st->p_full[t], kSoftmaxThreads / 32);
             mbar_init(&st->o_final[t], 1);
+            mbar_init(&st->o_staged[t], kSoftmaxThreads / 32);  // the 4 softmax warps of tile t
         }
         mbar_init(&st->teardown, 1);
         st->abort_flag = 0;
@@ -573,21 +577,30 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
             if (mbar_wait_warp(&st->o_final[t], 0, wctx, 81)) {
                 tc_fence_after();
                 const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+                // 16-bit O: written over Q_t (every product of tile t has
+                // completed, its last S before its last P V) as D / 64 boxes of
+                // 128 rows x 64 columns, 128-byte swizzled (16-byte chunk c of
+                // row r at chunk position c ^ (r & 7)), then stored by the TMA
+                // engine: rows past N are outside the tensor and not written.
+                // Split-KV partials (fp32) are stored row by row.
+                uint8_t* qt_tile = sQ + t * Cfg::kQBytes;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t orr[32];
                     tmem_ld32(obase + c * 32, orr);
                     tmem_ld_wait();
                     reg_fence(orr);
-                    if (kPartial && i < p.N) {
-                        float4* dst = reinterpret_cast<float4*>(p.o_part + (prow + i) * D + c * 32);
+                    if constexpr (kPartial) {
+                        if (i < p.N) {
+                            float4* dst = reinterpret_cast<float4*>(p.o_part + (prow + i) * D + c * 32);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_float4(__uint_as_float(orr[4 * v]) * inv, __uint_as_float(orr[4 * v + 1]) * inv,
-                                                 __uint_as_float(orr[4 * v + 2]) * inv,
-                                                 __uint_as_float(orr[4 * v + 3]) * inv);
-                    } else if (i < p.N) {
-                        uint4* dst = reinterpret_cast<uint4*>(O + (size_t)i * D + c * 32);
+                            for (int v = 0; v < 8; ++v)
+                                dst[v] = make_float4(__uint_as_float(orr[4 * v]) * inv, __uint_as_float(orr[4 * v + 1]) * inv,
+                                                     __uint_as_float(orr[4 * v + 2]) * inv,
+                                                     __uint_as_float(orr[4 * v + 3]) * inv);
+                        }
+                    } else {
+                        uint8_t* row = qt_tile + (c >> 1) * Cfg::kBoxBytes + r * 128;
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint4 w4;
@@ -595,7 +608,8 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                             w4.y = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
                             w4.z = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
                             w4.w = Elem16<T>::pack2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
-                            dst[v] = w4;
+                            const int chunk = (c & 1) * 4 + v;
+                            *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = w4;
                         }
                     }
                 }
@@ -603,6 +617,17 @@ __global__ void __launch_bounds__(kThreadsPP, 1)
                     const float lse_i = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
                     if (kPartial) p.lse_part[prow + i] = lse_i;
                     else p.lse[(size_t)bh * p.N + i] = lse_i;
+                }
+                if constexpr (!kPartial) {
+                    fence_proxy_async_smem();
+                    mbar_arrive_warp(&st->o_staged[t]);
+                    if ((warp & 3) == 0 && mbar_wait_warp(&st->o_staged[t], 0, wctx, 86) && lane == 0) {
+#pragma unroll
+                        for (int x = 0; x < Cfg::kBoxes; ++x)
+                            tma_store_3d(&tm_o, qt_tile + x * Cfg::kBoxBytes, x * 64, (2 * pair + t) * kBlockM, bh);
+                        bulk_commit_group();
+                        bulk_wait_all();  // complete before the CTA ends
+                    }
                 }
             }
         } else if (n == 0 && i < p.N) {
@@ -1152,11 +1177,14 @@ template <typename T, int D, bool kSplit, bool kPartial>
 int launch_fwd_tc_d(const Problem& pr) {
     constexpr int kSmem = FwdPPCfg<D>::kSmem;
     constexpr CUtensorMapDataType tt = Elem16<T>::kTmaType;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const int BH = pr.B * pr.H;
     if (!make_tmap16(&tq, pr.q, BH, pr.N, D, kBlockM, tt) || !make_tmap16(&tk, pr.k, BH, pr.N, D, kBlockN, tt) ||
         !make_tmap16(&tv, pr.v, BH, pr.N, D, kBlockN, tt))
         return FA_ERR_CUDA;
+    // O's tensor map (split-KV partials are fp32 and stored row by row)
+    if (kPartial) to = tq;
+    else if (!make_tmap16(&to, pr.o, BH, pr.N, D, kBlockM, tt)) return FA_ERR_CUDA;
     const FwdParams p = fwd_params(pr);
     auto kernel = fwd_pp_kernel<T, D, kSplit, kPartial>;
     static bool attr_set = false;
@@ -1187,7 +1215,7 @@ int launch_fwd_tc_d(const Problem& pr) {
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     record_main_start(pr.stream);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, p);
     record_main_stop(pr.stream);
     note_launches(1);
     if (e != cudaSuccess) {
