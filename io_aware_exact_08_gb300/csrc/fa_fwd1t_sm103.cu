@@ -96,7 +96,7 @@ struct Shared1t {
     uint64_t s_free;   // the softmax has read S(u): S(u+1) may be written
     uint64_t p_full;   // P(u) in TMEM
     uint64_t pv_done;  // P(u) V has completed: O may be rescaled, P overwritten
-    uint64_t mx_ready[2];  // both column halves' maxima of tile u (buffer u & 1) written
+    uint64_t mx_ready[2][4];  // both column halves' maxima of tile u (buffer u & 1), rows of quarter q, written
     uint64_t l_ready;      // both halves' row-sum shares written
     uint64_t o_final;
     uint64_t o_staged;  // every softmax warp has written its rows of O over Q
@@ -148,8 +148,10 @@ __global__ void __launch_bounds__(Layout1t<kDrop>::kThreads, 2)
         mbar_init(&st->s_free, Lay::kSoftWarps);
         mbar_init(&st->p_full, Lay::kSoftWarps);
         mbar_init(&st->pv_done, 1);
-        mbar_init(&st->mx_ready[0], Lay::kSoftWarps);
-        mbar_init(&st->mx_ready[1], Lay::kSoftWarps);
+        for (int q = 0; q < 4; ++q) {  // the two warps (one per column half) of lane quarter q
+            mbar_init(&st->mx_ready[0][q], Lay::kHalves);
+            mbar_init(&st->mx_ready[1][q], Lay::kHalves);
+        }
         mbar_init(&st->l_ready, Lay::kSoftWarps);
         mbar_init(&st->o_final, 1);
         mbar_init(&st->o_staged, Lay::kSoftWarps);
@@ -333,13 +335,15 @@ __global__ void __launch_bounds__(Layout1t<kDrop>::kThreads, 2)
             pm[6] = fmaxf(pm[6], pm[7]);
             pm[0] = fmax3(pm[0], pm[3], pm[6]);
             if constexpr (Lay::kHalves == 2) {
-                // the row maximum of the tile from both halves (buffer u & 1:
-                // a half writes it again at u + 2 only after both halves have
-                // passed the exchange of u + 1, so after this one's reads)
+                // the row maximum of the tile from both halves, exchanged
+                // between the two warps that share these 32 rows (a barrier
+                // per lane quarter; buffer u & 1: a warp writes it again at
+                // u + 2 only after both have passed the exchange of u + 1, so
+                // after this one's reads)
                 float* mx = sMax + (u & 1) * 256;
                 mx[half * 128 + r] = pm[0];
-                mbar_arrive_warp(&st->mx_ready[u & 1]);
-                if (!mbar_wait_warp(&st->mx_ready[u & 1], (u >> 1) & 1, wctx, 384)) {
+                mbar_arrive_warp(&st->mx_ready[u & 1][quarter]);
+                if (!mbar_wait_warp(&st->mx_ready[u & 1][quarter], (u >> 1) & 1, wctx, 384)) {
                     ok = false;
                     break;
                 }
