@@ -11,8 +11,8 @@
  *
  * Conventions shared by every entry point:
  *  - Tensors are contiguous [B, H, N, d] row-major (d fastest), in device
- *    memory, 16-byte aligned. q, k, v, o, dO, dq, dk, dv all have that shape
- *    and the element type `dtype`. lse is fp32 [B, H, N] in natural log:
+ *    memory (host memory for fa_fwd_bwd_host), 16-byte aligned. q, k, v, o,
+ *    dO, dq, dk, dv all have that shape and the element type `dtype`. lse is fp32 [B, H, N] in natural log:
  *    lse = m + ln(l), which carries the same information as the pair (l, m)
  *    the pages keep for the backward pass.
  *  - d must be 64, 128 or 256. B, H >= 1, N >= 0 (N == 0 is a no-op).
@@ -41,7 +41,8 @@
  *    fa_check_device_status. The library allocates no device memory per
  *    call; the only device memory it holds is static: a status word of two
  *    ints and the fixed FA_BWD_NOALLOC_SCRATCH_BYTES (32 MiB) array of
- *    fa_bwd_noalloc, present on every GPU that loads the library.
+ *    fa_bwd_noalloc, present on every GPU that loads the library
+ *    (fa_fwd_bwd_host also keeps two streams and a few events per device).
  *  - The device addresses of those two static objects are looked up once
  *    per device and cached for the life of the process, so resetting a
  *    device (cudaDeviceReset, or a reset of its primary context) while the
@@ -136,6 +137,66 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    int B, int H, int N, int d, float scale, int causal,
                    const uint8_t* block_mask, float dropout_p, uint64_t seed,
                    fa_dtype dtype, const int32_t* kv_len, void* stream);
+
+/*
+ * One training step on HOST tensors: o, lse = forward(q, k, v) and
+ * dq, dk, dv = backward(q, k, v, o, lse, dO), the same computation as fa_fwd
+ * followed by fa_bwd, for callers whose tensors are in host memory. The
+ * method itself starts from Q, K, V in HBM and ends with O in HBM (blog post
+ * "Flash Attention", section "Flash Attention"); this call adds the
+ * transfers and hides them behind the kernels. The heads are cut into
+ * chunks that pass through a ring of three device slots in the workspace:
+ * the copies of chunk c+1 in and chunk c-1 out run on two internal streams
+ * while chunk c computes on `stream`.
+ *   q, k, v, dO    inputs, host memory, [B, H, N, d] of `dtype`.
+ *   o, dq, dk, dv  outputs, host memory, [B, H, N, d] of `dtype`.
+ *   lse            output, host memory, fp32 [B, H, N].
+ *   block_mask, kv_len
+ *                  as in fa_fwd but in HOST memory (copied into the
+ *                  workspace), or NULL.
+ *   chunk_heads    heads per chunk; 0 picks it (at most 4 chunks, each of
+ *                  at least 256 128-row query tiles where the problem has
+ *                  that many). With key padding a chunk holds whole batches
+ *                  or lies within one. With dropout the step is one chunk:
+ *                  the keep bits are drawn from the absolute (b, h).
+ *   workspace      caller-owned device memory, 256-byte aligned, of at least
+ *                  fa_fwd_bwd_host_workspace_size bytes (about three chunks'
+ *                  tensors plus their backward workspace).
+ *   other arguments as in fa_fwd / fa_bwd.
+ * Asynchronous like a cudaMemcpyAsync: on return the work is queued and
+ * `stream` waits for all of it; the host buffers must stay valid and
+ * unchanged until the stream reaches that point. The copies overlap the
+ * kernels only for page-locked host memory (cudaHostAlloc,
+ * cudaHostRegister); with pageable memory the results are the same but
+ * the call returns only after its copies are done. The library creates two
+ * streams and a few events per device on the first call and keeps them
+ * until exit; calls on one device are serialised on the host while they
+ * queue their work.
+ * Returns the errors of fa_fwd and fa_bwd (FA_ERR_INVALID_ARG for a null
+ * host pointer or chunk_heads < 0; FA_ERR_WORKSPACE for a missing, small or
+ * misaligned workspace). An error from the kernels' entry points stops the
+ * call after the chunks already queued; `stream` still waits for them.
+ */
+int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO,
+                    void* o, float* lse, void* dq, void* dk, void* dv,
+                    int B, int H, int N, int d, float scale, int causal,
+                    const uint8_t* block_mask, float dropout_p, uint64_t seed,
+                    fa_dtype dtype, const int32_t* kv_len, int chunk_heads,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fa_fwd_bwd_host needs for these arguments (only
+ * whether block_mask and kv_len are NULL, and whether dropout_p > 0,
+ * matter); 0 for invalid sizes or N == 0. */
+size_t fa_fwd_bwd_host_workspace_size(int B, int H, int N, int d, fa_dtype dtype,
+                                      const uint8_t* block_mask, float dropout_p,
+                                      const int32_t* kv_len, int chunk_heads);
+
+/* Diagnostic: the chunks fa_fwd_bwd_host would use, in order. Writes up to
+ * max_chunks records of four ints (first head numbered b*H + h, the chunk's
+ * B, its H, its first batch) to desc (may be NULL) and returns the number
+ * of chunks, or FA_ERR_INVALID_ARG. */
+int fa_fwd_bwd_host_chunks(int B, int H, int N, const int32_t* kv_len, float dropout_p,
+                           int chunk_heads, int* desc, int max_chunks);
 
 /*
  * Split-KV forward: the same result as fa_fwd (O and LSE up to rounding),

@@ -3,13 +3,13 @@
 A thin ctypes layer over the C ABI in ``include/fa.h`` (``libfa_gb300.so``,
 built in-tree by ``build.py``). The functions ``fa_fwd``, ``fa_fwd_splitkv``,
 ``fa_fwd_splitkv_workspace_size``, ``fa_bwd``, ``fa_bwd_workspace_size``,
-``fa_dropout_mask``, ``fa_check_device_status``, ``fa_status_string`` and
-``fa_set_kernel_path`` take the same arguments as
-their C counterparts (device pointers as integers, sizes, a stream handle)
-and only marshal them. ``attention_fwd`` / ``attention_bwd`` and
-``FlashAttention`` add the tensor plumbing: PyTorch allocates the outputs
-and the workspace and supplies the current stream; every step of the
-computation runs in the library's CUDA kernels.
+``fa_dropout_mask``, ``fa_check_device_status``, ``fa_status_string``,
+``fa_set_kernel_path`` and ``fa_fwd_bwd_host`` take the same arguments as
+their C counterparts (pointers as integers, sizes, a stream handle) and only
+marshal them. ``attention_fwd`` / ``attention_bwd``, ``attention_fwd_bwd_host``
+(a step on host tensors) and ``FlashAttention`` add the tensor plumbing:
+PyTorch allocates the outputs and the workspace and supplies the current
+stream; every step of the computation runs in the library's CUDA kernels.
 
 There is no CPU fallback: if the library cannot be loaded, importing the
 binding's functions raises.
@@ -25,6 +25,7 @@ __all__ = [
     "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
     "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
     "fa_set_main_kernel_events", "fa_bwd_noalloc", "fa_fwd_fp8", "attention_fwd_fp8", "fa_ex2_probe", "FA_BWD_NOALLOC_SCRATCH_BYTES", "attention_fwd", "attention_bwd", "dropout_mask", "FlashAttention", "attention",
+    "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size", "fa_fwd_bwd_host_chunks", "attention_fwd_bwd_host",
 ]
 
 FA_BF16 = 0
@@ -39,7 +40,8 @@ _lock = threading.Lock()
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_mask",
             "fa_check_device_status", "fa_status_string", "fa_set_kernel_path", "fa_launch_count",
             "fa_bwd_noalloc", "fa_test_wait_timeout", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size",
-            "fa_set_main_kernel_events", "fa_fwd_fp8", "fa_ex2_probe")
+            "fa_set_main_kernel_events", "fa_fwd_fp8", "fa_ex2_probe", "fa_fwd_bwd_host",
+            "fa_fwd_bwd_host_workspace_size", "fa_fwd_bwd_host_chunks")
 
 # Size of the fixed device array fa_bwd_noalloc takes its workspace from.
 FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -90,6 +92,12 @@ def load_library(build_if_missing: bool = True):
         lib.fa_set_kernel_path.restype = I
         lib.fa_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, P]
         lib.fa_bwd_noalloc.restype = I
+        lib.fa_fwd_bwd_host.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, F, U64, I, P, I, P, SZ, P]
+        lib.fa_fwd_bwd_host.restype = I
+        lib.fa_fwd_bwd_host_workspace_size.argtypes = [I, I, I, I, I, P, F, P, I]
+        lib.fa_fwd_bwd_host_workspace_size.restype = SZ
+        lib.fa_fwd_bwd_host_chunks.argtypes = [I, I, I, P, F, I, P, I]
+        lib.fa_fwd_bwd_host_chunks.restype = I
         lib.fa_test_wait_timeout.argtypes = [U64, P]
         lib.fa_test_wait_timeout.restype = I
         lib.fa_ex2_probe.argtypes = [P, I, I, P]
@@ -148,6 +156,32 @@ def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, b
 
 def fa_bwd_workspace_size(B, H, N, d):
     return load_library().fa_bwd_workspace_size(B, H, N, d)
+
+
+def fa_fwd_bwd_host(q, k, v, dO, o, lse, dq, dk, dv, B, H, N, d, scale, causal, block_mask, dropout_p, seed,
+                    dtype, kv_len, chunk_heads, workspace, workspace_bytes, stream):
+    """Forward and backward on HOST buffers (addresses as integers), the
+    copies overlapped with the kernels chunk by chunk; see include/fa.h."""
+    return load_library().fa_fwd_bwd_host(q, k, v, dO, o, lse, dq, dk, dv, B, H, N, d, scale, int(causal),
+                                          block_mask, dropout_p, seed & 0xFFFFFFFFFFFFFFFF, dtype, kv_len,
+                                          int(chunk_heads), workspace, workspace_bytes, stream)
+
+
+def fa_fwd_bwd_host_workspace_size(B, H, N, d, dtype, block_mask, dropout_p, kv_len, chunk_heads):
+    return load_library().fa_fwd_bwd_host_workspace_size(B, H, N, d, dtype, block_mask, float(dropout_p), kv_len,
+                                                         int(chunk_heads))
+
+
+def fa_fwd_bwd_host_chunks(B, H, N, kv_len, dropout_p, chunk_heads):
+    """The chunks fa_fwd_bwd_host uses: a list of (first head, B, H, first
+    batch). kv_len only matters through being None or not."""
+    lib = load_library()
+    n = lib.fa_fwd_bwd_host_chunks(B, H, N, kv_len, float(dropout_p), int(chunk_heads), None, 0)
+    if n < 0:
+        raise FaError(n, "fa_fwd_bwd_host_chunks")
+    buf = (ctypes.c_int * (4 * max(n, 1)))()
+    lib.fa_fwd_bwd_host_chunks(B, H, N, kv_len, float(dropout_p), int(chunk_heads), buf, n)
+    return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
 
 
 def fa_dropout_mask(keep, B, H, N, p, seed, stream):
@@ -307,6 +341,48 @@ def attention_bwd(q, k, v, o, lse, do, scale=None, causal=False, block_mask=None
     if rc != 0:
         raise FaError(rc, "fa_bwd")
     return dq, dk, dv
+
+
+def attention_fwd_bwd_host(q, k, v, do, scale=None, causal=False, block_mask=None, dropout_p=0.0, seed=0,
+                           kv_len=None, chunk_heads=0, out=None, workspace=None, device=None, stream=None):
+    """O, LSE, dQ, dK, dV for [B,H,N,d] tensors in HOST memory (fa_fwd_bwd_host).
+
+    q, k, v, do: contiguous CPU tensors (page-locked, e.g. .pin_memory(),
+    for the copies to overlap the kernels); block_mask (uint8) and kv_len
+    (int32) are CPU tensors too. out: optional (o, lse, dq, dk, dv) CPU
+    tensors to write; by default they are allocated page-locked. The
+    workspace is device memory on `device` (default: the current CUDA
+    device), allocated here unless given. Returns (o, lse, dq, dk, dv); they
+    are ready once `stream` (default: the current stream) has caught up."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor [B,H,N,d]")
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype")
+    for name, t in (("block_mask", block_mask), ("kv_len", kv_len)):
+        if t is not None and (not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    B, H, N, d = q.shape
+    dt = _dtype_code(q)
+    scale = (1.0 / d ** 0.5) if scale is None else float(scale)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if out is None:
+        pin = q.is_pinned()
+        mk = lambda shape, dtype: torch.empty(shape, dtype=dtype, pin_memory=pin)
+        out = (mk(q.shape, q.dtype), mk((B, H, N), torch.float32), mk(q.shape, q.dtype), mk(q.shape, q.dtype),
+               mk(q.shape, q.dtype))
+    o, l, dq, dk, dv = out
+    need = fa_fwd_bwd_host_workspace_size(B, H, N, d, dt, _ptr(block_mask), dropout_p, _ptr(kv_len),
+                                          chunk_heads)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev) if workspace is None else workspace
+    with torch.cuda.device(dev):
+        rc = fa_fwd_bwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(o), _ptr(l), _ptr(dq), _ptr(dk), _ptr(dv),
+                             B, H, N, d, scale, causal, _ptr(block_mask), float(dropout_p), int(seed), dt,
+                             _ptr(kv_len), int(chunk_heads), _ptr(ws), ws.numel(), _stream(stream))
+    if rc != 0:
+        raise FaError(rc, "fa_fwd_bwd_host")
+    return o, l, dq, dk, dv
 
 
 def dropout_mask(B, H, N, p, seed, device="cuda", stream=None):
