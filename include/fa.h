@@ -155,8 +155,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *                  as in fa_fwd but in HOST memory (copied into the
  *                  workspace), or NULL.
  *   chunk_heads    heads per chunk; 0 picks it (at most 4 chunks, each of
- *                  at least 256 128-row query tiles where the problem has
- *                  that many). With key padding a chunk holds whole batches
+ *                  at least 8 heads' worth of 128-row query tiles, clamped
+ *                  to 256..512 tiles, where the problem has that many). With key padding a chunk holds whole batches
  *                  or lies within one. With dropout the step is one chunk:
  *                  the keep bits are drawn from the absolute (b, h).
  *   workspace      caller-owned device memory, 256-byte aligned, of at least

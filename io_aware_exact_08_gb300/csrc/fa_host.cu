@@ -48,17 +48,26 @@
 namespace {
 
 constexpr int kSlots = 3;          // device slots in the ring
-// Chunks per step when the caller leaves the size open: at most four, each of
-// at least 256 query tiles of 128 rows where the step has that many. The
-// host link of a GB300 moves ~200 GB/s each way (~340 GB/s both ways at
-// once), so at N = 8K the copies of a step take about as long as its
-// kernels: four chunks keep the first chunk's copy-in and the last chunk's
-// copy-out short, and each chunk still fills the GPU. Measured (B=2 H=16
-// N=8K d=128 causal): 3 chunks 2.46 ms, 4 chunks 2.34, 6 chunks 2.72,
-// 8 chunks 3.15; at B=8 H=12 N=1K d=64, 3 chunks 0.459 ms, 6 chunks 0.482,
-// 12 chunks 0.574, one chunk 0.538.
+// Chunks per step when the caller leaves the size open: at most four, each
+// of at least 8 heads' worth of 128-row query tiles, and no fewer than 256
+// or more than 512 tiles, where the step has that many.
+//  - The host link of a GB300 moves ~200 GB/s each way (~340 GB/s both ways
+//    at once), so at N = 8K the copies of a step take about as long as its
+//    kernels. Four chunks keep the first chunk's copy-in and the last
+//    chunk's copy-out short while each chunk still fills the GPU.
+//  - Long sequences need more tiles per chunk: a key tile of the causal
+//    backward meets every query tile of its head, so a chunk of few long
+//    heads lasts as long as that one item.
+// Measured (one step on host buffers):
+//  - B=2 H=16 N=8K d=128 causal: 3 chunks 2.46 ms, 4 chunks 2.34, 6 chunks
+//    2.72, 8 chunks 3.15;
+//  - B=8 H=12 N=1K d=64 causal: 3 chunks 0.459 ms, 6 chunks 0.482,
+//    12 chunks 0.574, one chunk 0.538;
+//  - B=1 H=4 N=16K d=128 causal: one chunk 1.375 ms, 2 chunks 1.633;
+//  - B=1 H=16 N=16K d=128 causal: 4 chunks 3.905 ms, 2 chunks 4.236;
+//  - B=2 H=8 N=4K d=256 causal: 2 chunks 1.396 ms, one chunk 1.869.
 constexpr int kMaxChunks = 4;
-constexpr long long kMinChunkTiles = 256;
+constexpr long long kMinChunkTiles = 256, kMaxChunkTiles = 512, kMinChunkHeads = 8;
 constexpr int kMaxDevices = 64;
 
 struct Chunk {
@@ -92,7 +101,8 @@ std::vector<Chunk> plan_chunks(int B, int H, int N, bool has_kv_len, bool dropou
         G = std::min<long long>(chunk_heads, F);
     } else {
         const long long nt = std::max(1, (N + 127) / 128);
-        const long long gmin = (kMinChunkTiles + nt - 1) / nt;
+        const long long tiles = std::min(kMaxChunkTiles, std::max(kMinChunkTiles, kMinChunkHeads * nt));
+        const long long gmin = (tiles + nt - 1) / nt;
         const long long n = std::max(1LL, std::min<long long>(kMaxChunks, F / gmin));
         G = (F + n - 1) / n;
     }

@@ -61,26 +61,31 @@ def test_chunks_partition_the_heads(B, H, N, kv_len, dropout, chunk_heads):
 @pytest.mark.parametrize("B,H,N", [(2, 16, 8192), (8, 12, 1024), (32, 16, 512), (1, 8, 16384), (1, 2, 256),
                                    (4, 64, 2048)])
 def test_automatic_chunks(B, H, N):
-    """At most four chunks; every chunk holds at least 256 query tiles
-    unless the whole step has fewer; a step too small to split stays one
-    chunk."""
+    """At most four chunks; every chunk holds at least min(512, max(256,
+    8 heads)) query tiles unless the whole step has fewer; a step too small
+    to split stays one chunk."""
     nt = (N + 127) // 128
+    least = min(512, max(256, 8 * nt))
     chunks = fa.fa_fwd_bwd_host_chunks(B, H, N, None, 0.0, 0)
     assert 1 <= len(chunks) <= 4
-    if B * H * nt < 2 * 256:
+    if B * H * nt < 2 * least:
         assert len(chunks) == 1
     for _, cb, ch, _ in chunks:
-        assert cb * ch * nt >= min(256, B * H * nt)
+        assert cb * ch * nt >= min(least, B * H * nt)
     sizes = [cb * ch for _, cb, ch, _ in chunks]
     assert max(sizes) - min(sizes) <= 1  # balanced
 
 
 def test_example_plans():
-    # B=2 H=16 N=8K: 64 tiles per head, 4 heads for 256 tiles, at most 4 chunks
+    # B=2 H=16 N=8K: 64 tiles per head, 8 heads (512 tiles) per chunk
     assert fa.fa_fwd_bwd_host_chunks(2, 16, 8192, None, 0.0, 0) == [(0, 1, 8, 0), (8, 1, 8, 0), (16, 1, 8, 0),
                                                                    (24, 1, 8, 0)]
     # B=8 H=12 N=1K: 8 tiles per head, 32 heads for 256 tiles, 3 chunks
     assert fa.fa_fwd_bwd_host_chunks(8, 12, 1024, None, 0.0, 0) == [(0, 1, 32, 0), (32, 1, 32, 0), (64, 1, 32, 0)]
+    # B=1 H=4 N=16K: 128 tiles per head, 4 heads for 512 tiles, one chunk
+    assert fa.fa_fwd_bwd_host_chunks(1, 4, 16384, None, 0.0, 0) == [(0, 1, 4, 0)]
+    # B=2 H=8 N=4K: 32 tiles per head, 8 heads (256 tiles) per chunk
+    assert fa.fa_fwd_bwd_host_chunks(2, 8, 4096, None, 0.0, 0) == [(0, 1, 8, 0), (8, 1, 8, 0)]
     # key padding, 2 heads per chunk of 3-head batches: pieces inside each batch
     assert fa.fa_fwd_bwd_host_chunks(2, 3, 300, FAKE, 0.0, 2) == [(0, 1, 2, 0), (2, 1, 1, 0), (3, 1, 2, 1),
                                                                   (5, 1, 1, 1)]
