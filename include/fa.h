@@ -163,6 +163,7 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *                  fa_fwd_bwd_host_workspace_size bytes (about three chunks'
  *                  tensors plus their backward workspace).
  *   other arguments as in fa_fwd / fa_bwd.
+ * Runs on the current device; `stream` must belong to it.
  * Asynchronous like a cudaMemcpyAsync: on return the work is queued and
  * `stream` waits for all of it; the host buffers must stay valid and
  * unchanged until the stream reaches that point. The copies overlap the

@@ -18,8 +18,9 @@
 //  - Events order each slot's reuse: a chunk's inputs are overwritten only
 //    after the backward that read them has finished, and its outputs only
 //    after they have been copied out.
-//  - The call ends by making the caller's stream wait for both copy streams,
-//    so work queued on it afterwards sees every result in host memory.
+//  - The call ends by making the caller's stream wait for the internal
+//    streams, so work queued on it afterwards sees every result in host
+//    memory.
 //
 // What constrains the chunks:
 //  - The dropout keep bit of (b, h, i, j) is drawn from a counter that holds
@@ -31,14 +32,16 @@
 //    batch on.
 //  - Without those, any run of consecutive heads is a valid chunk.
 //
-// The two internal streams and their events are created on a device's first
+// The three internal streams and their events are created on a device's first
 // call and kept until the process exits. Calls on one device are serialised
 // on the host while they enqueue work.
 #include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <initializer_list>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -161,8 +164,8 @@ Layout make_layout(int B, int N, int d, fa_dtype dtype, bool has_mask, bool has_
 // Per-device copy streams and the events that order the ring.
 struct DeviceCtx {
     bool ready = false;
-    cudaStream_t s_in = nullptr, s_out = nullptr;
-    cudaEvent_t ev_start = nullptr, ev_in_done = nullptr, ev_out_done = nullptr;
+    cudaStream_t s_in = nullptr, s_out = nullptr, s_comp = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_in_done = nullptr, ev_out_done = nullptr, ev_comp_done = nullptr;
     cudaEvent_t ev_qkv[kSlots] = {}, ev_do[kSlots] = {}, ev_fwd[kSlots] = {}, ev_bwd[kSlots] = {},
                 ev_out[kSlots] = {};
 };
@@ -172,17 +175,34 @@ DeviceCtx g_ctx[kMaxDevices];
 
 bool make_event(cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; }
 
-// The context of the current device, created on first use (under its lock).
+void destroy_ctx(DeviceCtx& c) {
+    for (cudaStream_t* st : {&c.s_in, &c.s_out, &c.s_comp})
+        if (*st) cudaStreamDestroy(*st);
+    for (cudaEvent_t* e : {&c.ev_start, &c.ev_in_done, &c.ev_out_done, &c.ev_comp_done})
+        if (*e) cudaEventDestroy(*e);
+    for (int s = 0; s < kSlots; ++s)
+        for (cudaEvent_t* e : {&c.ev_qkv[s], &c.ev_do[s], &c.ev_fwd[s], &c.ev_bwd[s], &c.ev_out[s]})
+            if (*e) cudaEventDestroy(*e);
+    c = DeviceCtx{};
+}
+
+// The context of the current device, created on first use (under its lock);
+// a failed creation releases what it made, so a later call starts afresh.
 DeviceCtx* device_ctx(int dev) {
     DeviceCtx& c = g_ctx[dev];
     if (c.ready) return &c;
-    if (cudaStreamCreateWithFlags(&c.s_in, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    if (cudaStreamCreateWithFlags(&c.s_out, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    if (!make_event(&c.ev_start) || !make_event(&c.ev_in_done) || !make_event(&c.ev_out_done)) return nullptr;
-    for (int s = 0; s < kSlots; ++s)
-        if (!make_event(&c.ev_qkv[s]) || !make_event(&c.ev_do[s]) || !make_event(&c.ev_fwd[s]) ||
-            !make_event(&c.ev_bwd[s]) || !make_event(&c.ev_out[s]))
-            return nullptr;
+    bool ok = cudaStreamCreateWithFlags(&c.s_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&c.s_out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&c.s_comp, cudaStreamNonBlocking) == cudaSuccess &&
+              make_event(&c.ev_start) && make_event(&c.ev_in_done) && make_event(&c.ev_out_done) &&
+              make_event(&c.ev_comp_done);
+    for (int s = 0; ok && s < kSlots; ++s)
+        ok = make_event(&c.ev_qkv[s]) && make_event(&c.ev_do[s]) && make_event(&c.ev_fwd[s]) &&
+             make_event(&c.ev_bwd[s]) && make_event(&c.ev_out[s]);
+    if (!ok) {
+        destroy_ctx(c);
+        return nullptr;
+    }
     c.ready = true;
     return &c;
 }
@@ -259,6 +279,7 @@ extern "C" int fa_fwd_bwd_host(const void* q, const void* k, const void* v, cons
     // (an earlier step may still be using the workspace)
     rc = from_cuda(cudaEventRecord(c->ev_start, cs), "record start");
     if (rc == FA_OK) rc = from_cuda(cudaStreamWaitEvent(c->s_in, c->ev_start, 0), "wait start");
+    if (rc == FA_OK) rc = from_cuda(cudaStreamWaitEvent(c->s_comp, c->ev_start, 0), "wait start");
     if (rc == FA_OK && kv_dev)
         rc = from_cuda(cudaMemcpyAsync(kv_dev, kv_len, (size_t)B * sizeof(int32_t), cudaMemcpyHostToDevice, c->s_in),
                        "copy kv_len");
@@ -294,20 +315,24 @@ extern "C" int fa_fwd_bwd_host(const void* q, const void* k, const void* v, cons
             rc = from_cuda(cudaMemcpyAsync(t[3], at(dO, off), bytes, cudaMemcpyHostToDevice, c->s_in), "copy dO");
         if (rc == FA_OK) rc = from_cuda(cudaEventRecord(c->ev_do[s], c->s_in), "record dO");
 
-        // compute on the caller's stream: the slot's outputs are free once
-        // the chunk that used the slot before has been copied out
-        if (rc == FA_OK) rc = from_cuda(cudaStreamWaitEvent(cs, c->ev_qkv[s], 0), "wait qkv");
-        if (rc == FA_OK && reuse) rc = from_cuda(cudaStreamWaitEvent(cs, c->ev_out[s], 0), "wait slot outputs");
+        // compute, alternately on the caller's stream and the second compute
+        // stream, so that a chunk's forward can start on the SMs the
+        // previous chunk's backward leaves idle as it finishes. The slot's
+        // outputs are free once the chunk that used the slot before has been
+        // copied out.
+        cudaStream_t ks = (i % 2 == 0) ? cs : c->s_comp;
+        if (rc == FA_OK) rc = from_cuda(cudaStreamWaitEvent(ks, c->ev_qkv[s], 0), "wait qkv");
+        if (rc == FA_OK && reuse) rc = from_cuda(cudaStreamWaitEvent(ks, c->ev_out[s], 0), "wait slot outputs");
         const int32_t* kv_chunk = kv_dev ? kv_dev + ch.b0 : nullptr;
         if (rc == FA_OK)
             rc = fa_fwd(t[0], t[1], t[2], t[4], lse_d, ch.B, ch.H, N, d, scale, causal, mask_dev, dropout_p, seed,
-                        dtype, kv_chunk, cs);
-        if (rc == FA_OK) rc = from_cuda(cudaEventRecord(c->ev_fwd[s], cs), "record fwd");
-        if (rc == FA_OK) rc = from_cuda(cudaStreamWaitEvent(cs, c->ev_do[s], 0), "wait dO");
+                        dtype, kv_chunk, ks);
+        if (rc == FA_OK) rc = from_cuda(cudaEventRecord(c->ev_fwd[s], ks), "record fwd");
+        if (rc == FA_OK) rc = from_cuda(cudaStreamWaitEvent(ks, c->ev_do[s], 0), "wait dO");
         if (rc == FA_OK)
             rc = fa_bwd(t[0], t[1], t[2], t[4], lse_d, t[3], t[5], t[6], t[7], ch.B, ch.H, N, d, scale, causal,
-                        mask_dev, dropout_p, seed, dtype, kv_chunk, bwd_ws, L.bwd_ws_bytes, cs);
-        if (rc == FA_OK) rc = from_cuda(cudaEventRecord(c->ev_bwd[s], cs), "record bwd");
+                        mask_dev, dropout_p, seed, dtype, kv_chunk, bwd_ws, L.bwd_ws_bytes, ks);
+        if (rc == FA_OK) rc = from_cuda(cudaEventRecord(c->ev_bwd[s], ks), "record bwd");
 
         // out: o and lse as soon as the forward is done, the gradients after
         // the backward
@@ -325,12 +350,16 @@ extern "C" int fa_fwd_bwd_host(const void* q, const void* k, const void* v, cons
         if (rc == FA_OK) rc = from_cuda(cudaEventRecord(c->ev_out[s], c->s_out), "record out");
     }
 
-    // join: the caller's stream waits for both copy streams, also after an
-    // error, so that nothing of this call is left unordered behind it
-    const int rc_in = from_cuda(cudaEventRecord(c->ev_in_done, c->s_in), "record in done");
-    const int rc_out = from_cuda(cudaEventRecord(c->ev_out_done, c->s_out), "record out done");
-    const int rc_j1 = rc_in == FA_OK ? from_cuda(cudaStreamWaitEvent(cs, c->ev_in_done, 0), "join in") : rc_in;
-    const int rc_j2 = rc_out == FA_OK ? from_cuda(cudaStreamWaitEvent(cs, c->ev_out_done, 0), "join out") : rc_out;
-    if (rc != FA_OK) return rc;
-    return rc_j1 != FA_OK ? rc_j1 : rc_j2;
+    // join: the caller's stream waits for the other three streams, also
+    // after an error, so that nothing of this call is left unordered behind
+    // it
+    int rc_join = FA_OK;
+    const std::pair<cudaStream_t, cudaEvent_t> joins[3] = {
+        {c->s_in, c->ev_in_done}, {c->s_comp, c->ev_comp_done}, {c->s_out, c->ev_out_done}};
+    for (const auto& j : joins) {
+        int r = from_cuda(cudaEventRecord(j.second, j.first), "record done");
+        if (r == FA_OK) r = from_cuda(cudaStreamWaitEvent(cs, j.second, 0), "join");
+        if (rc_join == FA_OK) rc_join = r;
+    }
+    return rc != FA_OK ? rc : rc_join;
 }
