@@ -30,12 +30,15 @@ CASES = [
                                         dropout_p=0.15), 1),
     ("d256_causal", Workload("h6", 0, B=1, H=4, N=260, d=256, dtype="bf16", causal=True), 1),
     ("fp32_d64", Workload("h7", 0, B=1, H=4, N=130, d=64, dtype="fp32", causal=True), 1),
+    ("one_row", Workload("h10", 0, B=2, H=2, N=1, d=64, dtype="bf16", causal=True), 1),
+    ("kvlen_one_head_batches", Workload("h11", 0, B=4, H=1, N=190, d=128, dtype="bf16", kv_len_range=(1, 190)), 1),
 ]
 
 
-def _host_step(inp, chunk_heads, device):
-    q = inp["q"].pin_memory()
-    k, v, do = (inp[n].pin_memory() for n in ("k", "v", "do"))
+def _host_step(inp, chunk_heads, device, pinned=True):
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t.contiguous())
+    q = pin(inp["q"])
+    k, v, do = (pin(inp[n]) for n in ("k", "v", "do"))
     o, lse, dq, dk, dv = fa.attention_fwd_bwd_host(
         q, k, v, do, scale=inp["scale"], causal=inp["causal"], block_mask=inp["block_mask"],
         dropout_p=inp["dropout_p"], seed=inp["seed"], kv_len=inp["kv_len"], chunk_heads=chunk_heads,
@@ -98,3 +101,16 @@ def test_back_to_back_calls_share_the_workspace(cuda_device):
     for inp, (_, res) in zip(inps, outs):
         got = {n: t.float().numpy().astype(np.float64) for n, t in zip(("o", "lse", "dq", "dk", "dv"), res)}
         compare(got, oracle_fwd_bwd(inp), "bf16")
+
+
+def test_pageable_host_memory(cuda_device):
+    """Pageable (not page-locked) host tensors: the driver stages the copies
+    and the call returns only after them, with the same results."""
+    w = Workload("h12", 0, B=1, H=5, N=200, d=128, dtype="bf16", causal=True)
+    inp = make_inputs(w, seed=33)
+    assert not inp["q"].is_pinned()
+    got = _host_step(inp, 1, cuda_device, pinned=False)
+    ref = _host_step(inp, 1, cuda_device, pinned=True)
+    for key in ("o", "lse", "dk", "dv"):
+        assert np.array_equal(got[key], ref[key], equal_nan=True), key
+    compare(got, oracle_fwd_bwd(inp), "bf16")
