@@ -360,10 +360,12 @@ def attention_fwd_bwd_host(q, k, v, do, scale=None, causal=False, block_mask=Non
             raise ValueError(f"{name} must be a contiguous CPU tensor [B,H,N,d]")
         if t.shape != q.shape or t.dtype != q.dtype:
             raise ValueError(f"{name} must match q in shape and dtype")
-    for name, t in (("block_mask", block_mask), ("kv_len", kv_len)):
-        if t is not None and (not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous()):
-            raise ValueError(f"{name} must be a contiguous CPU tensor")
     B, H, N, d = q.shape
+    nb = (N + 127) // 128
+    for name, t, dt, numel in (("block_mask", block_mask, torch.uint8, nb * nb), ("kv_len", kv_len, torch.int32, B)):
+        if t is not None and (not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous() or
+                              t.dtype != dt or t.numel() != numel):
+            raise ValueError(f"{name} must be a contiguous CPU {dt} tensor of {numel} elements")
     dt = _dtype_code(q)
     scale = (1.0 / d ** 0.5) if scale is None else float(scale)
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)

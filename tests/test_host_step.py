@@ -142,3 +142,18 @@ def test_argument_errors(kw, expect):
 
 def test_zero_length_is_a_noop():
     assert fa.fa_fwd_bwd_host(**_args(N=0, q=None, workspace=None)) == 0
+
+
+def test_binding_checks_host_tensors():
+    """attention_fwd_bwd_host refuses device tensors and masks of the wrong
+    type or size before calling the library."""
+    torch = pytest.importorskip("torch")
+    q = torch.zeros((1, 2, 130, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.attention_fwd_bwd_host(q, q, q, q.float())  # dO of another dtype
+    with pytest.raises(ValueError):
+        fa.attention_fwd_bwd_host(q, q, q, q, kv_len=torch.tensor([130], dtype=torch.int64))
+    with pytest.raises(ValueError):
+        fa.attention_fwd_bwd_host(q, q, q, q, kv_len=torch.tensor([130, 1], dtype=torch.int32))
+    with pytest.raises(ValueError):
+        fa.attention_fwd_bwd_host(q, q, q, q, block_mask=torch.ones(3, dtype=torch.uint8))
