@@ -257,6 +257,19 @@ def _check(t, name, like=None):
         raise ValueError(f"{name} must match q in shape and dtype")
 
 
+def _check_masks(block_mask, kv_len, B, N, device):
+    """The optional masks must be what the kernels read: block_mask uint8
+    [ceil(N/128)^2] and kv_len int32 [B], contiguous, on q's device."""
+    torch = _torch()
+    nb = (N + 127) // 128
+    for name, t, dt, numel in (("block_mask", block_mask, torch.uint8, nb * nb), ("kv_len", kv_len, torch.int32, B)):
+        if t is None:
+            continue
+        if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != device or not t.is_contiguous() or
+                t.dtype != dt or t.numel() != numel):
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor of {numel} elements on {device}")
+
+
 def _stream(stream):
     torch = _torch()
     s = torch.cuda.current_stream() if stream is None else stream
@@ -274,6 +287,7 @@ def attention_fwd(q, k, v, scale=None, causal=False, block_mask=None, dropout_p=
     _check(k, "k", q)
     _check(v, "v", q)
     B, H, N, d = q.shape
+    _check_masks(block_mask, kv_len, B, N, q.device)
     scale = (1.0 / d ** 0.5) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
@@ -312,6 +326,7 @@ def attention_fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, scale=None, 
     B, H, N, d = q8.shape
     if k8.shape != q8.shape or tuple(vt8.shape) != (B, H, d, N):
         raise ValueError("k8 must match q8 and vt8 must be [B,H,d,N]")
+    _check_masks(block_mask, kv_len, B, N, q8.device)
     scale = (1.0 / d ** 0.5) if scale is None else float(scale)
     o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
     l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
@@ -329,6 +344,7 @@ def attention_bwd(q, k, v, o, lse, do, scale=None, causal=False, block_mask=None
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _check(t, name, q)
     B, H, N, d = q.shape
+    _check_masks(block_mask, kv_len, B, N, q.device)
     scale = (1.0 / d ** 0.5) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk

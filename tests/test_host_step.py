@@ -157,3 +157,14 @@ def test_binding_checks_host_tensors():
         fa.attention_fwd_bwd_host(q, q, q, q, kv_len=torch.tensor([130, 1], dtype=torch.int32))
     with pytest.raises(ValueError):
         fa.attention_fwd_bwd_host(q, q, q, q, block_mask=torch.ones(3, dtype=torch.uint8))
+
+
+def test_device_binding_checks_masks():
+    """attention_fwd / attention_bwd refuse masks the kernels would misread
+    (wrong dtype, size or device) before calling the library."""
+    torch = pytest.importorskip("torch")
+    q = torch.zeros((1, 1, 300, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa._check_masks(torch.ones(3, 3, dtype=torch.uint8), None, 1, 300, q.device)  # a CPU mask
+    with pytest.raises(ValueError):
+        fa._check_masks(None, torch.tensor([300], dtype=torch.int64), 1, 300, q.device)
