@@ -168,3 +168,16 @@ def test_device_binding_checks_masks():
         fa._check_masks(torch.ones(3, 3, dtype=torch.uint8), None, 1, 300, q.device)  # a CPU mask
     with pytest.raises(ValueError):
         fa._check_masks(None, torch.tensor([300], dtype=torch.int64), 1, 300, q.device)
+
+
+@pytest.mark.parametrize("B,H,N", [(65535, 1, 128), (1, 65535, 64), (255, 257, 1)])
+@pytest.mark.parametrize("kv_len", [None, FAKE])
+def test_chunks_at_the_largest_head_counts(B, H, N, kv_len):
+    """B * H up to 65535 (the kernels' limit): one head per chunk, and the
+    library's own plan, still partition the heads; one more head is refused."""
+    for chunk_heads in (1, 0):
+        chunks = fa.fa_fwd_bwd_host_chunks(B, H, N, kv_len, 0.0, chunk_heads)
+        _check_partition(B, H, chunks, kv_len is not None, False)
+    with pytest.raises(fa.FaError):
+        fa.fa_fwd_bwd_host_chunks(B * H + 1, 1, N, kv_len, 0.0, 0)
+    assert fa.fa_fwd_bwd_host_workspace_size(B * H + 1, 1, N, 64, fa.FA_BF16, None, 0.0, kv_len, 0) == 0
