@@ -181,3 +181,16 @@ def test_chunks_at_the_largest_head_counts(B, H, N, kv_len):
     with pytest.raises(fa.FaError):
         fa.fa_fwd_bwd_host_chunks(B * H + 1, 1, N, kv_len, 0.0, 0)
     assert fa.fa_fwd_bwd_host_workspace_size(B * H + 1, 1, N, 64, fa.FA_BF16, None, 0.0, kv_len, 0) == 0
+
+
+def test_chunk_query_writes_at_most_max_chunks_records():
+    """fa_fwd_bwd_host_chunks returns the full count but writes only the
+    first max_chunks records of four ints, and accepts a NULL buffer."""
+    import ctypes
+    lib = fa.load_library()
+    n = lib.fa_fwd_bwd_host_chunks(2, 3, 300, None, 0.0, 1, None, 0)
+    assert n == 6
+    buf = (ctypes.c_int * (4 * 4))(*([-7] * 16))
+    assert lib.fa_fwd_bwd_host_chunks(2, 3, 300, None, 0.0, 1, buf, 2) == 6
+    assert list(buf[:8]) == [0, 1, 1, 0, 1, 1, 1, 0]
+    assert list(buf[8:]) == [-7] * 8
